@@ -1,0 +1,435 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused decode-batch QKV front on GB300.
+
+One step = one qkv_front call (projection + q/k RMS norm + RoPE + y store +
+paged K/V insert) over one batch of synthetic tokens.  Prints ONE JSON line
+(rank 0).  Metric: achieved HBM GB/s = algorithmic bytes of a call
+(W + x read, out + K/V written) / time per call; the line also carries
+us_per_call.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle on the same workload
+
+Timing: W is rotated over R device copies with R x |W| >= 3 x L2, so every
+call streams its weights from HBM; calls are captured in CUDA graphs (their
+PDL edges kept) and timed with CUDA events on the launching stream; the max
+over ranks is taken.  Multi-GPU runs are independent replicas (each rank one
+tensor-parallel shard of KV heads; no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from kv_insert_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "µs/call and achieved HBM GB/s (fraction of GB300 peak) at M=1..16, 1 GPU"
+UNIT = "GB/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCE = os.path.join(ROOT, "kv_insert_gb300", "csrc", "qkv_front.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "qkv_front_traffic.json")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=wl.BENCH_WORKLOAD, choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--graph-calls", type=int, default=96,
+                    help="calls per captured CUDA graph (a multiple of the W copies is used)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-seconds", type=float, default=90.0,
+                    help="target duration of the whole --impl reference run")
+    a = ap.parse_args(argv)
+    if a.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if a.steps < 1:
+        ap.error("--steps must be >= 1")
+    return a
+
+
+# ---- distributed plumbing (host side) ------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(backend: str):
+    world, rank, _ = dist_env()
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+    return world, rank
+
+
+def barrier():
+    if torch.distributed.is_initialized():
+        torch.distributed.barrier()
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    """The maximum of a per-rank float over all ranks (the job's wall time)."""
+    if not torch.distributed.is_initialized():
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(bytes_per_step: int, steps: int, world: int, seconds_max: float) -> dict:
+    """Whole-job throughput: units all ranks processed / the slowest rank's time."""
+    us = seconds_max / steps * 1e6
+    gbs = bytes_per_step * steps * world / seconds_max / 1e9
+    return {"value": gbs, "us_per_call": us, "ms_per_step": us / 1e3}
+
+
+# ---- peaks, traffic, clocks --------------------------------------------------
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            v = float(json.load(fh)["hbm_gbs"])
+        return v, "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    for f in (KERNEL_SOURCE, os.path.join(ROOT, "include", "qkvfront.h")):
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    this exact kernel source and workload; else None."""
+    try:
+        with open(TRAFFIC_FILE) as fh:
+            rec = json.load(fh)
+    except (OSError, ValueError):
+        return None
+    if rec.get("source_sha256") != source_digest():
+        return None
+    per = rec.get("per_workload", {}).get(workload)
+    return None if per is None else float(per["dram_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the GPU works."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.strip()]
+        self.file.close()
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [c.strip() for c in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, r[5:9]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        busy = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---- the CPU oracle (baseline and reference arm) ---------------------------
+
+def oracle_unit_inputs(inp: dict, w: wl.Workload, t: int, g: int):
+    """One token and one KV-head group of the workload: the rows of W that KV
+    head g owns ([q heads 8g..8g+7 | k head g | v head g | gate heads
+    8g..8g+7]), i.e. one tensor-parallel shard, and token t."""
+    nkv = w.num_kv_heads
+    heads = (list(range(8 * g, 8 * g + 8)) + [8 * nkv + g, 9 * nkv + g]
+             + list(range(10 * nkv + 8 * g, 10 * nkv + 8 * g + 8)))
+    rows = np.concatenate([np.arange(h * 64, h * 64 + 64) for h in heads])
+    Wb = wl.bits(inp["W"])[rows]
+    return (wl.bits(inp["x"])[t: t + 1], np.ascontiguousarray(Wb),
+            inp["positions"].numpy()[t: t + 1], np.array([0], np.int64))
+
+
+def time_oracle_units(inp, w, units: int):
+    """Run `units` (token, KV group) oracle calls; returns seconds."""
+    import oracle
+    cs = inp["cos_sin"].numpy()
+    cache = np.zeros((1, 1, 16, 128), np.uint16)
+    n_units = w.M * w.num_kv_heads
+    prepared = [oracle_unit_inputs(inp, w, u % w.M, (u // w.M) % w.num_kv_heads)
+                for u in range(min(units, n_units))]
+    t0 = time.perf_counter()
+    for u in range(units):
+        x, Wb, pos, sl = prepared[u % len(prepared)]
+        _, err = oracle.qkv_front(x, Wb, pos, sl, cs, cache, 1)
+        if err:
+            raise RuntimeError(f"oracle error {err}")
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(inp, w, seconds: float) -> dict:
+    """The oracle, as it stands, on host cores: whole calls of the workload
+    until `seconds` of CPU work (at least one)."""
+    import oracle
+    cs = inp["cos_sin"].numpy()
+    xb, Wb = wl.bits(inp["x"]), wl.bits(inp["W"])
+    pos, sl = inp["positions"].numpy(), inp["slots"].numpy()
+    cache = wl.bits(inp["kv_cache"]).copy()
+    calls, t0 = 0, time.perf_counter()
+    while True:
+        _, err = oracle.qkv_front(xb, Wb, pos, sl, cs, cache, w.num_kv_heads)
+        if err:
+            raise RuntimeError(f"oracle error {err}")
+        calls += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return {"value": w.roofline_bytes() * calls / el / 1e9, "unit": UNIT, "cores": 1,
+            "kind": "oracle",
+            "sample": f"{calls} whole calls of {w.name} (single-threaded C oracle), {el:.1f} s"}
+
+
+def run_reference(args, w: wl.Workload):
+    world, rank = dist_init("gloo")
+    if rank != 0:
+        return None
+    inp = wl.make_inputs(w)
+    n_units = w.M * w.num_kv_heads
+    unit_bytes = w.roofline_bytes() / n_units
+    t_unit = time_oracle_units(inp, w, 1)
+    units_per_step = int(max(1, min(n_units, args.ref_seconds / ((args.steps + args.warmup) * t_unit))))
+    time_oracle_units(inp, w, units_per_step * args.warmup)
+    el = time_oracle_units(inp, w, units_per_step * args.steps)
+    value = unit_bytes * units_per_step * args.steps / el / 1e9
+    sample = (f"each step: {units_per_step} of the {n_units} (token, KV-head group) units of "
+              f"{w.name} through the single-threaded C oracle")
+    cfg = w.describe()
+    cfg.update({"l2": "n/a (host)", "units_per_step": units_per_step})
+    return {"metric": METRIC, "value": value, "unit": UNIT, "impl": "reference",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+# ---- our arm ----------------------------------------------------------------
+
+def run_ours(args, w: wl.Workload):
+    from kv_insert_gb300 import qkv_front as qf
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU (the product path has no CPU fallback)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_init("nccl")
+    qf.load()
+
+    inp = wl.make_inputs(w)
+    g = {k: v.to(dev) for k, v in inp.items()}
+    M, N, nkv = w.M, w.N, w.num_kv_heads
+    qf.prepare(N, nkv)
+    tiles, stages, splits, _ = qf.variant(N, M)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    w_bytes = N * wl.HIDDEN * 2
+    copies = max(2, math.ceil(3 * l2 / w_bytes))
+    Ws = [g["W"]] + [g["W"].clone() for _ in range(copies - 1)]
+    torch.cuda.synchronize(dev)   # W is read before the PDL wait: no writer may be in flight
+    out = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    per_graph = max(copies, (args.graph_calls // copies) * copies)
+
+    def call(i):
+        qf.launch(g["x"], Ws[i % copies], g["positions"], g["slots"], g["cos_sin"],
+                  g["kv_cache"], out)
+
+    def capture(n, start):
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(n):
+                call(start + i)
+        return graph
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            call(i)
+    stream.synchronize()
+    assert qf.status() == 0, "device status raised during warm-up"
+    full, rem = divmod(args.steps, per_graph)
+    g_full = capture(per_graph, 0) if full else None
+    g_rem = capture(rem, 0) if rem else None
+    # graph upload before timing (part of set-up, not a timed step)
+    with torch.cuda.stream(stream):
+        if g_full:
+            g_full.replay()
+        if g_rem:
+            g_rem.replay()
+    stream.synchronize()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(full):
+            g_full.replay()
+        if g_rem:
+            g_rem.replay()
+        end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clocks = sampler.stop()
+    el = start.elapsed_time(end) / 1e3
+    st = qf.status()
+    if st:
+        raise RuntimeError(f"device status {st:#x} raised in the timed region")
+    el_max = max_over_ranks(el, dev)
+    res = aggregate(w.roofline_bytes(), args.steps, world, el_max)
+
+    # end to end through the public API: pinned host inputs -> device, the call,
+    # device -> pinned host result, every step
+    e2e = None
+    if not args.no_e2e:
+        xh = inp["x"].pin_memory()
+        ph = inp["positions"].pin_memory()
+        sh = inp["slots"].pin_memory()
+        oh = torch.empty(M, N, dtype=torch.bfloat16).pin_memory()
+        xd, pd, sd = torch.empty_like(g["x"]), torch.empty_like(g["positions"]), torch.empty_like(g["slots"])
+
+        def e2e_step(i):
+            xd.copy_(xh, non_blocking=True)
+            pd.copy_(ph, non_blocking=True)
+            sd.copy_(sh, non_blocking=True)
+            qf.qkv_front(xd, Ws[i % copies], pd, sd, g["cos_sin"], g["kv_cache"], out)
+            oh.copy_(out, non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup):
+                e2e_step(i)
+        stream.synchronize()
+        e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize(dev)
+        with torch.cuda.stream(stream):
+            e_start.record(stream)
+            for i in range(args.steps):
+                e2e_step(i)
+            e_end.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        e_el = max_over_ranks(e_start.elapsed_time(e_end) / 1e3, dev)
+        e_res = aggregate(w.roofline_bytes(), args.steps, world, e_el)
+        e2e = {"value": e_res["value"], "unit": UNIT, "us_per_call": e_res["us_per_call"],
+               "h2d_bytes_per_step": xh.numel() * 2 + ph.numel() * 8 + sh.numel() * 8,
+               "d2h_bytes_per_step": oh.numel() * 2}
+        if qf.status():
+            raise RuntimeError("device status raised in the end-to-end leg")
+
+    if rank != 0:
+        return None
+    peak, peak_kind = hbm_peak()
+    bytes_call = w.roofline_bytes()
+    achieved = bytes_call / (el_max / args.steps) / 1e9
+    traffic = recorded_traffic(w.name)
+    line = {
+        "metric": METRIC, "value": res["value"], "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
+        "us_per_call": res["us_per_call"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": dict(w.describe(), **{
+            "variant": {"tiles": tiles, "stages": stages, "splits": splits},
+            "l2": f"inputs larger than L2: W rotated over {copies} copies of {w_bytes / 1e6:.1f} MB "
+                  f"(L2 {l2 / 1e6:.1f} MB)",
+            "graph_calls": per_graph, "parallelism": f"replicas x{world}"}),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "traffic": traffic, "bytes_per_launch": bytes_call,
+                     "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(inp, w, args.cpu_seconds)
+    return line
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    w = wl.WORKLOADS[args.workload]
+    line = run_reference(args, w) if args.impl == "reference" else run_ours(args, w)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if torch.distributed.is_initialized():
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,163 @@
+/*
+ * libqkvfront: the decode-batch attention front on one GB300 (sm_103a).
+ *
+ * Defined by the API pages of vllm.models.muse_spark.nvidia.specialized_decode:
+ *   "cutedsl.attention.qkv_front" (module docstring; functions qkv_front,
+ *   launch, unsupported, prepare, variant, hidden_rows_ok,
+ *   kv_cache_layout_ok, supports_shape) and "runtime.cute_ops" (split_qkv,
+ *   supports_call, unsupported_projection, attn2 paragraph for the cache).
+ *
+ * For 1 <= M <= 16 tokens one launch computes
+ *     out[M, N] = bf16( x[M, 8192] @ W[N, 8192]^T )       (FP32 accumulation)
+ * over packed rows [q | k | v | gate] (8 q heads, 1 k head, 1 v head and 8
+ * gate heads of 64 columns per KV head, so N = 1152 * num_kv_heads), then for
+ * each 64-wide q and k head the weightless RMS norm (eps 1e-6) and the
+ * interleaved RoPE (pairs 2i, 2i+1; cos in table column i, sin in 32 + i) of
+ * the token's position, stores the row in `out`, and writes each token's
+ * k head g into the K half (elements 0..63) and v head g into the V half
+ * (64..127) of cache slot `slots[t]` (page slot / 16, offset slot % 16) of KV
+ * head g.  v and gate columns of `out` hold the rounded projection.
+ *
+ * Conventions of every entry point below:
+ *   - bf16 arrays are passed as uint16_t bit patterns; all arrays are
+ *     row-major and contiguous; all pointers are DEVICE pointers owned by the
+ *     caller and must be 16-byte aligned;
+ *   - the library allocates no device memory per call and keeps no state
+ *     across calls except a device status word (qkv_front_status);
+ *   - `stream` is a cudaStream_t (NULL: the legacy default stream); calls are
+ *     asynchronous on it.  The kernel is launched with programmatic stream
+ *     serialization (PDL): it may start while the previous kernel on the
+ *     stream runs, reads only W before it waits for that kernel, and reads
+ *     x / positions / slots / cos_sin and writes out / kv_cache after;
+ *     so W must not be written by a kernel that may still be running when
+ *     the call is launched (weights are written at load time only);
+ *   - return value 0 (QKVF_OK) or a QKVF_ERR_* code; nothing is launched
+ *     when a code is returned.  qkv_front_strerror gives its text.
+ */
+#ifndef QKVFRONT_H
+#define QKVFRONT_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- return codes -------------------------------------------------------- */
+#define QKVF_OK 0
+#define QKVF_ERR_TOKENS 1        /* M outside 0..16 */
+#define QKVF_ERR_SHAPE 2         /* num_kv_heads < 1 or N != 1152 * num_kv_heads */
+#define QKVF_ERR_NULL 3          /* a required pointer is NULL */
+#define QKVF_ERR_ALIGN 4         /* a pointer is not 16-byte aligned */
+#define QKVF_ERR_DEVICE 5        /* the current device is not compute capability 10.3 */
+#define QKVF_ERR_CUDA 6          /* a CUDA runtime/driver call failed */
+#define QKVF_ERR_SIZES 7         /* cos_sin_rows < 1, num_pages < 1, or too large */
+#define QKVF_ERR_VARIANT 8       /* an explicit variant that this shape cannot use */
+#define QKVF_ERR_ARG 9           /* any other bad argument */
+
+/* ---- device status bits (qkv_front_status) ------------------------------- */
+#define QKVF_STATUS_BAD_SLOT 1u      /* a slot >= num_pages * 16: that token's insert skipped */
+#define QKVF_STATUS_BAD_POSITION 2u  /* a position outside [0, cos_sin_rows): its q/k heads and insert skipped */
+#define QKVF_STATUS_WAIT_TIMEOUT 4u  /* a bounded wait in the kernel gave up: outputs of that call are invalid */
+
+/*
+ * qkv_front: check the call, then launch the fused front.
+ *   x          [M, 8192] bf16 bits.  The attention input.
+ *   W          [N, 8192] bf16 bits.  Unquantized, bias-free QKV + o-gate weight.
+ *   positions  [M] int64.  Token positions; each must be in [0, cos_sin_rows).
+ *   slots      [M] int64.  Cache slot of each token (page * 16 + offset);
+ *              a negative slot means "no insert" (padding token); a slot
+ *              >= num_pages * 16 is skipped and flagged QKVF_STATUS_BAD_SLOT.
+ *   cos_sin    [cos_sin_rows, 64] fp32.  Row p: cos(p f_i) in column i,
+ *              sin(p f_i) in column 32 + i (interleaved, not neox style).
+ *   out        [M, N] bf16 bits, written.
+ *   kv_cache   [num_pages, num_kv_heads, 16, 128] bf16 bits; only the named
+ *              slots change.
+ *   M          0..16 tokens (M == 0 launches nothing and returns QKVF_OK).
+ *   N          1152 * num_kv_heads.
+ * Tokens must name distinct slots (two tokens writing one slot race).
+ * x, W and cos_sin must not overlap out or kv_cache.
+ */
+int qkv_front(const uint16_t *x, const uint16_t *W, const int64_t *positions,
+              const int64_t *slots, const float *cos_sin, int64_t cos_sin_rows,
+              uint16_t *out, uint16_t *kv_cache, int64_t num_pages, int M, int N,
+              int num_kv_heads, void *stream);
+
+/*
+ * qkv_front_unsupported: why qkv_front would refuse this call, or NULL when
+ * it takes it (page qkv_front, function unsupported).  Host-only checks, no
+ * CUDA call except the device query.  Returns a static string.
+ */
+const char *qkv_front_unsupported(const uint16_t *x, const uint16_t *W, const int64_t *positions,
+                                  const int64_t *slots, const float *cos_sin,
+                                  int64_t cos_sin_rows, uint16_t *out, uint16_t *kv_cache,
+                                  int64_t num_pages, int M, int N, int num_kv_heads);
+
+/*
+ * qkv_front_launch: qkv_front without its argument checks, for a call that
+ * qkv_front_unsupported already accepted (page qkv_front, function launch).
+ * Out-of-contract arguments here are undefined behaviour.
+ */
+int qkv_front_launch(const uint16_t *x, const uint16_t *W, const int64_t *positions,
+                     const int64_t *slots, const float *cos_sin, int64_t cos_sin_rows,
+                     uint16_t *out, uint16_t *kv_cache, int64_t num_pages, int M, int N,
+                     int num_kv_heads, void *stream);
+
+/*
+ * qkv_front_variant: the launch shape qkv_front uses for N columns and M
+ * tokens on the current device (page qkv_front, function variant):
+ *   *tiles  8-token column tiles (1 or 2),
+ *   *stages depth of the shared-memory weight ring,
+ *   *splits CTAs per head (the cluster size; K is split cyclically among them).
+ * Any output pointer may be NULL.  The result of the op depends on `splits`
+ * only (the K split fixes the summation order); `stages` never changes it.
+ */
+int qkv_front_variant(int N, int M, int *tiles, int *stages, int *splits);
+
+/*
+ * qkv_front_launch_variant: qkv_front (with its checks) at an explicit
+ * variant, for tests and tuning.  splits in {1, 2, 4, 8, 16}; stages >= 2
+ * and within the shared-memory limit; otherwise QKVF_ERR_VARIANT.
+ */
+int qkv_front_launch_variant(const uint16_t *x, const uint16_t *W, const int64_t *positions,
+                             const int64_t *slots, const float *cos_sin,
+                             int64_t cos_sin_rows, uint16_t *out, uint16_t *kv_cache,
+                             int64_t num_pages, int M, int N, int num_kv_heads, int splits,
+                             int stages, void *stream);
+
+/*
+ * qkv_front_prepare: set the kernel attributes (dynamic shared memory,
+ * non-portable cluster size) of the variants that N columns take, so that
+ * later calls can be captured in a CUDA graph (page qkv_front, function
+ * prepare).  Calls made without it prepare themselves on first use.
+ */
+int qkv_front_prepare(int N, int num_kv_heads);
+
+/*
+ * qkv_front_status: copy the device status word (an OR of QKVF_STATUS_* bits
+ * raised by calls since the last read) into *bits and clear it.
+ * Synchronizes the current device.
+ */
+int qkv_front_status(unsigned int *bits);
+
+/* Static text of a QKVF_* return code. */
+const char *qkv_front_strerror(int code);
+
+/*
+ * qkv_front_selftest_wait: launch a one-CTA kernel that waits, through the
+ * same bounded shared-memory barrier wait the front uses, on a barrier that
+ * nothing completes, for at most timeout_ns nanoseconds (1..10^9); it then
+ * raises QKVF_STATUS_WAIT_TIMEOUT and returns.  Tests that the kernel's waits
+ * end without hanging the GPU.
+ */
+int qkv_front_selftest_wait(int64_t timeout_ns, void *stream);
+
+/* Bounded-wait limit of the front's barrier waits in nanoseconds
+ * (default 2e9); values outside 1e3..1e10 are refused with QKVF_ERR_ARG. */
+int qkv_front_set_wait_limit(int64_t ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QKVFRONT_H */

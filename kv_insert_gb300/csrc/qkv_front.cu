@@ -1,0 +1,949 @@
+// libqkvfront: the decode-batch QKV front as one sm_103a kernel.
+//
+// What it computes is stated in include/qkvfront.h.  Sources: the API pages
+// "vllm.models.muse_spark.nvidia.specialized_decode.cutedsl.attention.qkv_front"
+// (module docstring: projection, weightless RMS norm, interleaved RoPE, y
+// store, paged K/V insert in one launch; summaries of QkvFrontKernel.produce,
+// consume, aux, send, finish) and "...runtime.cute_ops" (split_qkv row
+// layout, supports_call, unsupported_projection; attn2 paragraph for the
+// cache layout).
+//
+// Kernel design (one CTA per head and K split, a cluster per head when K is
+// split):
+//   - grid (splits, N / 64); CTA (r, h) owns head h (W rows 64h..64h+63) and
+//     the K stages r, r + splits, r + 2 splits, ... (cyclic stripes);
+//   - warp 4 lane 0 (producer) streams 64 x 64 bf16 W boxes and the matching
+//     token x 64 x boxes into a `stages`-deep shared-memory ring with TMA
+//     (128-byte swizzle), issuing the first ring's worth of W before the PDL
+//     wait (W is never written by a kernel in flight);
+//   - warps 0..3 (consumers) run mma.sync m16n8k16 bf16 -> fp32 with the W
+//     rows as the M side (16 rows per warp) and the tokens as the N side
+//     (one or two 8-token tiles), reading fragments with ldmatrix;
+//   - warp 5 (aux) loads the tokens' positions, slots and cos|sin rows after
+//     the PDL wait and checks them against the table and cache sizes;
+//   - the FP32 partials go to shared memory; with splits > 1 the owner CTA of
+//     token t (cluster rank t % splits) reads all ranks' partials through
+//     distributed shared memory and sums them in rank order 0, 1, ..., so the
+//     result depends only on the launch shape (no atomics, no global
+//     scratch);
+//   - the epilogue rounds to BF16, norms and rotates q and k heads (one lane
+//     per RoPE pair), stores the row and writes K / V into the paged cache.
+//
+// Every shared-memory barrier wait is bounded in time: on expiry the CTA
+// raises QKVF_STATUS_WAIT_TIMEOUT in a device status word, stops waiting,
+// drains its own copies in flight and exits normally.
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "qkvfront.h"
+
+namespace qkvf {
+
+constexpr int kHidden = 8192;        // hidden size (page qkv_front, hidden_rows_ok: [rows, 8192])
+constexpr int kHeadDim = 64;         // one head = 64 output columns (module docstring)
+constexpr int kQPerKv = 8;           // q (and gate) heads per KV head (cute_ops, split_qkv)
+constexpr int kPageSlots = 16;       // cache [pages, num_kv_heads, 16, 128] (cute_ops, attn2)
+constexpr int kSlotWidth = 128;      // K | V per slot
+constexpr int kMaxTokens = 16;       // 1 <= M <= 16 (module docstring)
+constexpr int kBoxK = 64;            // k per TMA box row: 128 bytes = one swizzle row
+constexpr int kBoxBytesW = 64 * 128; // W box: 64 rows x 128 bytes
+constexpr int kConsumerWarps = 4;
+constexpr int kProducerWarp = 4;
+constexpr int kAuxWarp = 5;
+constexpr int kWarps = 6;
+constexpr int kThreads = kWarps * 32;
+constexpr int kPartStride = 68;      // floats per token row of the partial (64 + 4: no bank conflicts)
+constexpr float kEps = 1e-6f;
+constexpr int kMaxSmemPerCta = 232448;   // 227 KB opt-in limit
+constexpr int kSmemPerSm = 233472;       // 228 KB per SM
+constexpr int kSmemReservedPerCta = 1024;
+
+enum HeadKind { kQ = 0, kK = 1, kV = 2, kGate = 3 };
+
+__device__ unsigned int g_status;
+
+struct FrontParams {
+    const int64_t *positions;
+    const int64_t *slots;
+    const float *cos_sin;
+    uint16_t *out;
+    uint16_t *kv_cache;
+    int64_t cos_rows;
+    int64_t num_pages;
+    unsigned long long wait_limit_ns;
+    int M;
+    int N;
+    int nkv;
+    int splits;
+    int stages;
+};
+
+// Shared-memory layout of one CTA, from the base (1024-byte aligned).
+struct Layout {
+    uint32_t w, x, full, empty, part, pos, slot, cs, flag, abort_flag, total;
+};
+
+__host__ __device__ inline Layout layout_of(int mt, int kb, int stages)
+{
+    Layout L;
+    uint32_t off = 0;
+    L.w = off;
+    off += (uint32_t)stages * kb * kBoxBytesW;
+    L.x = off;
+    off += (uint32_t)stages * kb * mt * 128;
+    L.full = off;
+    off += (uint32_t)stages * 8;
+    L.empty = off;
+    off += (uint32_t)stages * 8;
+    off = (off + 15u) & ~15u;
+    L.part = off;
+    off += (uint32_t)mt * kPartStride * 4;
+    L.pos = off;
+    off += kMaxTokens * 8;
+    L.slot = off;
+    off += kMaxTokens * 8;
+    L.cs = off;
+    off += kMaxTokens * kHeadDim * 4;
+    L.flag = off;
+    off += kMaxTokens * 4;
+    L.abort_flag = off;
+    off += 16;
+    L.total = off;
+    return L;
+}
+
+// dynamic shared memory to request: the layout plus slack to align the base
+__host__ __device__ inline uint32_t smem_bytes(int mt, int kb, int stages)
+{
+    return layout_of(mt, kb, stages).total + 1024;
+}
+
+// ---- PTX helpers -----------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait until the barrier's phase with this parity completes, for at most
+// limit_ns.  On expiry: raise the status bit, set the CTA's abort flag and
+// return false.  With `honour_abort`, also return false as soon as another
+// thread of the CTA has aborted.
+__device__ __noinline__ bool bounded_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                          unsigned long long limit_ns, bool honour_abort)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long start = global_ns();
+    while (true) {
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (honour_abort && *abort_flag) return false;
+        if (global_ns() - start > limit_ns) {
+            *abort_flag = 1;
+            atomicOr(&g_status, QKVF_STATUS_WAIT_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void griddep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ void tma_prefetch_map(const CUtensorMap *m)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
+
+// 2-D tiled TMA load of one box into shared memory, completing on `bar`.
+// c0 is the innermost (k) coordinate in elements: always a multiple of 64
+// here, so the 16-byte rule on the inner coordinate holds.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *m, uint32_t bar,
+                                            int c0, int c1, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                        uint32_t &r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t &r0, uint32_t &r1)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];"
+                 : "=r"(r0), "=r"(r1)
+                 : "r"(addr));
+}
+
+// D(16x8, fp32) += A(16x16, bf16, row) * B(16x8, bf16, col)
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile(
+        "barrier.cluster.arrive.release.aligned;\n"
+        "barrier.cluster.wait.acquire.aligned;\n" ::
+            : "memory");
+}
+
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ float2 ld_cluster_f2(uint32_t addr)
+{
+    float2 v;
+    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(__nv_bfloat16 lo, __nv_bfloat16 hi)
+{
+    return (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
+}
+
+// ---- the front kernel ------------------------------------------------------
+
+template <int MT, int KB>
+__global__ void __launch_bounds__(kThreads, 1)
+    qkv_front_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                     const FrontParams p)
+{
+    constexpr int NT = MT / 8;                       // 8-token mma column tiles
+    constexpr uint32_t kBoxBytesX = MT * 128;
+    constexpr uint32_t kStageTx = KB * (kBoxBytesW + kBoxBytesX);
+    constexpr int kStepsAll = kHidden / (kBoxK * KB);
+
+    extern __shared__ uint8_t smem_dyn[];
+    uint8_t *smem = smem_dyn + ((1024u - (smem_u32(smem_dyn) & 1023u)) & 1023u);
+    const Layout L = layout_of(MT, KB, p.stages);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int S = p.splits;
+    const uint32_t rank = S > 1 ? cluster_rank() : 0u;
+    const int head = blockIdx.y;
+    const int steps = kStepsAll / S;
+    const int stages = p.stages;
+
+    const uint32_t sW = smem_u32(smem + L.w);
+    const uint32_t sX = smem_u32(smem + L.x);
+    const uint32_t full0 = smem_u32(smem + L.full);
+    const uint32_t empty0 = smem_u32(smem + L.empty);
+    float *part = reinterpret_cast<float *>(smem + L.part);
+    int64_t *s_pos = reinterpret_cast<int64_t *>(smem + L.pos);
+    int64_t *s_slot = reinterpret_cast<int64_t *>(smem + L.slot);
+    float *s_cs = reinterpret_cast<float *>(smem + L.cs);
+    int *s_flag = reinterpret_cast<int *>(smem + L.flag);
+    volatile int *s_abort = reinterpret_cast<volatile int *>(smem + L.abort_flag);
+
+    const int q_heads = kQPerKv * p.nkv;
+    const int kind = head < q_heads ? kQ : head < q_heads + p.nkv ? kK
+                   : head < q_heads + 2 * p.nkv ? kV : kGate;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, kConsumerWarps);
+        }
+        *s_abort = 0;
+        fence_barrier_init();
+        // Dependents may launch now: before their own PDL wait they read only
+        // their weights, which this kernel never writes.
+        griddep_launch_dependents();
+    }
+    __syncthreads();
+
+    if (warp == kProducerWarp) {
+        // ---- produce: the W / x ring ------------------------------------
+        if (lane == 0) {
+            const uint64_t pol_w = policy_evict_first();   // streamed once
+            const uint64_t pol_x = policy_evict_last();    // re-read by every CTA
+            tma_prefetch_map(&tmW);
+            tma_prefetch_map(&tmX);
+            const int row0 = head * kHeadDim;
+            const int npre = steps < stages ? steps : stages;
+            for (int i = 0; i < npre; ++i) {
+                const int j = (int)rank + i * S;
+                mbar_expect_tx(full0 + 8 * i, kStageTx);
+                for (int b = 0; b < KB; ++b)
+                    tma_load_2d(sW + (uint32_t)(i * KB + b) * kBoxBytesW, &tmW, full0 + 8 * i,
+                                (j * KB + b) * kBoxK, row0, pol_w);
+            }
+            griddep_wait();   // x is written by the kernel before this one
+            for (int i = 0; i < npre; ++i) {
+                const int j = (int)rank + i * S;
+                for (int b = 0; b < KB; ++b)
+                    tma_load_2d(sX + (uint32_t)(i * KB + b) * kBoxBytesX, &tmX, full0 + 8 * i,
+                                (j * KB + b) * kBoxK, 0, pol_x);
+            }
+            int issued = npre;
+            int s = npre == stages ? 0 : npre;
+            int use = npre == stages ? 1 : 0;   // how many times slot s was filled before
+            for (int i = npre; i < steps; ++i) {
+                if (!bounded_wait(empty0 + 8 * s, (uint32_t)((use - 1) & 1), s_abort,
+                                  p.wait_limit_ns, true))
+                    break;
+                const int j = (int)rank + i * S;
+                mbar_expect_tx(full0 + 8 * s, kStageTx);
+                for (int b = 0; b < KB; ++b) {
+                    tma_load_2d(sW + (uint32_t)(s * KB + b) * kBoxBytesW, &tmW, full0 + 8 * s,
+                                (j * KB + b) * kBoxK, row0, pol_w);
+                    tma_load_2d(sX + (uint32_t)(s * KB + b) * kBoxBytesX, &tmX, full0 + 8 * s,
+                                (j * KB + b) * kBoxK, 0, pol_x);
+                }
+                ++issued;
+                if (++s == stages) {
+                    s = 0;
+                    ++use;
+                }
+            }
+            if (*s_abort) {
+                // drain: every copy this CTA issued lands before it exits
+                const int first = issued > stages ? issued - stages : 0;
+                for (int i = first; i < issued; ++i)
+                    bounded_wait(full0 + 8 * (i % stages), (uint32_t)((i / stages) & 1), s_abort,
+                                 p.wait_limit_ns, false);
+            }
+        }
+        __syncwarp();
+        griddep_wait();
+    } else if (warp == kAuxWarp) {
+        // ---- aux: the epilogue's per-token inputs -------------------------
+        griddep_wait();
+        if (lane < p.M) {
+            const int64_t pos = p.positions[lane];
+            const int64_t slot = p.slots[lane];
+            const bool pos_ok = pos >= 0 && pos < p.cos_rows;
+            const bool slot_over = slot >= p.num_pages * kPageSlots;
+            const bool insert = slot >= 0 && !slot_over && pos_ok;
+            s_pos[lane] = pos;
+            s_slot[lane] = slot;
+            s_flag[lane] = (pos_ok ? 1 : 0) | (insert ? 2 : 0);
+            const unsigned bad = (pos_ok ? 0u : QKVF_STATUS_BAD_POSITION) |
+                                 (slot_over ? QKVF_STATUS_BAD_SLOT : 0u);
+            if (bad && head == 0 && rank == 0) atomicOr(&g_status, bad);
+        }
+        __syncwarp();
+        if (kind == kQ || kind == kK) {
+            for (int t = (int)rank; t < p.M; t += S) {
+                if (!(s_flag[t] & 1)) continue;
+                const float2 v =
+                    reinterpret_cast<const float2 *>(p.cos_sin + s_pos[t] * kHeadDim)[lane];
+                reinterpret_cast<float2 *>(s_cs + t * kHeadDim)[lane] = v;
+            }
+        }
+    } else {
+        // ---- consume: mma.sync over the ring ------------------------------
+        griddep_wait();
+        float acc[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) acc[nt][r] = 0.f;
+
+        // ldmatrix row addresses.  A: lane l feeds row (l & 7) + 8 ((l >> 3) & 1)
+        // of this warp's 16 W rows, 16-byte chunk (l >> 4) of the k16 step.
+        // B: lane l feeds token (l & 7) (+ 8 (l >> 4) with two tiles), chunk
+        // ((l >> 3) & 1).  The 128-byte swizzle XORs the chunk with row % 8.
+        const uint32_t a_row = (uint32_t)(warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8);
+        const uint32_t a_off = a_row * 128u;
+        const uint32_t a_hi = (uint32_t)(lane >> 4);
+        const uint32_t b_tok = NT == 2 ? (uint32_t)((lane & 7) + ((lane >> 4) << 3))
+                                       : (uint32_t)(lane & 7);
+        const uint32_t b_off = b_tok * 128u;
+        const uint32_t b_hi = (uint32_t)((lane >> 3) & 1);
+        const uint32_t sw = (uint32_t)(lane & 7);   // row % 8 for both operands
+
+        int s = 0;
+        uint32_t phase = 0;
+        for (int i = 0; i < steps; ++i) {
+            // every lane waits (each gets the barrier's acquire); the warp
+            // then agrees, so ldmatrix / mma always run on a converged warp
+            const bool landed = bounded_wait(full0 + 8 * s, phase, s_abort, p.wait_limit_ns, true);
+            if (__all_sync(0xffffffffu, landed)) {
+#pragma unroll
+                for (int b = 0; b < KB; ++b) {
+                    const uint32_t wbox = sW + (uint32_t)(s * KB + b) * kBoxBytesW;
+                    const uint32_t xbox = sX + (uint32_t)(s * KB + b) * kBoxBytesX;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        uint32_t a0, a1, a2, a3;
+                        ldsm_x4(wbox + a_off + ((((uint32_t)(2 * kk) + a_hi) ^ sw) << 4), a0, a1,
+                                a2, a3);
+                        const uint32_t baddr =
+                            xbox + b_off + ((((uint32_t)(2 * kk) + b_hi) ^ sw) << 4);
+                        if constexpr (NT == 2) {
+                            uint32_t b0, b1, b2, b3;
+                            ldsm_x4(baddr, b0, b1, b2, b3);
+                            mma_bf16_16816(acc[0], a0, a1, a2, a3, b0, b1);
+                            mma_bf16_16816(acc[1], a0, a1, a2, a3, b2, b3);
+                        } else {
+                            uint32_t b0, b1;
+                            ldsm_x2(baddr, b0, b1);
+                            mma_bf16_16816(acc[0], a0, a1, a2, a3, b0, b1);
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8 * s);
+            if (++s == stages) {
+                s = 0;
+                phase ^= 1u;
+            }
+        }
+        // accumulator fragment: c0 (row g, token 2t), c1 (g, 2t+1),
+        // c2 (g+8, 2t), c3 (g+8, 2t+1) with g = lane / 4, t = lane % 4
+        const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int tok = nt * 8 + 2 * t;
+            const int col = warp * 16 + g;
+            part[tok * kPartStride + col] = acc[nt][0];
+            part[(tok + 1) * kPartStride + col] = acc[nt][1];
+            part[tok * kPartStride + col + 8] = acc[nt][2];
+            part[(tok + 1) * kPartStride + col + 8] = acc[nt][3];
+        }
+    }
+    __syncthreads();
+    if (S > 1) cluster_sync_all();   // every rank's partial is in its shared memory
+
+    // ---- finish: reduce, round, norm, RoPE, store, insert -------------------
+    const uint32_t part_addr = smem_u32(part);
+    for (int li = warp;; li += kWarps) {
+        const int u = (int)rank + li * S;   // tokens owned by this rank: u % S == rank
+        if (u >= p.M) break;
+        float2 v;
+        if (S == 1) {
+            v = reinterpret_cast<const float2 *>(part + u * kPartStride)[lane];
+        } else {
+            const uint32_t a = part_addr + (uint32_t)(u * kPartStride + 2 * lane) * 4u;
+            v = ld_cluster_f2(map_to_rank(a, 0));
+            for (int src = 1; src < S; ++src) {
+                const float2 r = ld_cluster_f2(map_to_rank(a, (uint32_t)src));
+                v.x = __fadd_rn(v.x, r.x);
+                v.y = __fadd_rn(v.y, r.y);
+            }
+        }
+        const int flag = s_flag[u];
+        const __nv_bfloat16 p0 = __float2bfloat16_rn(v.x);
+        const __nv_bfloat16 p1 = __float2bfloat16_rn(v.y);
+        uint32_t word;
+        if (kind == kQ || kind == kK) {
+            if (!(flag & 1)) continue;   // no table row for this position: nothing written
+            const float f0 = __bfloat162float(p0), f1 = __bfloat162float(p1);
+            // weightless RMS norm over the head's 64 columns (butterfly sum:
+            // every lane ends with the same bits)
+            float ss = __fadd_rn(__fmul_rn(f0, f0), __fmul_rn(f1, f1));
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1)
+                ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, off));
+            const float ms = __fdiv_rn(ss, (float)kHeadDim);
+            const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, kEps)));
+            const float a = __fmul_rn(f0, r), b = __fmul_rn(f1, r);
+            // interleaved RoPE: pair (2 lane, 2 lane + 1), cos in column lane,
+            // sin in column 32 + lane of the position's row
+            const float c = s_cs[u * kHeadDim + lane];
+            const float sn = s_cs[u * kHeadDim + 32 + lane];
+            const float y0 = __fsub_rn(__fmul_rn(a, c), __fmul_rn(b, sn));
+            const float y1 = __fadd_rn(__fmul_rn(b, c), __fmul_rn(a, sn));
+            word = pack_bf16x2(__float2bfloat16_rn(y0), __float2bfloat16_rn(y1));
+        } else {
+            word = pack_bf16x2(p0, p1);
+        }
+        uint32_t *orow = reinterpret_cast<uint32_t *>(p.out + (size_t)u * p.N + (size_t)head * kHeadDim);
+        orow[lane] = word;
+        if ((kind == kK || kind == kV) && (flag & 2)) {
+            const int64_t slot = s_slot[u];
+            const int64_t page = slot / kPageSlots, offs = slot % kPageSlots;
+            const int gkv = head - q_heads - (kind == kV ? p.nkv : 0);
+            uint16_t *dst = p.kv_cache + ((page * p.nkv + gkv) * kPageSlots + offs) * kSlotWidth +
+                            (kind == kV ? kHeadDim : 0);
+            reinterpret_cast<uint32_t *>(dst)[lane] = word;
+        }
+    }
+    if (S > 1) cluster_sync_all();   // no CTA leaves while its partial may still be read
+}
+
+// One CTA waits on a barrier that nothing completes, through the front's own
+// bounded wait; it must give up after limit_ns and raise the status bit.
+__global__ void wait_selftest_kernel(unsigned long long limit_ns)
+{
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0)
+        bounded_wait(smem_u32(&bar), 0u, reinterpret_cast<volatile int *>(&abort_flag), limit_ns,
+                     false);
+}
+
+// ---- host side -------------------------------------------------------------
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct DeviceState {
+    bool probed = false;
+    bool ok = false;
+    bool prepared = false;
+    int sms = 0;
+};
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mutex;
+DeviceState g_devices[kMaxDevices];
+EncodeTiledFn g_encode = nullptr;
+unsigned long long g_wait_limit_ns = 2000000000ull;
+
+using KernelFn = void (*)(CUtensorMap, CUtensorMap, FrontParams);
+
+KernelFn kernel_for(int mt)
+{
+    return mt == 8 ? (KernelFn)qkv_front_kernel<8, 2> : (KernelFn)qkv_front_kernel<16, 2>;
+}
+constexpr int kKB = 2;   // 64-k boxes per ring stage: 128 k, 16 KB of W
+
+int probe_device(DeviceState **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return QKVF_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return QKVF_ERR_DEVICE;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState &d = g_devices[dev];
+    if (!d.probed) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return QKVF_ERR_CUDA;
+        d.probed = true;
+        d.ok = (major == 10 && minor == 3);
+        d.sms = sms;
+    }
+    if (!d.ok) return QKVF_ERR_DEVICE;
+    if (!g_encode) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn)
+            return QKVF_ERR_CUDA;
+        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    if (!d.prepared) {
+        for (int mt : {8, 16}) {
+            KernelFn k = kernel_for(mt);
+            if (cudaFuncSetAttribute((const void *)k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kMaxSmemPerCta) != cudaSuccess ||
+                cudaFuncSetAttribute((const void *)k,
+                                     cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+                return QKVF_ERR_CUDA;
+        }
+        d.prepared = true;
+    }
+    *out = &d;
+    return QKVF_OK;
+}
+
+struct Variant {
+    int mt, splits, stages;
+};
+
+int max_stages(int mt, int per_sm)
+{
+    const int budget = per_sm <= 1 ? kMaxSmemPerCta : kSmemPerSm / per_sm - kSmemReservedPerCta;
+    int st = 2;
+    while ((int)smem_bytes(mt, kKB, st + 1) <= budget) ++st;
+    return st;
+}
+
+// The launch shape for N columns and M tokens on `sms` SMs.  splits: the
+// largest power of two (<= 16) that keeps heads x splits within the SM count;
+// stages: as deep as shared memory allows at the CTAs per SM this needs
+// (clusters are given two CTAs per SM so that a GPC holds whole clusters),
+// and no deeper than the CTA's number of K stages.
+Variant choose_variant(int N, int M, int sms)
+{
+    Variant v;
+    const int heads = N / kHeadDim;
+    v.mt = M <= 8 ? 8 : 16;
+    v.splits = 1;
+    while (v.splits < 16 && heads * v.splits * 2 <= sms) v.splits *= 2;
+    const int ctas = heads * v.splits;
+    int per_sm = (ctas + sms - 1) / sms;
+    if (v.splits > 1 && per_sm < 2) per_sm = 2;
+    const int steps = kHidden / (kBoxK * kKB) / v.splits;
+    v.stages = max_stages(v.mt, per_sm);
+    if (v.stages > steps) v.stages = steps;
+    if (v.stages < 2) v.stages = 2;
+    return v;
+}
+
+bool aligned(const void *ptr, uintptr_t a) { return ((uintptr_t)ptr % a) == 0; }
+
+bool overlap(const void *a, size_t na, const void *b, size_t nb)
+{
+    const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+    return na && nb && x < y + nb && y < x + na;
+}
+
+const char *check_args(const uint16_t *x, const uint16_t *W, const int64_t *positions,
+                       const int64_t *slots, const float *cos_sin, int64_t cos_sin_rows,
+                       uint16_t *out, uint16_t *kv_cache, int64_t num_pages, int M, int N,
+                       int num_kv_heads, int *code)
+{
+    *code = QKVF_ERR_TOKENS;
+    if (M < 0 || M > kMaxTokens) return "M must be 0..16 tokens";
+    *code = QKVF_ERR_SHAPE;
+    if (num_kv_heads < 1 || num_kv_heads > 64)
+        return "num_kv_heads must be 1..64";
+    if (N != 2 * (kQPerKv + 1) * kHeadDim * num_kv_heads)
+        return "N must be 1152 * num_kv_heads: rows [q | k | v | gate], 8 q and 8 gate heads of 64 per KV head";
+    *code = QKVF_ERR_SIZES;
+    if (cos_sin_rows < 1 || cos_sin_rows > (int64_t(1) << 40)) return "cos_sin_rows must be >= 1";
+    if (num_pages < 1 || num_pages > (int64_t(1) << 36)) return "num_pages must be >= 1";
+    if (M == 0) {
+        *code = QKVF_OK;
+        return nullptr;
+    }
+    *code = QKVF_ERR_NULL;
+    if (!x || !W || !positions || !slots || !cos_sin || !out || !kv_cache)
+        return "a required pointer is NULL";
+    *code = QKVF_ERR_ALIGN;
+    if (!aligned(x, 16) || !aligned(W, 16))
+        return "x and W must be 16-byte aligned bf16 [rows, 8192]";
+    if (!aligned(out, 16) || !aligned(kv_cache, 16) || !aligned(cos_sin, 16))
+        return "out, kv_cache and cos_sin must be 16-byte aligned";
+    if (!aligned(positions, 8) || !aligned(slots, 8))
+        return "positions and slots must be 8-byte aligned int64";
+    *code = QKVF_ERR_ARG;
+    const size_t out_b = (size_t)M * N * 2;
+    const size_t cache_b = (size_t)num_pages * num_kv_heads * kPageSlots * kSlotWidth * 2;
+    const size_t x_b = (size_t)M * kHidden * 2, w_b = (size_t)N * kHidden * 2;
+    const size_t cs_b = (size_t)cos_sin_rows * kHeadDim * 4, idx_b = (size_t)M * 8;
+    const void *ins[] = {x, W, cos_sin, positions, slots};
+    const size_t in_b[] = {x_b, w_b, cs_b, idx_b, idx_b};
+    for (int i = 0; i < 5; ++i)
+        if (overlap(ins[i], in_b[i], out, out_b) || overlap(ins[i], in_b[i], kv_cache, cache_b))
+            return "an input overlaps out or kv_cache";
+    if (overlap(out, out_b, kv_cache, cache_b)) return "out overlaps kv_cache";
+    *code = QKVF_OK;
+    return nullptr;
+}
+
+int encode_maps(const uint16_t *x, const uint16_t *W, int M, int N, int mt, CUtensorMap *mw,
+                CUtensorMap *mx)
+{
+    const cuuint64_t wdim[2] = {(cuuint64_t)kHidden, (cuuint64_t)N};
+    const cuuint64_t wstride[1] = {(cuuint64_t)kHidden * 2};
+    const cuuint32_t wbox[2] = {(cuuint32_t)kBoxK, (cuuint32_t)kHeadDim};
+    const cuuint32_t estride[2] = {1, 1};
+    if (g_encode(mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (void *)W, wdim, wstride, wbox, estride,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return QKVF_ERR_CUDA;
+    // x rows past M read as zeros (out-of-bounds fill), so a tile of 8 or 16
+    // tokens covers any M
+    const cuuint64_t xdim[2] = {(cuuint64_t)kHidden, (cuuint64_t)M};
+    const cuuint32_t xbox[2] = {(cuuint32_t)kBoxK, (cuuint32_t)mt};
+    if (g_encode(mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (void *)x, xdim, wstride, xbox, estride,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return QKVF_ERR_CUDA;
+    return QKVF_OK;
+}
+
+int launch_front(const uint16_t *x, const uint16_t *W, const int64_t *positions,
+                 const int64_t *slots, const float *cos_sin, int64_t cos_sin_rows, uint16_t *out,
+                 uint16_t *kv_cache, int64_t num_pages, int M, int N, int num_kv_heads,
+                 const Variant &v, void *stream)
+{
+    CUtensorMap mw, mx;
+    int rc = encode_maps(x, W, M, N, v.mt, &mw, &mx);
+    if (rc != QKVF_OK) return rc;
+    FrontParams prm;
+    prm.positions = positions;
+    prm.slots = slots;
+    prm.cos_sin = cos_sin;
+    prm.out = out;
+    prm.kv_cache = kv_cache;
+    prm.cos_rows = cos_sin_rows;
+    prm.num_pages = num_pages;
+    prm.wait_limit_ns = g_wait_limit_ns;
+    prm.M = M;
+    prm.N = N;
+    prm.nkv = num_kv_heads;
+    prm.splits = v.splits;
+    prm.stages = v.stages;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)v.splits, (unsigned)(N / kHeadDim), 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem_bytes(v.mt, kKB, v.stages);
+    cfg.stream = (cudaStream_t)stream;
+    cudaLaunchAttribute attrs[2];
+    int na = 0;
+    if (v.splits > 1) {
+        attrs[na].id = cudaLaunchAttributeClusterDimension;
+        attrs[na].val.clusterDim.x = (unsigned)v.splits;
+        attrs[na].val.clusterDim.y = 1;
+        attrs[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    cfg.attrs = attrs;
+    cfg.numAttrs = (unsigned)na;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel_for(v.mt), mw, mx, prm);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return QKVF_ERR_CUDA;
+    }
+    return QKVF_OK;
+}
+
+}  // namespace qkvf
+
+using namespace qkvf;
+
+extern "C" {
+
+const char *qkv_front_strerror(int code)
+{
+    switch (code) {
+    case QKVF_OK: return "ok";
+    case QKVF_ERR_TOKENS: return "M must be 0..16 tokens";
+    case QKVF_ERR_SHAPE: return "N must be 1152 * num_kv_heads with num_kv_heads >= 1";
+    case QKVF_ERR_NULL: return "a required pointer is NULL";
+    case QKVF_ERR_ALIGN: return "a pointer is not aligned (16 bytes; 8 for positions and slots)";
+    case QKVF_ERR_DEVICE: return "the current GPU is not compute capability 10.3 (sm_103a)";
+    case QKVF_ERR_CUDA: return "a CUDA call failed";
+    case QKVF_ERR_SIZES: return "cos_sin_rows and num_pages must be >= 1";
+    case QKVF_ERR_VARIANT: return "this variant cannot run this shape";
+    case QKVF_ERR_ARG: return "bad argument (overlapping buffers or out-of-range setting)";
+    default: return "unknown qkv_front error";
+    }
+}
+
+const char *qkv_front_unsupported(const uint16_t *x, const uint16_t *W, const int64_t *positions,
+                                  const int64_t *slots, const float *cos_sin,
+                                  int64_t cos_sin_rows, uint16_t *out, uint16_t *kv_cache,
+                                  int64_t num_pages, int M, int N, int num_kv_heads)
+{
+    int code;
+    const char *why = check_args(x, W, positions, slots, cos_sin, cos_sin_rows, out, kv_cache,
+                                 num_pages, M, N, num_kv_heads, &code);
+    if (why) return why;
+    DeviceState *d;
+    int rc = probe_device(&d);
+    if (rc != QKVF_OK) return qkv_front_strerror(rc);
+    return nullptr;
+}
+
+int qkv_front_launch(const uint16_t *x, const uint16_t *W, const int64_t *positions,
+                     const int64_t *slots, const float *cos_sin, int64_t cos_sin_rows,
+                     uint16_t *out, uint16_t *kv_cache, int64_t num_pages, int M, int N,
+                     int num_kv_heads, void *stream)
+{
+    if (M == 0) return QKVF_OK;
+    DeviceState *d;
+    int rc = probe_device(&d);
+    if (rc != QKVF_OK) return rc;
+    const Variant v = choose_variant(N, M, d->sms);
+    return launch_front(x, W, positions, slots, cos_sin, cos_sin_rows, out, kv_cache, num_pages, M,
+                        N, num_kv_heads, v, stream);
+}
+
+int qkv_front(const uint16_t *x, const uint16_t *W, const int64_t *positions,
+              const int64_t *slots, const float *cos_sin, int64_t cos_sin_rows, uint16_t *out,
+              uint16_t *kv_cache, int64_t num_pages, int M, int N, int num_kv_heads, void *stream)
+{
+    int code;
+    if (check_args(x, W, positions, slots, cos_sin, cos_sin_rows, out, kv_cache, num_pages, M, N,
+                   num_kv_heads, &code))
+        return code;
+    return qkv_front_launch(x, W, positions, slots, cos_sin, cos_sin_rows, out, kv_cache,
+                            num_pages, M, N, num_kv_heads, stream);
+}
+
+int qkv_front_variant(int N, int M, int *tiles, int *stages, int *splits)
+{
+    if (M < 1 || M > kMaxTokens) return QKVF_ERR_TOKENS;
+    if (N < 1152 || N % 1152) return QKVF_ERR_SHAPE;
+    DeviceState *d;
+    int rc = probe_device(&d);
+    if (rc != QKVF_OK) return rc;
+    const Variant v = choose_variant(N, M, d->sms);
+    if (tiles) *tiles = v.mt / 8;
+    if (stages) *stages = v.stages;
+    if (splits) *splits = v.splits;
+    return QKVF_OK;
+}
+
+int qkv_front_launch_variant(const uint16_t *x, const uint16_t *W, const int64_t *positions,
+                             const int64_t *slots, const float *cos_sin, int64_t cos_sin_rows,
+                             uint16_t *out, uint16_t *kv_cache, int64_t num_pages, int M, int N,
+                             int num_kv_heads, int splits, int stages, void *stream)
+{
+    int code;
+    if (check_args(x, W, positions, slots, cos_sin, cos_sin_rows, out, kv_cache, num_pages, M, N,
+                   num_kv_heads, &code))
+        return code;
+    if (M == 0) return QKVF_OK;
+    if (splits != 1 && splits != 2 && splits != 4 && splits != 8 && splits != 16)
+        return QKVF_ERR_VARIANT;
+    Variant v;
+    v.mt = M <= 8 ? 8 : 16;
+    v.splits = splits;
+    v.stages = stages;
+    if (stages < 2 || (int)smem_bytes(v.mt, kKB, stages) > kMaxSmemPerCta) return QKVF_ERR_VARIANT;
+    DeviceState *d;
+    int rc = probe_device(&d);
+    if (rc != QKVF_OK) return rc;
+    return launch_front(x, W, positions, slots, cos_sin, cos_sin_rows, out, kv_cache, num_pages, M,
+                        N, num_kv_heads, v, stream);
+}
+
+int qkv_front_prepare(int N, int num_kv_heads)
+{
+    if (num_kv_heads < 1 || N != 2 * (kQPerKv + 1) * kHeadDim * num_kv_heads) return QKVF_ERR_SHAPE;
+    DeviceState *d;
+    return probe_device(&d);
+}
+
+int qkv_front_status(unsigned int *bits)
+{
+    if (!bits) return QKVF_ERR_NULL;
+    unsigned int v = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess) return QKVF_ERR_CUDA;
+    if (cudaMemcpyFromSymbol(&v, g_status, sizeof v) != cudaSuccess) return QKVF_ERR_CUDA;
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(g_status, &zero, sizeof zero) != cudaSuccess) return QKVF_ERR_CUDA;
+    *bits = v;
+    return QKVF_OK;
+}
+
+int qkv_front_selftest_wait(int64_t timeout_ns, void *stream)
+{
+    if (timeout_ns < 1 || timeout_ns > 1000000000ll) return QKVF_ERR_ARG;
+    DeviceState *d;
+    int rc = probe_device(&d);
+    if (rc != QKVF_OK) return rc;
+    wait_selftest_kernel<<<1, 32, 0, (cudaStream_t)stream>>>((unsigned long long)timeout_ns);
+    return cudaGetLastError() == cudaSuccess ? QKVF_OK : QKVF_ERR_CUDA;
+}
+
+int qkv_front_set_wait_limit(int64_t ns)
+{
+    if (ns < 1000 || ns > 10000000000ll) return QKVF_ERR_ARG;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    g_wait_limit_ns = (unsigned long long)ns;
+    return QKVF_OK;
+}
+
+}  // extern "C"

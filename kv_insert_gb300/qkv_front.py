@@ -1,0 +1,263 @@
+"""Python binding of libqkvfront: argument marshalling over the C ABI only.
+
+Every step of the op runs in the library's CUDA kernel.  Tensors are torch
+CUDA tensors (torch supplies device memory and streams); this module checks
+their dtypes, shapes and contiguity, passes raw pointers and sizes, and turns
+error codes into exceptions.  There is no CPU path: without the compiled
+library every call raises.
+
+Names follow the pages' API (page "vllm.models.muse_spark.nvidia.
+specialized_decode.cutedsl.attention.qkv_front": qkv_front, launch,
+unsupported, prepare, variant, hidden_rows_ok, kv_cache_layout_ok,
+supports_shape, token_tiles; page "...runtime.cute_ops": split_qkv,
+supports_call).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+import torch
+
+from . import _build
+
+HIDDEN = 8192
+HEAD_DIM = 64
+Q_PER_KV = 8
+PAGE_SLOTS = 16
+SLOT_WIDTH = 128
+MAX_TOKENS = 16
+
+STATUS_BAD_SLOT = 1
+STATUS_BAD_POSITION = 2
+STATUS_WAIT_TIMEOUT = 4
+
+HEADER = os.path.join(_build.ROOT, "include", "qkvfront.h")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class QkvFrontError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"qkv_front error {code}: {message}")
+        self.code = code
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB_PATH
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(path)
+        vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        front_args = [vp, vp, vp, vp, vp, i64, vp, vp, i64, i32, i32, i32]
+        lib.qkv_front.argtypes = front_args + [vp]
+        lib.qkv_front.restype = i32
+        lib.qkv_front_launch.argtypes = front_args + [vp]
+        lib.qkv_front_launch.restype = i32
+        lib.qkv_front_unsupported.argtypes = front_args
+        lib.qkv_front_unsupported.restype = ctypes.c_char_p
+        lib.qkv_front_launch_variant.argtypes = front_args + [i32, i32, vp]
+        lib.qkv_front_launch_variant.restype = i32
+        lib.qkv_front_variant.argtypes = [i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32),
+                                          ctypes.POINTER(i32)]
+        lib.qkv_front_variant.restype = i32
+        lib.qkv_front_prepare.argtypes = [i32, i32]
+        lib.qkv_front_prepare.restype = i32
+        lib.qkv_front_status.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+        lib.qkv_front_status.restype = i32
+        lib.qkv_front_strerror.argtypes = [i32]
+        lib.qkv_front_strerror.restype = ctypes.c_char_p
+        lib.qkv_front_selftest_wait.argtypes = [i64, vp]
+        lib.qkv_front_selftest_wait.restype = i32
+        lib.qkv_front_set_wait_limit.argtypes = [i64]
+        lib.qkv_front_set_wait_limit.restype = i32
+        _lib = lib
+        return lib
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/qkvfront.h declares."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(qkv_front\w*)\s*\(", text)))
+
+
+def strerror(code: int) -> str:
+    return load().qkv_front_strerror(code).decode()
+
+
+def _check(code: int) -> None:
+    if code != 0:
+        raise QkvFrontError(code, strerror(code))
+
+
+# ---- host-side checks (shapes and dtypes the C ABI cannot see) -------------
+
+def hidden_rows_ok(t: torch.Tensor) -> bool:
+    """Whether t is a contiguous, 16-byte aligned bf16 [rows, 8192] CUDA tensor."""
+    return (t.dtype == torch.bfloat16 and t.dim() == 2 and t.shape[1] == HIDDEN
+            and t.is_contiguous() and t.data_ptr() % 16 == 0)
+
+
+def kv_cache_layout_ok(kv_cache: torch.Tensor) -> bool:
+    """Whether a cache is bf16 [pages, num_kv_heads, 16, 128], contiguous, 16-byte aligned."""
+    return (kv_cache.dtype == torch.bfloat16 and kv_cache.dim() == 4
+            and kv_cache.shape[2] == PAGE_SLOTS and kv_cache.shape[3] == SLOT_WIDTH
+            and kv_cache.is_contiguous() and kv_cache.data_ptr() % 16 == 0)
+
+
+def supports_shape(n: int, num_kv_heads: int) -> bool:
+    """Whether the kernel computes an n-wide projection with these KV heads."""
+    return num_kv_heads >= 1 and n == 2 * (Q_PER_KV + 1) * num_kv_heads * HEAD_DIM
+
+
+def token_tiles(m: int) -> int:
+    """8-token mma column tiles for m tokens."""
+    return (m + 7) // 8
+
+
+def split_qkv(qkv: torch.Tensor, num_kv_heads: int):
+    """The q and gate column views of the front's output rows [q | k | v | gate]."""
+    q_width = Q_PER_KV * num_kv_heads * HEAD_DIM
+    kv_width = num_kv_heads * HEAD_DIM
+    if qkv.dim() != 2 or qkv.shape[1] != 2 * q_width + 2 * kv_width:
+        raise ValueError(f"qkv must be [tokens, {2 * q_width + 2 * kv_width}] for "
+                         f"{num_kv_heads} KV heads, got {tuple(qkv.shape)}")
+    return qkv[:, :q_width], qkv[:, q_width + 2 * kv_width:]
+
+
+def _tensor_reason(x, weight, positions, cos_sin, slots, kv_cache, out):
+    if not all(t.is_cuda for t in (x, weight, positions, cos_sin, slots, kv_cache)):
+        return "tensors on a CUDA device"
+    dev = x.device
+    if any(t.device != dev for t in (weight, positions, cos_sin, slots, kv_cache)):
+        return "tensors on different devices"
+    if not hidden_rows_ok(x) or not hidden_rows_ok(weight):
+        return f"x and weight other than contiguous 16-byte aligned bf16 [rows, {HIDDEN}]"
+    M = x.shape[0]
+    if not 0 <= M <= MAX_TOKENS:
+        return f"{M} tokens (the kernel takes 1 to {MAX_TOKENS})"
+    for name, t in (("positions", positions), ("slots", slots)):
+        if t.dtype != torch.int64 or t.dim() != 1 or t.shape[0] != M or not t.is_contiguous():
+            return f"{name} other than contiguous int64 [{M}]"
+    if (cos_sin.dtype != torch.float32 or cos_sin.dim() != 2 or cos_sin.shape[1] != HEAD_DIM
+            or not cos_sin.is_contiguous()):
+        return "a rotary table other than a contiguous fp32 [*, 64] one"
+    if not kv_cache_layout_ok(kv_cache):
+        return "a KV cache other than contiguous bf16 [pages, num_kv_heads, 16, 128]"
+    nkv = kv_cache.shape[1]
+    if not supports_shape(weight.shape[0], nkv):
+        return f"a projection of {weight.shape[0]} rows for {nkv} KV heads"
+    if out is not None:
+        if (out.dtype != torch.bfloat16 or out.shape != (M, weight.shape[0])
+                or not out.is_contiguous() or out.device != dev):
+            return f"out other than contiguous bf16 [{M}, {weight.shape[0]}]"
+    return None
+
+
+def _args(x, weight, positions, slots, cos_sin, out, kv_cache):
+    return (x.data_ptr(), weight.data_ptr(), positions.data_ptr(), slots.data_ptr(),
+            cos_sin.data_ptr(), cos_sin.shape[0], out.data_ptr() if out is not None else None,
+            kv_cache.data_ptr(), kv_cache.shape[0], x.shape[0], weight.shape[0],
+            kv_cache.shape[1])
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def unsupported(x, weight, positions, cos_sin, slots, kv_cache, out=None) -> str | None:
+    """Why the kernel cannot take this call (with out, also its output), or None."""
+    why = _tensor_reason(x, weight, positions, cos_sin, slots, kv_cache, out)
+    if why is not None:
+        return why
+    if out is None:
+        return None
+    with torch.cuda.device(x.device):
+        r = load().qkv_front_unsupported(*_args(x, weight, positions, slots, cos_sin, out, kv_cache))
+    return None if r is None else r.decode()
+
+
+def supports_call(x, weight, positions, cos_sin, slots, kv_cache, num_kv_heads, out=None) -> bool:
+    """Whether the front takes this call of a layer with num_kv_heads."""
+    return (unsupported(x, weight, positions, cos_sin, slots, kv_cache, out) is None
+            and kv_cache.shape[1] == num_kv_heads)
+
+
+def qkv_front(x, weight, positions, slots, cos_sin, kv_cache, out=None, stream=None):
+    """out[M, N] = x @ weight^T with the q and k heads normed and rotated, and
+    the k / v heads inserted into kv_cache at slots.  Returns out."""
+    if out is None:
+        out = torch.empty(x.shape[0], weight.shape[0], dtype=torch.bfloat16, device=x.device)
+    why = _tensor_reason(x, weight, positions, cos_sin, slots, kv_cache, out)
+    if why is not None:
+        raise ValueError(f"qkv_front does not support {why}")
+    with torch.cuda.device(x.device):
+        _check(load().qkv_front(*_args(x, weight, positions, slots, cos_sin, out, kv_cache),
+                                _stream(stream)))
+    return out
+
+
+def launch(x, weight, positions, slots, cos_sin, kv_cache, out, stream=None):
+    """qkv_front without its checks, for a call `unsupported` accepted with out."""
+    _check(load().qkv_front_launch(*_args(x, weight, positions, slots, cos_sin, out, kv_cache),
+                                   _stream(stream)))
+    return out
+
+
+def launch_variant(x, weight, positions, slots, cos_sin, kv_cache, out, splits, stages,
+                   stream=None):
+    """qkv_front at an explicit (splits, stages) variant."""
+    why = _tensor_reason(x, weight, positions, cos_sin, slots, kv_cache, out)
+    if why is not None:
+        raise ValueError(f"qkv_front does not support {why}")
+    with torch.cuda.device(x.device):
+        _check(load().qkv_front_launch_variant(
+            *_args(x, weight, positions, slots, cos_sin, out, kv_cache), int(splits), int(stages),
+            _stream(stream)))
+    return out
+
+
+def variant(n: int, m: int) -> tuple[int, int, int, int]:
+    """(tiles, stages, splits, fixed_m) of the kernel for n columns, m rows
+    (fixed_m is 0: one build serves every m of its tile count)."""
+    t, s, k = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    _check(load().qkv_front_variant(n, m, ctypes.byref(t), ctypes.byref(s), ctypes.byref(k)))
+    return t.value, s.value, k.value, 0
+
+
+def prepare(n: int, num_kv_heads: int) -> None:
+    """Set the kernel attributes the variants of n columns need (before graph capture)."""
+    _check(load().qkv_front_prepare(n, num_kv_heads))
+
+
+def status() -> int:
+    """Read and clear the device status word (synchronizes the device)."""
+    v = ctypes.c_uint()
+    _check(load().qkv_front_status(ctypes.byref(v)))
+    return v.value
+
+
+def selftest_wait(timeout_ns: int, stream=None) -> None:
+    _check(load().qkv_front_selftest_wait(int(timeout_ns), _stream(stream)))
+
+
+def set_wait_limit(ns: int) -> None:
+    _check(load().qkv_front_set_wait_limit(int(ns)))

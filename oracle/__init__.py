@@ -43,7 +43,7 @@ def build(force: bool = False) -> str:
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
     cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
-           "-fno-builtin", "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"]
+           "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH

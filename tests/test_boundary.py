@@ -1,0 +1,113 @@
+"""The C-ABI library on a machine without a GPU: it builds, loads, exports
+every function include/qkvfront.h declares, and refuses bad calls on the host
+before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from kv_insert_gb300 import qkv_front as qf
+from kv_insert_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return qf.load()
+
+
+def test_library_exports_every_declared_function(lib):
+    names = qf.header_functions()
+    assert len(names) >= 10
+    raw = ctypes.CDLL(qf.library_path())
+    for n in names:
+        assert hasattr(raw, n), n
+
+
+def test_binding_uses_only_declared_functions():
+    src = open(os.path.join(ROOT, "kv_insert_gb300", "qkv_front.py")).read()
+    used = set(re.findall(r"lib\.(qkv_front\w*)", src)) | set(re.findall(r"load\(\)\.(qkv_front\w*)", src))
+    assert used <= set(qf.header_functions()), used - set(qf.header_functions())
+
+
+def test_strerror_every_code(lib):
+    for code in range(0, 10):
+        assert qf.strerror(code)
+    assert "unknown" in qf.strerror(99)
+
+
+# fake, 16-byte aligned addresses: the checks below fail before anything is read
+X, W, POS, SL, CS, OUT, CACHE = ((i + 1) << 36 for i in range(7))
+
+
+def call(lib, x=X, w=W, pos=POS, sl=SL, cs=CS, rows=4096, out=OUT, cache=CACHE, pages=4, M=1,
+         N=1152, nkv=1):
+    return lib.qkv_front(x, w, pos, sl, cs, rows, out, cache, pages, M, N, nkv, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(M=17), 1), (dict(M=-1), 1),
+    (dict(N=1153), 2), (dict(nkv=0), 2), (dict(N=2304, nkv=1), 2),
+    (dict(x=0), 3), (dict(cache=0), 3), (dict(pos=0), 3),
+    (dict(x=X + 2), 4), (dict(w=W + 8), 4), (dict(out=OUT + 4), 4), (dict(sl=SL + 4), 4),
+    (dict(rows=0), 7), (dict(pages=0), 7),
+    (dict(out=X), 9), (dict(cache=W + 64), 9),
+])
+def test_host_refusals_before_any_cuda_call(lib, kw, code):
+    assert call(lib, **kw) == code
+    args = dict(x=X, w=W, pos=POS, sl=SL, cs=CS, rows=4096, out=OUT, cache=CACHE, pages=4, M=1,
+                N=1152, nkv=1)
+    args.update(kw)
+    why = lib.qkv_front_unsupported(args["x"], args["w"], args["pos"], args["sl"], args["cs"],
+                                    args["rows"], args["out"], args["cache"], args["pages"],
+                                    args["M"], args["N"], args["nkv"])
+    assert why is not None and len(why) > 5
+
+
+def test_zero_tokens_is_a_no_op(lib):
+    assert call(lib, M=0, x=0, out=0) == 0
+
+
+def test_variant_and_launch_variant_refusals(lib):
+    assert lib.qkv_front_variant(1152, 0, None, None, None) == 1
+    assert lib.qkv_front_variant(1000, 4, None, None, None) == 2
+    assert lib.qkv_front_launch_variant(X, W, POS, SL, CS, 4096, OUT, CACHE, 4, 1, 1152, 1, 3, 4,
+                                        None) in (8,)
+    assert lib.qkv_front_launch_variant(X, W, POS, SL, CS, 4096, OUT, CACHE, 4, 1, 1152, 1, 1, 1,
+                                        None) == 8
+    assert lib.qkv_front_set_wait_limit(5) == 9
+    assert lib.qkv_front_selftest_wait(0, None) == 9
+    assert lib.qkv_front_prepare(1000, 1) == 2
+
+
+def test_no_gpu_here_is_reported_not_crashed(lib):
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    # valid arguments: the call reaches the device query, which fails cleanly
+    assert call(lib) in (5, 6)
+
+
+def test_layout_helpers():
+    q = torch.zeros(3, 9216)
+    qv, gv = qf.split_qkv(q, 8)
+    assert qv.shape == (3, 4096) and gv.shape == (3, 4096)
+    assert gv.data_ptr() == q.data_ptr() + (4096 + 1024) * 4
+    with pytest.raises(ValueError):
+        qf.split_qkv(q, 4)
+    assert qf.supports_shape(1152, 1) and qf.supports_shape(18432, 16)
+    assert not qf.supports_shape(1152, 2)
+    assert [qf.token_tiles(m) for m in (1, 8, 9, 16)] == [1, 1, 2, 2]
+
+
+def test_product_path_never_touches_the_oracle():
+    pkg = os.path.join(ROOT, "kv_insert_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"\boracle\b", text.replace("oracle", "oracle")
+                                     if f != "workloads.py" else ""), f

@@ -1,0 +1,107 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on
+the same seeded inputs, at the full sizes of every workload.
+
+Bar: BF16 values within |d| <= 2e-2 + 1e-2 |oracle|; cache placement exact
+(only named slots change and each holds its token's k / v head bits); with
+integer-valued inputs the projection is exact in any summation order, so the
+v and gate columns must match the oracle bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+from kv_insert_gb300 import qkv_front as qf
+from kv_insert_gb300 import workloads as wl
+
+from _parity import (assert_cache, assert_values, check_workload, device_inputs, run_device,
+                     run_oracle)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    qf.status()   # clear any bit left by an earlier module
+
+
+@pytest.mark.parametrize("name", list(wl.WORKLOADS))
+def test_workload_matches_oracle(name):
+    check_workload(wl.WORKLOADS[name])
+
+
+def _vg_cols(nkv):
+    q_width = 8 * nkv * 64
+    return slice(q_width + nkv * 64, None)   # v then gate heads
+
+
+@pytest.mark.parametrize("name", ["m1_nkv1_n1152", "m8_nkv8_n9216", "m16_nkv8_n9216_consecutive",
+                                  "sweep_m13_nkv8_n9216", "m8_nkv16_n18432"])
+def test_integer_inputs_bit_exact_projection(name):
+    w = wl.WORKLOADS[name]
+    _, out_bits, out_ref = check_workload(w, integer_valued=True)
+    vg = _vg_cols(w.num_kv_heads)
+    assert np.array_equal(out_bits[:, vg], out_ref[:, vg])
+
+
+@pytest.mark.parametrize("M", list(range(1, 17)))
+def test_every_token_count_one_kv_head(M):
+    """Every M from 1 to 16 (ragged 8-token tiles) at N = 1152."""
+    w = wl.Workload(f"m{M}_nkv1", M=M, num_kv_heads=1, max_pos=4096, num_pages=8, seed=2000 + M)
+    check_workload(w)
+
+
+@pytest.mark.parametrize("nkv", [2, 3, 4])
+def test_other_kv_head_counts(nkv):
+    w = wl.Workload(f"m5_nkv{nkv}", M=5, num_kv_heads=nkv, max_pos=8192, num_pages=64,
+                    seed=2100 + nkv)
+    check_workload(w)
+
+
+def test_negative_slot_inserts_nothing():
+    w = wl.Workload("pad", M=6, num_kv_heads=2, max_pos=1024, num_pages=16, seed=2201)
+    inp = wl.make_inputs(w)
+    inp["slots"][2] = -1
+    g = device_inputs(inp)
+    out = run_device(g)
+    assert qf.status() == 0
+    out_bits = wl.bits(out.cpu())
+    out_ref, cache_ref, err = run_oracle(inp, w.num_kv_heads)
+    assert err == 0
+    assert_values(out_bits, out_ref)
+    assert_cache(inp, w.num_kv_heads, g["kv_cache"], out_bits, cache_ref)
+
+
+def test_out_of_range_slot_and_position_are_flagged_not_written():
+    """Checked in the kernel: a slot past the cache and a position past the
+    table raise status bits; that token's insert (and for the position, its
+    q and k heads) is skipped; nothing is written out of bounds."""
+    w = wl.Workload("bad", M=4, num_kv_heads=1, max_pos=512, num_pages=4, seed=2202)
+    inp = wl.make_inputs(w)
+    inp["slots"][1] = w.num_pages * 16 + 5
+    inp["positions"][3] = w.max_pos + 7
+    g = device_inputs(inp)
+    sentinel = torch.full((w.M, w.N), 3.0, dtype=torch.bfloat16)
+    out = run_device(g, out=sentinel.to("cuda:0"))
+    st = qf.status()
+    assert st & qf.STATUS_BAD_SLOT and st & qf.STATUS_BAD_POSITION
+    out_bits = wl.bits(out.cpu())
+    out_ref, cache_ref, err = run_oracle(inp, w.num_kv_heads,
+                                         out_bits=wl.bits(sentinel))
+    assert err == 3
+    assert np.array_equal(out_bits[3, : 9 * 64], out_ref[3, : 9 * 64])   # untouched sentinel
+    assert_values(out_bits, out_ref)
+    assert_cache(inp, w.num_kv_heads, g["kv_cache"], out_bits, cache_ref)
+
+
+def test_zero_tokens_launches_nothing():
+    w = wl.WORKLOADS["m1_nkv1_n1152"]
+    inp = wl.make_inputs(w)
+    g = device_inputs(inp)
+    before = g["kv_cache"].clone()
+    out = torch.empty(0, w.N, dtype=torch.bfloat16, device="cuda:0")
+    qf.qkv_front(g["x"][:0], g["W"], g["positions"][:0], g["slots"][:0], g["cos_sin"],
+                 g["kv_cache"], out)
+    torch.cuda.synchronize()
+    assert torch.equal(before, g["kv_cache"])
