@@ -407,19 +407,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kAuxWarp) {
         // ---- aux: the epilogue's per-token inputs -------------------------
         griddep_wait();
+        unsigned bad = 0u;
         if (lane < p.M) {
             const int64_t pos = p.positions[lane];
             const int64_t slot = p.slots[lane];
+            const int64_t slot_end = p.num_pages * (int64_t)kPageSlots;
             const bool pos_ok = pos >= 0 && pos < p.cos_rows;
-            const bool slot_over = slot >= p.num_pages * kPageSlots;
+            const bool slot_over = slot >= slot_end;
             const bool insert = slot >= 0 && !slot_over && pos_ok;
             s_pos[lane] = pos;
             s_slot[lane] = slot;
             s_flag[lane] = (pos_ok ? 1 : 0) | (insert ? 2 : 0);
-            const unsigned bad = (pos_ok ? 0u : QKVF_STATUS_BAD_POSITION) |
-                                 (slot_over ? QKVF_STATUS_BAD_SLOT : 0u);
-            if (bad && head == 0 && rank == 0) atomicOr(&g_status, bad);
+            bad = (pos_ok ? 0u : QKVF_STATUS_BAD_POSITION) | (slot_over ? QKVF_STATUS_BAD_SLOT : 0u);
         }
+        // one report per call: the warp's OR, from one CTA
+        bad = __reduce_or_sync(0xffffffffu, bad);
+        if (lane == 0 && bad != 0u && head == 0 && rank == 0) atomicOr(&g_status, bad);
         __syncwarp();
         if (kind == kQ || kind == kK) {
             for (int t = (int)rank; t < p.M; t += S) {

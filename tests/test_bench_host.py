@@ -1,0 +1,74 @@
+"""Host logic of bench.py on CPU: the max-over-ranks timing and whole-job
+throughput with two gloo ranks, and the reference arm's line format."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    import bench
+    bench.dist_init("gloo")
+    el = 1.0 + rank          # rank 1 is the slowest
+    m = bench.max_over_ranks(el)
+    res = bench.aggregate(bytes_per_step=1000, steps=10, world=world, seconds_max=m)
+    bench.barrier()
+    torch.distributed.destroy_process_group()
+    q.put((rank, m, res))
+
+
+def test_max_over_ranks_and_aggregate_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = [q.get(timeout=120) for _ in procs]
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, m, res in got:
+        assert m == 2.0
+        assert res["value"] == pytest.approx(1000 * 10 * 2 / 2.0 / 1e9)
+        assert res["us_per_call"] == pytest.approx(2.0 / 10 * 1e6)
+
+
+def test_reference_arm_line_format():
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "3", "--warmup", "3", "--ref-seconds", "1",
+                        "--workload", "m1_nkv1_n1152"],
+                       capture_output=True, text=True, env=env, timeout=600)
+    assert r.returncode == 0, r.stderr
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
+    assert line["higher_is_better"] is True
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_roofline_bytes_formula():
+    from kv_insert_gb300 import workloads as wl
+    w = wl.WORKLOADS["m8_nkv8_n9216"]
+    assert w.roofline_bytes() == 151_289_856
+    assert wl.WORKLOADS["m1_nkv1_n1152"].roofline_bytes() == 18_893_312
+    assert wl.WORKLOADS["m8_nkv16_n18432"].roofline_bytes() == 302_448_640

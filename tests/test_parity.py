@@ -76,23 +76,48 @@ def test_negative_slot_inserts_nothing():
 def test_out_of_range_slot_and_position_are_flagged_not_written():
     """Checked in the kernel: a slot past the cache and a position past the
     table raise status bits; that token's insert (and for the position, its
-    q and k heads) is skipped; nothing is written out of bounds."""
+    q and k heads) is skipped.  The cache is a view of the first pages of a
+    larger buffer, so a wrong insert would land in memory the test owns and
+    is seen in the pages past the view."""
     w = wl.Workload("bad", M=4, num_kv_heads=1, max_pos=512, num_pages=4, seed=2202)
     inp = wl.make_inputs(w)
     inp["slots"][1] = w.num_pages * 16 + 5
     inp["positions"][3] = w.max_pos + 7
     g = device_inputs(inp)
+    parent = torch.zeros(2 * w.num_pages, 1, 16, 128, dtype=torch.bfloat16, device="cuda:0")
+    parent[: w.num_pages].copy_(g["kv_cache"])
+    g["kv_cache"] = parent[: w.num_pages]
+    assert g["kv_cache"].is_contiguous()
     sentinel = torch.full((w.M, w.N), 3.0, dtype=torch.bfloat16)
     out = run_device(g, out=sentinel.to("cuda:0"))
     st = qf.status()
-    assert st & qf.STATUS_BAD_SLOT and st & qf.STATUS_BAD_POSITION
+    assert int(parent[w.num_pages:].view(torch.int16).abs().sum()) == 0, "insert past the cache"
     out_bits = wl.bits(out.cpu())
-    out_ref, cache_ref, err = run_oracle(inp, w.num_kv_heads,
-                                         out_bits=wl.bits(sentinel))
+    out_ref, cache_ref, err = run_oracle(inp, w.num_kv_heads, out_bits=wl.bits(sentinel))
     assert err == 3
     assert np.array_equal(out_bits[3, : 9 * 64], out_ref[3, : 9 * 64])   # untouched sentinel
     assert_values(out_bits, out_ref)
     assert_cache(inp, w.num_kv_heads, g["kv_cache"], out_bits, cache_ref)
+    assert st == qf.STATUS_BAD_SLOT | qf.STATUS_BAD_POSITION, st
+
+
+@pytest.mark.parametrize("which", ["slot", "position"])
+def test_each_bad_index_alone_is_flagged(which):
+    w = wl.Workload("bad1", M=3, num_kv_heads=2, max_pos=256, num_pages=2, seed=2203)
+    inp = wl.make_inputs(w)
+    if which == "slot":
+        inp["slots"][0] = w.num_pages * 16
+    else:
+        inp["positions"][2] = -5
+    g = device_inputs(inp)
+    parent = torch.zeros(2 * w.num_pages, 2, 16, 128, dtype=torch.bfloat16, device="cuda:0")
+    parent[: w.num_pages].copy_(g["kv_cache"])
+    g["kv_cache"] = parent[: w.num_pages]
+    run_device(g)
+    st = qf.status()
+    assert int(parent[w.num_pages:].view(torch.int16).abs().sum()) == 0, "insert past the cache"
+    want = qf.STATUS_BAD_SLOT if which == "slot" else qf.STATUS_BAD_POSITION
+    assert st == want, st
 
 
 def test_zero_tokens_launches_nothing():
