@@ -62,8 +62,9 @@ def assert_cache(inp: dict, nkv: int, cache_dev: torch.Tensor, out_bits: np.ndar
     cache = wl.bits(cache_dev.cpu())
     changed = np.argwhere((cache != pre).any(axis=(1, 3)))
     named = {}
-    for t, s in enumerate(inp["slots"].tolist()):
-        if 0 <= s < pre.shape[0] * 16:
+    rows = inp["cos_sin"].shape[0]
+    for t, (s, p) in enumerate(zip(inp["slots"].tolist(), inp["positions"].tolist())):
+        if 0 <= s < pre.shape[0] * 16 and 0 <= p < rows:   # tokens that insert
             named[(s // 16, s % 16)] = t
     for pg, off in changed:
         assert (int(pg), int(off)) in named, f"slot {pg * 16 + off} written but named by no token"
