@@ -82,9 +82,13 @@ struct FrontParams {
     int nkv;
     int splits;
     int stages;
+    int kb;           // 64-k boxes per ring stage (1, 2 or 4)
+    int l2_prefetch;  // ring stages of W prefetched into L2 before the PDL wait
 };
 
-// Shared-memory layout of one CTA, from the base (1024-byte aligned).
+// Shared-memory layout of one CTA, from the base (1024-byte aligned).  The
+// FP32 partials reuse the start of the W ring: they are written only after
+// every consumer warp has finished reading the ring.
 struct Layout {
     uint32_t w, x, full, empty, part, pos, slot, cs, flag, abort_flag, total;
 };
@@ -94,6 +98,7 @@ __host__ __device__ inline Layout layout_of(int mt, int kb, int stages)
     Layout L;
     uint32_t off = 0;
     L.w = off;
+    L.part = off;
     off += (uint32_t)stages * kb * kBoxBytesW;
     L.x = off;
     off += (uint32_t)stages * kb * mt * 128;
@@ -102,8 +107,6 @@ __host__ __device__ inline Layout layout_of(int mt, int kb, int stages)
     L.empty = off;
     off += (uint32_t)stages * 8;
     off = (off + 15u) & ~15u;
-    L.part = off;
-    off += (uint32_t)mt * kPartStride * 4;
     L.pos = off;
     off += kMaxTokens * 8;
     L.slot = off;
@@ -237,6 +240,20 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *m, 
         : "memory");
 }
 
+// Prefetch one W box into L2 (no shared-memory destination, no barrier).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *m, int c0, int c1)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(c0), "r"(c1)
+                 : "memory");
+}
+
+__device__ __forceinline__ void consumer_bar_sync()
+{
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+}
+
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
                                         uint32_t &r3)
 {
@@ -300,15 +317,16 @@ __device__ __forceinline__ uint32_t pack_bf16x2(__nv_bfloat16 lo, __nv_bfloat16 
 
 // ---- the front kernel ------------------------------------------------------
 
-template <int MT, int KB>
+template <int MT>
 __global__ void __launch_bounds__(kThreads, 1)
     qkv_front_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                      const FrontParams p)
 {
     constexpr int NT = MT / 8;                       // 8-token mma column tiles
     constexpr uint32_t kBoxBytesX = MT * 128;
-    constexpr uint32_t kStageTx = KB * (kBoxBytesW + kBoxBytesX);
-    constexpr int kStepsAll = kHidden / (kBoxK * KB);
+    const int KB = p.kb;
+    const uint32_t kStageTx = (uint32_t)KB * (kBoxBytesW + kBoxBytesX);
+    const int kStepsAll = kHidden / (kBoxK * KB);
 
     extern __shared__ uint8_t smem_dyn[];
     uint8_t *smem = smem_dyn + ((1024u - (smem_u32(smem_dyn) & 1023u)) & 1023u);
@@ -365,6 +383,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int b = 0; b < KB; ++b)
                     tma_load_2d(sW + (uint32_t)(i * KB + b) * kBoxBytesW, &tmW, full0 + 8 * i,
                                 (j * KB + b) * kBoxK, row0, pol_w);
+            }
+            // weights further ahead into L2 while the previous kernel finishes
+            const int pf_end = npre + p.l2_prefetch < steps ? npre + p.l2_prefetch : steps;
+            for (int i = npre; i < pf_end; ++i) {
+                const int j = (int)rank + i * S;
+                for (int b = 0; b < KB; ++b) tma_prefetch_l2_2d(&tmW, (j * KB + b) * kBoxK, row0);
             }
             griddep_wait();   // x is written by the kernel before this one
             for (int i = 0; i < npre; ++i) {
@@ -461,7 +485,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             // then agrees, so ldmatrix / mma always run on a converged warp
             const bool landed = bounded_wait(full0 + 8 * s, phase, s_abort, p.wait_limit_ns, true);
             if (__all_sync(0xffffffffu, landed)) {
-#pragma unroll
                 for (int b = 0; b < KB; ++b) {
                     const uint32_t wbox = sW + (uint32_t)(s * KB + b) * kBoxBytesW;
                     const uint32_t xbox = sX + (uint32_t)(s * KB + b) * kBoxBytesX;
@@ -492,6 +515,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 phase ^= 1u;
             }
         }
+        // the partials overwrite the ring: every consumer warp must be done with it
+        consumer_bar_sync();
         // accumulator fragment: c0 (row g, token 2t), c1 (g, 2t+1),
         // c2 (g+8, 2t), c3 (g+8, 2t+1) with g = lane / 4, t = lane % 4
         const int g = lane >> 2, t = lane & 3;
@@ -606,9 +631,10 @@ using KernelFn = void (*)(CUtensorMap, CUtensorMap, FrontParams);
 
 KernelFn kernel_for(int mt)
 {
-    return mt == 8 ? (KernelFn)qkv_front_kernel<8, 2> : (KernelFn)qkv_front_kernel<16, 2>;
+    return mt == 8 ? (KernelFn)qkv_front_kernel<8> : (KernelFn)qkv_front_kernel<16>;
 }
-constexpr int kKB = 2;   // 64-k boxes per ring stage: 128 k, 16 KB of W
+constexpr int kDefaultKB = 2;          // 64-k boxes per ring stage: 128 k, 16 KB of W
+constexpr int kDefaultL2Prefetch = 0;  // W stages prefetched into L2 before the PDL wait
 
 int probe_device(DeviceState **out)
 {
@@ -653,14 +679,14 @@ int probe_device(DeviceState **out)
 }
 
 struct Variant {
-    int mt, splits, stages;
+    int mt, splits, stages, kb, l2_prefetch;
 };
 
-int max_stages(int mt, int per_sm)
+int max_stages(int mt, int kb, int per_sm)
 {
     const int budget = per_sm <= 1 ? kMaxSmemPerCta : kSmemPerSm / per_sm - kSmemReservedPerCta;
     int st = 2;
-    while ((int)smem_bytes(mt, kKB, st + 1) <= budget) ++st;
+    while ((int)smem_bytes(mt, kb, st + 1) <= budget) ++st;
     return st;
 }
 
@@ -674,16 +700,30 @@ Variant choose_variant(int N, int M, int sms)
     Variant v;
     const int heads = N / kHeadDim;
     v.mt = M <= 8 ? 8 : 16;
+    v.kb = kDefaultKB;
+    v.l2_prefetch = kDefaultL2Prefetch;
     v.splits = 1;
     while (v.splits < 16 && heads * v.splits * 2 <= sms) v.splits *= 2;
     const int ctas = heads * v.splits;
     int per_sm = (ctas + sms - 1) / sms;
     if (v.splits > 1 && per_sm < 2) per_sm = 2;
-    const int steps = kHidden / (kBoxK * kKB) / v.splits;
-    v.stages = max_stages(v.mt, per_sm);
+    const int steps = kHidden / (kBoxK * v.kb) / v.splits;
+    v.stages = max_stages(v.mt, v.kb, per_sm);
     if (v.stages > steps) v.stages = steps;
     if (v.stages < 2) v.stages = 2;
     return v;
+}
+
+// Whether a variant can run: a power-of-two split and stage size that divide
+// the 128 boxes of K, and a ring that fits the shared-memory limit.
+bool variant_ok(const Variant &v)
+{
+    const bool pow2_s = v.splits == 1 || v.splits == 2 || v.splits == 4 || v.splits == 8 ||
+                        v.splits == 16;
+    const bool kb_ok = v.kb == 1 || v.kb == 2 || v.kb == 4;
+    if (!pow2_s || !kb_ok || v.stages < 2 || v.l2_prefetch < 0 || v.l2_prefetch > 64) return false;
+    if (v.splits * v.kb > kHidden / kBoxK) return false;
+    return (int)smem_bytes(v.mt, v.kb, v.stages) <= kMaxSmemPerCta;
 }
 
 bool aligned(const void *ptr, uintptr_t a) { return ((uintptr_t)ptr % a) == 0; }
@@ -782,11 +822,13 @@ int launch_front(const uint16_t *x, const uint16_t *W, const int64_t *positions,
     prm.nkv = num_kv_heads;
     prm.splits = v.splits;
     prm.stages = v.stages;
+    prm.kb = v.kb;
+    prm.l2_prefetch = v.l2_prefetch;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)v.splits, (unsigned)(N / kHeadDim), 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem_bytes(v.mt, kKB, v.stages);
+    cfg.dynamicSmemBytes = smem_bytes(v.mt, v.kb, v.stages);
     cfg.stream = (cudaStream_t)stream;
     cudaLaunchAttribute attrs[2];
     int na = 0;
@@ -898,13 +940,13 @@ int qkv_front_launch_variant(const uint16_t *x, const uint16_t *W, const int64_t
                    num_kv_heads, &code))
         return code;
     if (M == 0) return QKVF_OK;
-    if (splits != 1 && splits != 2 && splits != 4 && splits != 8 && splits != 16)
-        return QKVF_ERR_VARIANT;
     Variant v;
     v.mt = M <= 8 ? 8 : 16;
     v.splits = splits;
     v.stages = stages;
-    if (stages < 2 || (int)smem_bytes(v.mt, kKB, stages) > kMaxSmemPerCta) return QKVF_ERR_VARIANT;
+    v.kb = kDefaultKB;
+    v.l2_prefetch = kDefaultL2Prefetch;
+    if (!variant_ok(v)) return QKVF_ERR_VARIANT;
     DeviceState *d;
     int rc = probe_device(&d);
     if (rc != QKVF_OK) return rc;
