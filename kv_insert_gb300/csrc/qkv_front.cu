@@ -459,11 +459,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ---- consume: mma.sync over the ring ------------------------------
         griddep_wait();
-        float acc[NT][4];
+        // one accumulator set per k16 step of a box: four independent mma
+        // chains instead of one serial chain (mma.sync latency, not issue
+        // rate, is what limits a single chain); summed in a fixed order at the end
+        float acc[NT][4][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int r = 0; r < 4; ++r) acc[nt][r] = 0.f;
+            for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) acc[nt][kk][r] = 0.f;
 
         // ldmatrix row addresses.  A: lane l feeds row (l & 7) + 8 ((l >> 3) & 1)
         // of this warp's 16 W rows, 16-byte chunk (l >> 4) of the k16 step.
@@ -483,28 +488,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < steps; ++i) {
             // every lane waits (each gets the barrier's acquire); the warp
             // then agrees, so ldmatrix / mma always run on a converged warp
-            const bool landed = bounded_wait(full0 + 8 * s, phase, s_abort, p.wait_limit_ns, true);
+            const bool landed = mbar_try_wait(full0 + 8 * s, phase) ||
+                                bounded_wait(full0 + 8 * s, phase, s_abort, p.wait_limit_ns, true);
             if (__all_sync(0xffffffffu, landed)) {
                 for (int b = 0; b < KB; ++b) {
                     const uint32_t wbox = sW + (uint32_t)(s * KB + b) * kBoxBytesW;
                     const uint32_t xbox = sX + (uint32_t)(s * KB + b) * kBoxBytesX;
+                    uint32_t a[4][4], bb[4][4];
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        uint32_t a0, a1, a2, a3;
-                        ldsm_x4(wbox + a_off + ((((uint32_t)(2 * kk) + a_hi) ^ sw) << 4), a0, a1,
-                                a2, a3);
+                        ldsm_x4(wbox + a_off + ((((uint32_t)(2 * kk) + a_hi) ^ sw) << 4), a[kk][0],
+                                a[kk][1], a[kk][2], a[kk][3]);
                         const uint32_t baddr =
                             xbox + b_off + ((((uint32_t)(2 * kk) + b_hi) ^ sw) << 4);
-                        if constexpr (NT == 2) {
-                            uint32_t b0, b1, b2, b3;
-                            ldsm_x4(baddr, b0, b1, b2, b3);
-                            mma_bf16_16816(acc[0], a0, a1, a2, a3, b0, b1);
-                            mma_bf16_16816(acc[1], a0, a1, a2, a3, b2, b3);
-                        } else {
-                            uint32_t b0, b1;
-                            ldsm_x2(baddr, b0, b1);
-                            mma_bf16_16816(acc[0], a0, a1, a2, a3, b0, b1);
-                        }
+                        if constexpr (NT == 2)
+                            ldsm_x4(baddr, bb[kk][0], bb[kk][1], bb[kk][2], bb[kk][3]);
+                        else
+                            ldsm_x2(baddr, bb[kk][0], bb[kk][1]);
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        mma_bf16_16816(acc[0][kk], a[kk][0], a[kk][1], a[kk][2], a[kk][3],
+                                       bb[kk][0], bb[kk][1]);
+                        if constexpr (NT == 2)
+                            mma_bf16_16816(acc[1][kk], a[kk][0], a[kk][1], a[kk][2], a[kk][3],
+                                           bb[kk][2], bb[kk][3]);
                     }
                 }
             }
@@ -515,6 +523,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 phase ^= 1u;
             }
         }
+        float sum[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+                sum[nt][r] = __fadd_rn(__fadd_rn(acc[nt][0][r], acc[nt][1][r]),
+                                       __fadd_rn(acc[nt][2][r], acc[nt][3][r]));
         // the partials overwrite the ring: every consumer warp must be done with it
         consumer_bar_sync();
         // accumulator fragment: c0 (row g, token 2t), c1 (g, 2t+1),
@@ -524,10 +539,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int nt = 0; nt < NT; ++nt) {
             const int tok = nt * 8 + 2 * t;
             const int col = warp * 16 + g;
-            part[tok * kPartStride + col] = acc[nt][0];
-            part[(tok + 1) * kPartStride + col] = acc[nt][1];
-            part[tok * kPartStride + col + 8] = acc[nt][2];
-            part[(tok + 1) * kPartStride + col + 8] = acc[nt][3];
+            part[tok * kPartStride + col] = sum[nt][0];
+            part[(tok + 1) * kPartStride + col] = sum[nt][1];
+            part[tok * kPartStride + col + 8] = sum[nt][2];
+            part[(tok + 1) * kPartStride + col + 8] = sum[nt][3];
         }
     }
     __syncthreads();
@@ -633,7 +648,7 @@ KernelFn kernel_for(int mt)
 {
     return mt == 8 ? (KernelFn)qkv_front_kernel<8> : (KernelFn)qkv_front_kernel<16>;
 }
-constexpr int kDefaultKB = 2;          // 64-k boxes per ring stage: 128 k, 16 KB of W
+constexpr int kDefaultKB = 4;          // 64-k boxes per ring stage: 256 k, 32 KB of W
 constexpr int kDefaultL2Prefetch = 0;  // W stages prefetched into L2 before the PDL wait
 
 int probe_device(DeviceState **out)
