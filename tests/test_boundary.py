@@ -113,3 +113,23 @@ def test_product_path_never_touches_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
                 assert "qkv_oracle" not in text and "liboracle" not in text, f
+
+
+def test_variants_the_gpu_tests_launch_are_accepted(lib):
+    """Every (splits, stages) the GPU tests request passes the host-side
+    variant check: the call gets past it to the device query (which fails on
+    a machine without a GPU) instead of returning QKVF_ERR_VARIANT."""
+    if torch.cuda.is_available():
+        pytest.skip("checked through the GPU tests themselves")
+    import test_determinism as td
+    from kv_insert_gb300 import workloads as wl
+    cases = [(n, s, st) for n, _ in [("m8_nkv8_n9216", 0), ("m16_nkv8_n9216_consecutive", 0),
+                                   ("m1_nkv1_n1152", 0)] for s in (1, 2, 8)
+             for st in td.RING_DEPTHS]
+    cases += [(n, s, td.split_stages(s)) for n, sl in td.SPLIT_CASES for s in sl]
+    cases += [(n, s, 3) for n, sl in td.SPLIT_CASES for s in sl]
+    for name, splits, stages in cases:
+        w = wl.WORKLOADS[name]
+        rc = lib.qkv_front_launch_variant(X, W, POS, SL, CS, 4096, OUT, CACHE, 4, w.M, w.N,
+                                          w.num_kv_heads, splits, stages, None)
+        assert rc in (5, 6), (name, splits, stages, rc)

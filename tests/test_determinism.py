@@ -12,6 +12,19 @@ from _parity import assert_cache, assert_values, device_inputs, run_device, run_
 
 pytestmark = pytest.mark.gpu
 
+# ring depths and K splits the GPU tests launch; tests/test_boundary.py checks
+# on the CPU that the library accepts each of them
+RING_DEPTHS = (2, 3, 4, 5)
+SPLIT_CASES = [
+    ("m8_nkv8_n9216", (1, 2, 4)),
+    ("m1_nkv1_n1152", (1, 2, 4, 8, 16)),
+    ("m16_nkv8_n9216_consecutive", (1, 2, 4, 8)),
+]
+
+
+def split_stages(splits):
+    return 2 if splits == 16 else 4
+
 
 @pytest.fixture(scope="module", autouse=True)
 def _built():
@@ -44,7 +57,7 @@ def test_ring_depth_does_not_change_result(name, splits):
     w = wl.WORKLOADS[name]
     inp = wl.make_inputs(w)
     ref = None
-    for stages in (2, 3, 5, 8):
+    for stages in RING_DEPTHS:
         g = _fresh(inp)
         out = run_device(g, splits=splits, stages=stages)
         if ref is None:
@@ -53,11 +66,7 @@ def test_ring_depth_does_not_change_result(name, splits):
             assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), stages
 
 
-@pytest.mark.parametrize("name,splits_list", [
-    ("m8_nkv8_n9216", (1, 2, 4)),
-    ("m1_nkv1_n1152", (1, 2, 4, 8, 16)),
-    ("m16_nkv8_n9216_consecutive", (1, 2, 4, 8)),
-])
+@pytest.mark.parametrize("name,splits_list", SPLIT_CASES)
 def test_every_k_split_matches_oracle(name, splits_list):
     w = wl.WORKLOADS[name]
     inp = wl.make_inputs(w)
@@ -65,7 +74,7 @@ def test_every_k_split_matches_oracle(name, splits_list):
     assert err == 0
     for splits in splits_list:
         g = _fresh(inp)
-        out = run_device(g, splits=splits, stages=2 if splits == 16 else 4)
+        out = run_device(g, splits=splits, stages=split_stages(splits))
         assert qf.status() == 0
         out_bits = wl.bits(out.cpu())
         assert_values(out_bits, out_ref, what=f"out at splits={splits}")
