@@ -292,7 +292,7 @@ def run_ours(args, w: wl.Workload):
     g = {k: v.to(dev) for k, v in inp.items()}
     M, N, nkv = w.M, w.N, w.num_kv_heads
     qf.prepare(N, nkv)
-    tiles, stages, splits, _ = qf.variant(N, M)
+    variant = qf.variant_full(N, M)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     w_bytes = N * wl.HIDDEN * 2
     copies = max(2, math.ceil(3 * l2 / w_bytes))
@@ -403,7 +403,7 @@ def run_ours(args, w: wl.Workload):
         "us_per_call": res["us_per_call"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": dict(w.describe(), **{
-            "variant": {"tiles": tiles, "stages": stages, "splits": splits},
+            "variant": variant,
             "l2": f"inputs larger than L2: W rotated over {copies} copies of {w_bytes / 1e6:.1f} MB "
                   f"(L2 {l2 / 1e6:.1f} MB)",
             "graph_calls": per_graph, "parallelism": f"replicas x{world}"}),

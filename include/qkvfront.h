@@ -103,27 +103,37 @@ int qkv_front_launch(const uint16_t *x, const uint16_t *W, const int64_t *positi
                      uint16_t *out, uint16_t *kv_cache, int64_t num_pages, int M, int N,
                      int num_kv_heads, void *stream);
 
+/* ---- contraction engines (qkv_front_variant, qkv_front_launch_variant) --- */
+#define QKVF_CONSUMER_DEFAULT 0   /* the library's choice */
+#define QKVF_CONSUMER_MMA_SYNC 1  /* mma.sync m16n8k16 in four consumer warps */
+#define QKVF_CONSUMER_TCGEN05 2   /* tcgen05.mma M=64 into tensor memory, one issuing thread */
+
 /*
  * qkv_front_variant: the launch shape qkv_front uses for N columns and M
  * tokens on the current device (page qkv_front, function variant):
- *   *tiles  8-token column tiles (1 or 2),
- *   *stages depth of the shared-memory weight ring,
- *   *splits CTAs per head (the cluster size; K is split cyclically among them).
- * Any output pointer may be NULL.  The result of the op depends on `splits`
- * only (the K split fixes the summation order); `stages` never changes it.
+ *   *tiles    8-token column tiles (1 or 2),
+ *   *stages   depth of the shared-memory weight ring,
+ *   *splits   CTAs per head (the cluster size; K is split cyclically among them),
+ *   *kb       64-wide K boxes per ring stage (1, 2 or 4),
+ *   *consumer QKVF_CONSUMER_MMA_SYNC or QKVF_CONSUMER_TCGEN05.
+ * Any output pointer may be NULL.  The result depends on the launch shape:
+ * `splits` and `kb` fix how K is divided among CTAs, and the consumer fixes
+ * the order inside one CTA; `stages` never changes it.
  */
-int qkv_front_variant(int N, int M, int *tiles, int *stages, int *splits);
+int qkv_front_variant(int N, int M, int *tiles, int *stages, int *splits, int *kb, int *consumer);
 
 /*
  * qkv_front_launch_variant: qkv_front (with its checks) at an explicit
- * variant, for tests and tuning.  splits in {1, 2, 4, 8, 16}; stages >= 2
- * and within the shared-memory limit; otherwise QKVF_ERR_VARIANT.
+ * variant, for tests and tuning.  splits in {1, 2, 4, 8, 16}; kb in {1, 2, 4}
+ * (0: the default) with splits * kb <= 128; stages >= 2 within the
+ * shared-memory limit; consumer one of QKVF_CONSUMER_*.  Otherwise
+ * QKVF_ERR_VARIANT.
  */
 int qkv_front_launch_variant(const uint16_t *x, const uint16_t *W, const int64_t *positions,
                              const int64_t *slots, const float *cos_sin,
                              int64_t cos_sin_rows, uint16_t *out, uint16_t *kv_cache,
                              int64_t num_pages, int M, int N, int num_kv_heads, int splits,
-                             int stages, void *stream);
+                             int stages, int kb, int consumer, void *stream);
 
 /*
  * qkv_front_prepare: set the kernel attributes (dynamic shared memory,

@@ -90,7 +90,7 @@ struct FrontParams {
 // FP32 partials reuse the start of the W ring: they are written only after
 // every consumer warp has finished reading the ring.
 struct Layout {
-    uint32_t w, x, full, empty, part, pos, slot, cs, flag, abort_flag, total;
+    uint32_t w, x, full, empty, done, tmem_slot, part, pos, slot, cs, flag, abort_flag, total;
 };
 
 __host__ __device__ inline Layout layout_of(int mt, int kb, int stages)
@@ -106,6 +106,10 @@ __host__ __device__ inline Layout layout_of(int mt, int kb, int stages)
     off += (uint32_t)stages * 8;
     L.empty = off;
     off += (uint32_t)stages * 8;
+    L.done = off;
+    off += 8;
+    L.tmem_slot = off;
+    off += 8;
     off = (off + 15u) & ~15u;
     L.pos = off;
     off += kMaxTokens * 8;
@@ -254,6 +258,91 @@ __device__ __forceinline__ void consumer_bar_sync()
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
 }
 
+// ---- tcgen05 (5th-generation tensor core, accumulator in tensor memory) ----
+
+// Shared-memory matrix descriptor of a K-major operand stored as TMA wrote it
+// with the 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr)
+{
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);   // start address / 16
+    d |= (uint64_t)1 << 16;                             // leading offset (unused when swizzled)
+    d |= (uint64_t)(1024u >> 4) << 32;                  // stride offset: one 8-row group
+    d |= (uint64_t)1 << 46;                             // descriptor version
+    d |= (uint64_t)2 << 61;                             // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor of kind::f16: BF16 A and B, FP32 accumulator, both
+// operands K-major, M x N.
+__host__ __device__ constexpr uint32_t umma_idesc_bf16(int m, int n)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
+           ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
+                                          uint32_t accumulate)
+{
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "setp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+        "}\n" ::"r"(tmem_d),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on `bar` when every tcgen05.mma this thread issued so far is done.
+__device__ __forceinline__ void umma_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+constexpr uint32_t kTmemCols = 32;   // smallest allocation; the accumulator needs 8 or 16 columns
+
+__device__ __forceinline__ void tmem_alloc(uint32_t slot_saddr)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_saddr),
+                 "n"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "n"(kTmemCols)
+                 : "memory");
+}
+
+// 32 lanes x 8 (or 16) consecutive 32-bit columns of tensor memory: thread i
+// of the warp gets lane (taddr.lane + i), columns taddr.col .. +7 (+15).
+__device__ __forceinline__ void tmem_ld_x8(uint32_t taddr, uint32_t (&r)[8])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+        "%12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
                                         uint32_t &r3)
 {
@@ -317,7 +406,10 @@ __device__ __forceinline__ uint32_t pack_bf16x2(__nv_bfloat16 lo, __nv_bfloat16 
 
 // ---- the front kernel ------------------------------------------------------
 
-template <int MT>
+// TC: the contraction runs on tcgen05 (one thread issues M=64 x N=MT x K=16
+// MMAs from the ring into a tensor-memory accumulator); otherwise on
+// mma.sync in the four consumer warps.
+template <int MT, bool TC>
 __global__ void __launch_bounds__(kThreads, 1)
     qkv_front_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                      const FrontParams p)
@@ -344,6 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sX = smem_u32(smem + L.x);
     const uint32_t full0 = smem_u32(smem + L.full);
     const uint32_t empty0 = smem_u32(smem + L.empty);
+    const uint32_t done_bar = smem_u32(smem + L.done);
     float *part = reinterpret_cast<float *>(smem + L.part);
     int64_t *s_pos = reinterpret_cast<int64_t *>(smem + L.pos);
     int64_t *s_slot = reinterpret_cast<int64_t *>(smem + L.slot);
@@ -358,15 +451,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, kConsumerWarps);
+            // released by the MMA issuer's commit (TC) or by each consumer warp
+            mbar_init(empty0 + 8 * s, TC ? 1 : kConsumerWarps);
         }
+        mbar_init(done_bar, 1);
         *s_abort = 0;
         fence_barrier_init();
         // Dependents may launch now: before their own PDL wait they read only
         // their weights, which this kernel never writes.
         griddep_launch_dependents();
     }
+    if constexpr (TC) {
+        __syncwarp();
+        if (warp == 0) tmem_alloc(smem_u32(smem + L.tmem_slot));   // whole warp, converged
+        tc_fence_before();
+    }
     __syncthreads();
+    if constexpr (TC) tc_fence_after();
+    const uint32_t tmem_d = TC ? *reinterpret_cast<volatile uint32_t *>(smem + L.tmem_slot) : 0u;
 
     if (warp == kProducerWarp) {
         // ---- produce: the W / x ring ------------------------------------
@@ -455,6 +557,55 @@ __global__ void __launch_bounds__(kThreads, 1)
                     reinterpret_cast<const float2 *>(p.cos_sin + s_pos[t] * kHeadDim)[lane];
                 reinterpret_cast<float2 *>(s_cs + t * kHeadDim)[lane] = v;
             }
+        }
+    } else if constexpr (TC) {
+        // ---- consume (tcgen05): one thread issues every MMA -----------------
+        griddep_wait();
+        if (warp == 0 && lane == 0) {
+            constexpr uint32_t idesc = umma_idesc_bf16(64, MT);
+            int s = 0;
+            uint32_t phase = 0;
+            for (int i = 0; i < steps; ++i) {
+                if (mbar_try_wait(full0 + 8 * s, phase) ||
+                    bounded_wait(full0 + 8 * s, phase, s_abort, p.wait_limit_ns, true)) {
+                    tc_fence_after();
+                    for (int b = 0; b < KB; ++b) {
+                        const uint32_t wbox = sW + (uint32_t)(s * KB + b) * kBoxBytesW;
+                        const uint32_t xbox = sX + (uint32_t)(s * KB + b) * kBoxBytesX;
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)   // K = 16 per MMA: 32 bytes along the row
+                            umma_bf16(tmem_d, umma_desc_sw128(wbox + 32u * kk),
+                                      umma_desc_sw128(xbox + 32u * kk), idesc,
+                                      (i | b | kk) != 0 ? 1u : 0u);
+                    }
+                }
+                umma_commit(empty0 + 8 * s);   // the slot is free once these MMAs have read it
+                if (++s == stages) {
+                    s = 0;
+                    phase ^= 1u;
+                }
+            }
+            umma_commit(done_bar);
+        }
+        __syncwarp();
+        // The M = 64 accumulator holds rows 16w..16w+15 in lanes 0..15 of
+        // tensor-memory sub-partition w; warp w reads its own sub-partition.
+        const bool ready = mbar_try_wait(done_bar, 0) ||
+                           bounded_wait(done_bar, 0, s_abort, p.wait_limit_ns, false);
+        (void)ready;
+        __syncwarp();
+        tc_fence_after();
+        const uint32_t taddr = tmem_d + ((uint32_t)(warp * 32) << 16);
+        uint32_t r[MT];
+        if constexpr (MT == 8)
+            tmem_ld_x8(taddr, r);
+        else
+            tmem_ld_x16(taddr, r);
+        tmem_ld_wait();
+        if (lane < 16) {
+#pragma unroll
+            for (int tok = 0; tok < MT; ++tok)
+                part[tok * kPartStride + warp * 16 + lane] = __uint_as_float(r[tok]);
         }
     } else {
         // ---- consume: mma.sync over the ring ------------------------------
@@ -545,7 +696,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             part[(tok + 1) * kPartStride + col + 8] = sum[nt][3];
         }
     }
+    if constexpr (TC) tc_fence_before();
     __syncthreads();
+    if constexpr (TC) {
+        if (warp == 0) {   // every tensor-memory read is done
+            tc_fence_after();
+            tmem_dealloc(tmem_d);
+        }
+    }
     if (S > 1) cluster_sync_all();   // every rank's partial is in its shared memory
 
     // ---- finish: reduce, round, norm, RoPE, store, insert -------------------
@@ -644,12 +802,14 @@ unsigned long long g_wait_limit_ns = 2000000000ull;
 
 using KernelFn = void (*)(CUtensorMap, CUtensorMap, FrontParams);
 
-KernelFn kernel_for(int mt)
+KernelFn kernel_for(int mt, bool tc)
 {
-    return mt == 8 ? (KernelFn)qkv_front_kernel<8> : (KernelFn)qkv_front_kernel<16>;
+    if (tc) return mt == 8 ? (KernelFn)qkv_front_kernel<8, true> : (KernelFn)qkv_front_kernel<16, true>;
+    return mt == 8 ? (KernelFn)qkv_front_kernel<8, false> : (KernelFn)qkv_front_kernel<16, false>;
 }
 constexpr int kDefaultKB = 4;          // 64-k boxes per ring stage: 256 k, 32 KB of W
-constexpr int kDefaultL2Prefetch = 0;  // W stages prefetched into L2 before the PDL wait
+constexpr int kDefaultL2Prefetch = 8;  // W stages prefetched into L2 before the PDL wait
+constexpr bool kDefaultTC = false;     // consumer: tcgen05 (true) or mma.sync
 
 int probe_device(DeviceState **out)
 {
@@ -679,8 +839,8 @@ int probe_device(DeviceState **out)
         g_encode = reinterpret_cast<EncodeTiledFn>(fn);
     }
     if (!d.prepared) {
-        for (int mt : {8, 16}) {
-            KernelFn k = kernel_for(mt);
+        for (int i = 0; i < 4; ++i) {
+            KernelFn k = kernel_for(i & 1 ? 16 : 8, i >= 2);
             if (cudaFuncSetAttribute((const void *)k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      kMaxSmemPerCta) != cudaSuccess ||
                 cudaFuncSetAttribute((const void *)k,
@@ -695,6 +855,7 @@ int probe_device(DeviceState **out)
 
 struct Variant {
     int mt, splits, stages, kb, l2_prefetch;
+    bool tc;   // tcgen05 consumer (else mma.sync)
 };
 
 int max_stages(int mt, int kb, int per_sm)
@@ -707,9 +868,9 @@ int max_stages(int mt, int kb, int per_sm)
 
 // The launch shape for N columns and M tokens on `sms` SMs.  splits: the
 // largest power of two (<= 16) that keeps heads x splits within the SM count;
-// stages: as deep as shared memory allows at the CTAs per SM this needs
-// (clusters are given two CTAs per SM so that a GPC holds whole clusters),
-// and no deeper than the CTA's number of K stages.
+// stages: as deep as shared memory allows, with one CTA per SM when each
+// head is one CTA and two per SM for clusters (so that a GPC holds whole
+// clusters), and no deeper than the CTA's number of K stages.
 Variant choose_variant(int N, int M, int sms)
 {
     Variant v;
@@ -717,11 +878,10 @@ Variant choose_variant(int N, int M, int sms)
     v.mt = M <= 8 ? 8 : 16;
     v.kb = kDefaultKB;
     v.l2_prefetch = kDefaultL2Prefetch;
+    v.tc = kDefaultTC;
     v.splits = 1;
     while (v.splits < 16 && heads * v.splits * 2 <= sms) v.splits *= 2;
-    const int ctas = heads * v.splits;
-    int per_sm = (ctas + sms - 1) / sms;
-    if (v.splits > 1 && per_sm < 2) per_sm = 2;
+    const int per_sm = v.splits > 1 ? 2 : 1;
     const int steps = kHidden / (kBoxK * v.kb) / v.splits;
     v.stages = max_stages(v.mt, v.kb, per_sm);
     if (v.stages > steps) v.stages = steps;
@@ -859,7 +1019,7 @@ int launch_front(const uint16_t *x, const uint16_t *W, const int64_t *positions,
     ++na;
     cfg.attrs = attrs;
     cfg.numAttrs = (unsigned)na;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel_for(v.mt), mw, mx, prm);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel_for(v.mt, v.tc), mw, mx, prm);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         return QKVF_ERR_CUDA;
@@ -931,7 +1091,7 @@ int qkv_front(const uint16_t *x, const uint16_t *W, const int64_t *positions,
                             num_pages, M, N, num_kv_heads, stream);
 }
 
-int qkv_front_variant(int N, int M, int *tiles, int *stages, int *splits)
+int qkv_front_variant(int N, int M, int *tiles, int *stages, int *splits, int *kb, int *consumer)
 {
     if (M < 1 || M > kMaxTokens) return QKVF_ERR_TOKENS;
     if (N < 1152 || N % 1152) return QKVF_ERR_SHAPE;
@@ -942,25 +1102,32 @@ int qkv_front_variant(int N, int M, int *tiles, int *stages, int *splits)
     if (tiles) *tiles = v.mt / 8;
     if (stages) *stages = v.stages;
     if (splits) *splits = v.splits;
+    if (kb) *kb = v.kb;
+    if (consumer) *consumer = v.tc ? QKVF_CONSUMER_TCGEN05 : QKVF_CONSUMER_MMA_SYNC;
     return QKVF_OK;
 }
 
 int qkv_front_launch_variant(const uint16_t *x, const uint16_t *W, const int64_t *positions,
                              const int64_t *slots, const float *cos_sin, int64_t cos_sin_rows,
                              uint16_t *out, uint16_t *kv_cache, int64_t num_pages, int M, int N,
-                             int num_kv_heads, int splits, int stages, void *stream)
+                             int num_kv_heads, int splits, int stages, int kb, int consumer,
+                             void *stream)
 {
     int code;
     if (check_args(x, W, positions, slots, cos_sin, cos_sin_rows, out, kv_cache, num_pages, M, N,
                    num_kv_heads, &code))
         return code;
     if (M == 0) return QKVF_OK;
+    if (consumer != QKVF_CONSUMER_DEFAULT && consumer != QKVF_CONSUMER_MMA_SYNC &&
+        consumer != QKVF_CONSUMER_TCGEN05)
+        return QKVF_ERR_VARIANT;
     Variant v;
     v.mt = M <= 8 ? 8 : 16;
     v.splits = splits;
     v.stages = stages;
-    v.kb = kDefaultKB;
+    v.kb = kb == 0 ? kDefaultKB : kb;
     v.l2_prefetch = kDefaultL2Prefetch;
+    v.tc = consumer == QKVF_CONSUMER_DEFAULT ? kDefaultTC : consumer == QKVF_CONSUMER_TCGEN05;
     if (!variant_ok(v)) return QKVF_ERR_VARIANT;
     DeviceState *d;
     int rc = probe_device(&d);

@@ -30,6 +30,8 @@ PAGE_SLOTS = 16
 SLOT_WIDTH = 128
 MAX_TOKENS = 16
 
+CONSUMER_DEFAULT, CONSUMER_MMA_SYNC, CONSUMER_TCGEN05 = 0, 1, 2
+
 STATUS_BAD_SLOT = 1
 STATUS_BAD_POSITION = 2
 STATUS_WAIT_TIMEOUT = 4
@@ -69,10 +71,9 @@ def load() -> ctypes.CDLL:
         lib.qkv_front_launch.restype = i32
         lib.qkv_front_unsupported.argtypes = front_args
         lib.qkv_front_unsupported.restype = ctypes.c_char_p
-        lib.qkv_front_launch_variant.argtypes = front_args + [i32, i32, vp]
+        lib.qkv_front_launch_variant.argtypes = front_args + [i32, i32, i32, i32, vp]
         lib.qkv_front_launch_variant.restype = i32
-        lib.qkv_front_variant.argtypes = [i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32),
-                                          ctypes.POINTER(i32)]
+        lib.qkv_front_variant.argtypes = [i32, i32] + [ctypes.POINTER(i32)] * 5
         lib.qkv_front_variant.restype = i32
         lib.qkv_front_prepare.argtypes = [i32, i32]
         lib.qkv_front_prepare.restype = i32
@@ -222,25 +223,34 @@ def launch(x, weight, positions, slots, cos_sin, kv_cache, out, stream=None):
     return out
 
 
-def launch_variant(x, weight, positions, slots, cos_sin, kv_cache, out, splits, stages,
-                   stream=None):
-    """qkv_front at an explicit (splits, stages) variant."""
+def launch_variant(x, weight, positions, slots, cos_sin, kv_cache, out, splits, stages, kb=0,
+                   consumer=CONSUMER_DEFAULT, stream=None):
+    """qkv_front at an explicit (splits, stages, kb, consumer) variant."""
     why = _tensor_reason(x, weight, positions, cos_sin, slots, kv_cache, out)
     if why is not None:
         raise ValueError(f"qkv_front does not support {why}")
     with torch.cuda.device(x.device):
         _check(load().qkv_front_launch_variant(
             *_args(x, weight, positions, slots, cos_sin, out, kv_cache), int(splits), int(stages),
-            _stream(stream)))
+            int(kb), int(consumer), _stream(stream)))
     return out
 
 
 def variant(n: int, m: int) -> tuple[int, int, int, int]:
     """(tiles, stages, splits, fixed_m) of the kernel for n columns, m rows
     (fixed_m is 0: one build serves every m of its tile count)."""
-    t, s, k = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
-    _check(load().qkv_front_variant(n, m, ctypes.byref(t), ctypes.byref(s), ctypes.byref(k)))
-    return t.value, s.value, k.value, 0
+    v = variant_full(n, m)
+    return v["tiles"], v["stages"], v["splits"], 0
+
+
+def variant_full(n: int, m: int) -> dict:
+    """Every field of the launch shape for n columns, m rows."""
+    f = [ctypes.c_int() for _ in range(5)]
+    _check(load().qkv_front_variant(n, m, *[ctypes.byref(v) for v in f]))
+    names = ("tiles", "stages", "splits", "kb", "consumer")
+    out = {k: v.value for k, v in zip(names, f)}
+    out["consumer"] = {CONSUMER_MMA_SYNC: "mma.sync", CONSUMER_TCGEN05: "tcgen05"}[out["consumer"]]
+    return out
 
 
 def prepare(n: int, num_kv_heads: int) -> None:

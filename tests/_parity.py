@@ -18,7 +18,9 @@ def device_inputs(inp: dict, device="cuda:0") -> dict:
     return {k: v.to(device) for k, v in inp.items()}
 
 
-def run_device(g: dict, splits=None, stages=None, out=None):
+def run_device(g: dict, splits=None, stages=None, out=None, kb=0, consumer=0):
+    """One call through the C ABI: the library's own variant, or an explicit
+    (splits, stages, kb, consumer) one."""
     M, N = g["x"].shape[0], g["W"].shape[0]
     if out is None:
         out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=g["x"].device)
@@ -26,7 +28,7 @@ def run_device(g: dict, splits=None, stages=None, out=None):
         qf.qkv_front(g["x"], g["W"], g["positions"], g["slots"], g["cos_sin"], g["kv_cache"], out)
     else:
         qf.launch_variant(g["x"], g["W"], g["positions"], g["slots"], g["cos_sin"], g["kv_cache"],
-                          out, splits, stages)
+                          out, splits, stages, kb=kb, consumer=consumer)
     torch.cuda.synchronize()
     return out
 
@@ -78,10 +80,11 @@ def assert_cache(inp: dict, nkv: int, cache_dev: torch.Tensor, out_bits: np.ndar
         assert_values(cache[pg, :, off, :], cache_ref[pg, :, off, :], what=f"cache slot {pg * 16 + off}")
 
 
-def check_workload(w: wl.Workload, integer_valued=False, splits=None, stages=None):
+def check_workload(w: wl.Workload, integer_valued=False, splits=None, stages=None, kb=0,
+                   consumer=0):
     inp = wl.make_inputs(w, integer_valued=integer_valued)
     g = device_inputs(inp)
-    out = run_device(g, splits, stages)
+    out = run_device(g, splits, stages, kb=kb, consumer=consumer)
     assert qf.status() == 0
     out_bits = wl.bits(out.cpu())
     out_ref, cache_ref, err = run_oracle(inp, w.num_kv_heads)

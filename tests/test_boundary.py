@@ -73,12 +73,14 @@ def test_zero_tokens_is_a_no_op(lib):
 
 
 def test_variant_and_launch_variant_refusals(lib):
-    assert lib.qkv_front_variant(1152, 0, None, None, None) == 1
-    assert lib.qkv_front_variant(1000, 4, None, None, None) == 2
-    assert lib.qkv_front_launch_variant(X, W, POS, SL, CS, 4096, OUT, CACHE, 4, 1, 1152, 1, 3, 4,
-                                        None) in (8,)
-    assert lib.qkv_front_launch_variant(X, W, POS, SL, CS, 4096, OUT, CACHE, 4, 1, 1152, 1, 1, 1,
-                                        None) == 8
+    assert lib.qkv_front_variant(1152, 0, None, None, None, None, None) == 1
+    assert lib.qkv_front_variant(1000, 4, None, None, None, None, None) == 2
+    lv = lib.qkv_front_launch_variant
+    assert lv(X, W, POS, SL, CS, 4096, OUT, CACHE, 4, 1, 1152, 1, 3, 4, 0, 0, None) == 8  # splits 3
+    assert lv(X, W, POS, SL, CS, 4096, OUT, CACHE, 4, 1, 1152, 1, 1, 1, 0, 0, None) == 8  # 1 stage
+    assert lv(X, W, POS, SL, CS, 4096, OUT, CACHE, 4, 1, 1152, 1, 1, 3, 3, 0, None) == 8  # kb 3
+    assert lv(X, W, POS, SL, CS, 4096, OUT, CACHE, 4, 1, 1152, 1, 1, 3, 0, 7, None) == 8  # consumer
+    assert lv(X, W, POS, SL, CS, 4096, OUT, CACHE, 4, 1, 1152, 1, 1, 40, 4, 0, None) == 8  # smem
     assert lib.qkv_front_set_wait_limit(5) == 9
     assert lib.qkv_front_selftest_wait(0, None) == 9
     assert lib.qkv_front_prepare(1000, 1) == 2
@@ -130,6 +132,9 @@ def test_variants_the_gpu_tests_launch_are_accepted(lib):
     cases += [(n, s, 3) for n, sl in td.SPLIT_CASES for s in sl]
     for name, splits, stages in cases:
         w = wl.WORKLOADS[name]
-        rc = lib.qkv_front_launch_variant(X, W, POS, SL, CS, 4096, OUT, CACHE, 4, w.M, w.N,
-                                          w.num_kv_heads, splits, stages, None)
-        assert rc in (5, 6), (name, splits, stages, rc)
+        for consumer in (0, 1, 2):
+            for kb in (0, 1, 2, 4):
+                rc = lib.qkv_front_launch_variant(X, W, POS, SL, CS, 4096, OUT, CACHE, 4, w.M, w.N,
+                                                  w.num_kv_heads, splits, stages, kb, consumer,
+                                                  None)
+                assert rc in (5, 6), (name, splits, stages, kb, consumer, rc)

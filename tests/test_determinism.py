@@ -51,33 +51,52 @@ def test_repeat_runs_bitwise_equal(name):
         assert torch.equal(c.view(torch.int16), caches[0].view(torch.int16))
 
 
+ENGINES = [qf.CONSUMER_MMA_SYNC, qf.CONSUMER_TCGEN05]
+
+
+@pytest.mark.parametrize("consumer", ENGINES, ids=["mma_sync", "tcgen05"])
 @pytest.mark.parametrize("name,splits", [("m8_nkv8_n9216", 1), ("m16_nkv8_n9216_consecutive", 2),
                                          ("m1_nkv1_n1152", 8)])
-def test_ring_depth_does_not_change_result(name, splits):
+def test_ring_depth_does_not_change_result(name, splits, consumer):
     w = wl.WORKLOADS[name]
     inp = wl.make_inputs(w)
     ref = None
     for stages in RING_DEPTHS:
         g = _fresh(inp)
-        out = run_device(g, splits=splits, stages=stages)
+        out = run_device(g, splits=splits, stages=stages, consumer=consumer)
         if ref is None:
             ref = out
         else:
             assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), stages
 
 
+@pytest.mark.parametrize("consumer", ENGINES, ids=["mma_sync", "tcgen05"])
 @pytest.mark.parametrize("name,splits_list", SPLIT_CASES)
-def test_every_k_split_matches_oracle(name, splits_list):
+def test_every_k_split_matches_oracle(name, splits_list, consumer):
     w = wl.WORKLOADS[name]
     inp = wl.make_inputs(w)
     out_ref, cache_ref, err = run_oracle(inp, w.num_kv_heads)
     assert err == 0
     for splits in splits_list:
         g = _fresh(inp)
-        out = run_device(g, splits=splits, stages=split_stages(splits))
+        out = run_device(g, splits=splits, stages=split_stages(splits), consumer=consumer)
         assert qf.status() == 0
         out_bits = wl.bits(out.cpu())
         assert_values(out_bits, out_ref, what=f"out at splits={splits}")
         assert_cache(inp, w.num_kv_heads, g["kv_cache"], out_bits, cache_ref)
-        again = run_device(_fresh(inp), splits=splits, stages=3)
+        again = run_device(_fresh(inp), splits=splits, stages=3, consumer=consumer)
         assert torch.equal(again.view(torch.int16), out.view(torch.int16))
+
+
+@pytest.mark.parametrize("kb", [1, 2, 4])
+def test_every_stage_size_matches_oracle(kb):
+    w = wl.WORKLOADS["m16_nkv8_n9216_consecutive"]
+    inp = wl.make_inputs(w)
+    out_ref, cache_ref, err = run_oracle(inp, w.num_kv_heads)
+    for consumer in ENGINES:
+        g = _fresh(inp)
+        out = run_device(g, splits=1, stages=3, kb=kb, consumer=consumer)
+        assert qf.status() == 0
+        out_bits = wl.bits(out.cpu())
+        assert_values(out_bits, out_ref, what=f"out at kb={kb}, consumer={consumer}")
+        assert_cache(inp, w.num_kv_heads, g["kv_cache"], out_bits, cache_ref)

@@ -31,6 +31,18 @@ def test_workload_matches_oracle(name):
     check_workload(wl.WORKLOADS[name])
 
 
+ENGINES = [qf.CONSUMER_MMA_SYNC, qf.CONSUMER_TCGEN05]
+
+
+@pytest.mark.parametrize("consumer", ENGINES, ids=["mma_sync", "tcgen05"])
+@pytest.mark.parametrize("name", list(wl.WORKLOADS))
+def test_each_engine_matches_oracle(name, consumer):
+    """Both contraction engines at the library's split and ring depth."""
+    w = wl.WORKLOADS[name]
+    v = qf.variant_full(w.N, w.M)
+    check_workload(w, splits=v["splits"], stages=v["stages"], kb=v["kb"], consumer=consumer)
+
+
 def _vg_cols(nkv):
     q_width = 8 * nkv * 64
     return slice(q_width + nkv * 64, None)   # v then gate heads
@@ -38,18 +50,23 @@ def _vg_cols(nkv):
 
 @pytest.mark.parametrize("name", ["m1_nkv1_n1152", "m8_nkv8_n9216", "m16_nkv8_n9216_consecutive",
                                   "sweep_m13_nkv8_n9216", "m8_nkv16_n18432"])
-def test_integer_inputs_bit_exact_projection(name):
+@pytest.mark.parametrize("consumer", ENGINES, ids=["mma_sync", "tcgen05"])
+def test_integer_inputs_bit_exact_projection(name, consumer):
     w = wl.WORKLOADS[name]
-    _, out_bits, out_ref = check_workload(w, integer_valued=True)
+    v = qf.variant_full(w.N, w.M)
+    _, out_bits, out_ref = check_workload(w, integer_valued=True, splits=v["splits"],
+                                          stages=v["stages"], kb=v["kb"], consumer=consumer)
     vg = _vg_cols(w.num_kv_heads)
     assert np.array_equal(out_bits[:, vg], out_ref[:, vg])
 
 
+@pytest.mark.parametrize("consumer", ENGINES, ids=["mma_sync", "tcgen05"])
 @pytest.mark.parametrize("M", list(range(1, 17)))
-def test_every_token_count_one_kv_head(M):
+def test_every_token_count_one_kv_head(M, consumer):
     """Every M from 1 to 16 (ragged 8-token tiles) at N = 1152."""
     w = wl.Workload(f"m{M}_nkv1", M=M, num_kv_heads=1, max_pos=4096, num_pages=8, seed=2000 + M)
-    check_workload(w)
+    v = qf.variant_full(w.N, w.M)
+    check_workload(w, splits=v["splits"], stages=v["stages"], kb=v["kb"], consumer=consumer)
 
 
 @pytest.mark.parametrize("nkv", [2, 3, 4])
