@@ -150,6 +150,31 @@ int qkv_front_prepare(int N, int num_kv_heads);
  */
 int qkv_front_status(unsigned int *bits);
 
+/*
+ * qkv_front_from_host: the whole call for a caller whose tokens live in host
+ * memory.  On `stream`, asynchronously: copies x [M, 8192], positions [M] and
+ * slots [M] from host memory into the caller's device `staging` buffer, runs
+ * qkv_front on them, and copies out [M, N] back to `out_host`.  Host buffers
+ * should be pinned (page-locked) for the copies to be asynchronous, and must
+ * stay valid until the stream passes the call.  W, cos_sin and kv_cache are
+ * device pointers as for qkv_front.
+ *   staging        device buffer, 256-byte aligned, at least
+ *                  qkv_front_staging_bytes(M, N) bytes; owned by the caller;
+ *                  the call overwrites it (two calls in flight on different
+ *                  streams need two buffers).
+ * Same checks and codes as qkv_front, plus QKVF_ERR_SIZES when staging is too
+ * small and QKVF_ERR_ALIGN when it is not 256-byte aligned.  The library
+ * allocates nothing.
+ */
+int qkv_front_from_host(const uint16_t *x_host, const int64_t *positions_host,
+                        const int64_t *slots_host, uint16_t *out_host, const uint16_t *W,
+                        const float *cos_sin, int64_t cos_sin_rows, uint16_t *kv_cache,
+                        int64_t num_pages, void *staging, uint64_t staging_bytes, int M, int N,
+                        int num_kv_heads, void *stream);
+
+/* Device staging bytes qkv_front_from_host needs for M tokens and N columns. */
+uint64_t qkv_front_staging_bytes(int M, int N);
+
 /* Static text of a QKVF_* return code. */
 const char *qkv_front_strerror(int code);
 

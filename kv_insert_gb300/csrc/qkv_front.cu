@@ -1155,6 +1155,67 @@ int qkv_front_status(unsigned int *bits)
     return QKVF_OK;
 }
 
+// staging layout of qkv_front_from_host: x | positions | slots | out, each
+// starting on a 256-byte boundary
+struct Staging {
+    uint64_t x, pos, slot, out, total;
+};
+
+static Staging staging_layout(int M, int N)
+{
+    auto up = [](uint64_t v) { return (v + 255u) & ~(uint64_t)255u; };
+    Staging st;
+    st.x = 0;
+    st.pos = up(st.x + (uint64_t)M * kHidden * 2);
+    st.slot = up(st.pos + (uint64_t)M * 8);
+    st.out = up(st.slot + (uint64_t)M * 8);
+    st.total = up(st.out + (uint64_t)M * N * 2);
+    return st;
+}
+
+uint64_t qkv_front_staging_bytes(int M, int N)
+{
+    if (M < 0 || M > kMaxTokens || N < 0) return 0;
+    return staging_layout(M, N).total;
+}
+
+int qkv_front_from_host(const uint16_t *x_host, const int64_t *positions_host,
+                        const int64_t *slots_host, uint16_t *out_host, const uint16_t *W,
+                        const float *cos_sin, int64_t cos_sin_rows, uint16_t *kv_cache,
+                        int64_t num_pages, void *staging, uint64_t staging_bytes, int M, int N,
+                        int num_kv_heads, void *stream)
+{
+    if (M < 0 || M > kMaxTokens) return QKVF_ERR_TOKENS;
+    if (M == 0) return QKVF_OK;
+    if (!x_host || !positions_host || !slots_host || !out_host || !staging) return QKVF_ERR_NULL;
+    if ((uintptr_t)staging % 256) return QKVF_ERR_ALIGN;
+    const Staging st = staging_layout(M, N);
+    if (staging_bytes < st.total) return QKVF_ERR_SIZES;
+    uint8_t *base = static_cast<uint8_t *>(staging);
+    const uint16_t *x = reinterpret_cast<const uint16_t *>(base + st.x);
+    const int64_t *pos = reinterpret_cast<const int64_t *>(base + st.pos);
+    const int64_t *slots = reinterpret_cast<const int64_t *>(base + st.slot);
+    uint16_t *out = reinterpret_cast<uint16_t *>(base + st.out);
+    int code;
+    if (check_args(x, W, pos, slots, cos_sin, cos_sin_rows, out, kv_cache, num_pages, M, N,
+                   num_kv_heads, &code))
+        return code;
+    const cudaStream_t s = (cudaStream_t)stream;
+    if (cudaMemcpyAsync((void *)x, x_host, (size_t)M * kHidden * 2, cudaMemcpyHostToDevice, s) !=
+            cudaSuccess ||
+        cudaMemcpyAsync((void *)pos, positions_host, (size_t)M * 8, cudaMemcpyHostToDevice, s) !=
+            cudaSuccess ||
+        cudaMemcpyAsync((void *)slots, slots_host, (size_t)M * 8, cudaMemcpyHostToDevice, s) !=
+            cudaSuccess)
+        return QKVF_ERR_CUDA;
+    const int rc = qkv_front_launch(x, W, pos, slots, cos_sin, cos_sin_rows, out, kv_cache,
+                                    num_pages, M, N, num_kv_heads, stream);
+    if (rc != QKVF_OK) return rc;
+    if (cudaMemcpyAsync(out_host, out, (size_t)M * N * 2, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return QKVF_ERR_CUDA;
+    return QKVF_OK;
+}
+
 int qkv_front_selftest_wait(int64_t timeout_ns, void *stream)
 {
     if (timeout_ns < 1 || timeout_ns > 1000000000ll) return QKVF_ERR_ARG;

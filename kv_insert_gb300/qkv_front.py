@@ -85,6 +85,11 @@ def load() -> ctypes.CDLL:
         lib.qkv_front_selftest_wait.restype = i32
         lib.qkv_front_set_wait_limit.argtypes = [i64]
         lib.qkv_front_set_wait_limit.restype = i32
+        lib.qkv_front_from_host.argtypes = [vp, vp, vp, vp, vp, vp, i64, vp, i64, vp,
+                                            ctypes.c_uint64, i32, i32, i32, vp]
+        lib.qkv_front_from_host.restype = i32
+        lib.qkv_front_staging_bytes.argtypes = [i32, i32]
+        lib.qkv_front_staging_bytes.restype = ctypes.c_uint64
         _lib = lib
         return lib
 
@@ -263,6 +268,38 @@ def status() -> int:
     v = ctypes.c_uint()
     _check(load().qkv_front_status(ctypes.byref(v)))
     return v.value
+
+
+def staging_bytes(m: int, n: int) -> int:
+    """Device staging bytes qkv_front_from_host needs for m tokens, n columns."""
+    return int(load().qkv_front_staging_bytes(m, n))
+
+
+def qkv_front_from_host(x_host, positions_host, slots_host, out_host, weight, cos_sin, kv_cache,
+                        staging, stream=None):
+    """The whole call from host buffers: x / positions / slots copied in,
+    the front run, out copied back, all on one stream in one library call.
+    Host tensors should be pinned; `staging` is a device uint8 tensor of at
+    least staging_bytes(M, N) bytes."""
+    for name, t in (("x_host", x_host), ("positions_host", positions_host),
+                    ("slots_host", slots_host), ("out_host", out_host)):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous host tensor")
+    M, N = x_host.shape[0], weight.shape[0]
+    if (x_host.dtype != torch.bfloat16 or tuple(x_host.shape) != (M, HIDDEN)
+            or out_host.dtype != torch.bfloat16 or tuple(out_host.shape) != (M, N)
+            or positions_host.dtype != torch.int64 or slots_host.dtype != torch.int64
+            or positions_host.numel() != M or slots_host.numel() != M):
+        raise ValueError("host buffers must be bf16 x [M, 8192], int64 positions / slots [M], "
+                         "bf16 out [M, N]")
+    if not staging.is_cuda or staging.device != weight.device:
+        raise ValueError("staging must be on the weights' device")
+    _check(load().qkv_front_from_host(
+        x_host.data_ptr(), positions_host.data_ptr(), slots_host.data_ptr(), out_host.data_ptr(),
+        weight.data_ptr(), cos_sin.data_ptr(), cos_sin.shape[0], kv_cache.data_ptr(),
+        kv_cache.shape[0], staging.data_ptr(), staging.numel() * staging.element_size(), M, N,
+        kv_cache.shape[1], _stream(stream)))
+    return out_host
 
 
 def selftest_wait(timeout_ns: int, stream=None) -> None:

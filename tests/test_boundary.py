@@ -138,3 +138,17 @@ def test_variants_the_gpu_tests_launch_are_accepted(lib):
                                                   w.num_kv_heads, splits, stages, kb, consumer,
                                                   None)
                 assert rc in (5, 6), (name, splits, stages, kb, consumer, rc)
+
+
+def test_from_host_refusals(lib):
+    fh = lib.qkv_front_from_host
+    need = lib.qkv_front_staging_bytes(8, 9216)
+    assert need >= 8 * 8192 * 2 + 8 * 9216 * 2 + 2 * 64
+    assert need % 256 == 0
+    args = lambda st=OUT, nbytes=need, M=8: (X, POS, SL, CACHE + (1 << 35), W, CS, 4096, CACHE, 4096,
+                                             st, nbytes, M, 9216, 8, None)
+    assert fh(*args(M=17)) == 1
+    assert fh(*args(M=0)) == 0
+    assert fh(*args(st=OUT + 16)) == 4          # staging not 256-byte aligned
+    assert fh(*args(nbytes=need - 256)) == 7    # staging too small
+    assert lib.qkv_front_staging_bytes(17, 9216) == 0

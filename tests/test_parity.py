@@ -147,3 +147,24 @@ def test_zero_tokens_launches_nothing():
                  g["kv_cache"], out)
     torch.cuda.synchronize()
     assert torch.equal(before, g["kv_cache"])
+
+
+@pytest.mark.parametrize("name", ["m8_nkv8_n9216", "sweep_m13_nkv8_n9216"])
+def test_from_host_entry_matches_device_call(name):
+    """qkv_front_from_host (host x / positions / slots in, out back to host)
+    gives the device call's bits, in out and in the cache."""
+    w = wl.WORKLOADS[name]
+    inp = wl.make_inputs(w)
+    g = device_inputs(inp)
+    out_dev = run_device(g)
+    cache_dev = g["kv_cache"].clone()
+    g2 = device_inputs(inp)
+    xh, ph, sh = inp["x"].pin_memory(), inp["positions"].pin_memory(), inp["slots"].pin_memory()
+    oh = torch.zeros(w.M, w.N, dtype=torch.bfloat16).pin_memory()
+    staging = torch.empty(qf.staging_bytes(w.M, w.N), dtype=torch.uint8, device="cuda:0")
+    for _ in range(2):
+        qf.qkv_front_from_host(xh, ph, sh, oh, g2["W"], g2["cos_sin"], g2["kv_cache"], staging)
+        torch.cuda.synchronize()
+        assert qf.status() == 0
+        assert torch.equal(oh.view(torch.int16), out_dev.cpu().view(torch.int16))
+        assert torch.equal(g2["kv_cache"].view(torch.int16), cache_dev.view(torch.int16))
