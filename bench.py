@@ -52,7 +52,11 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", default=wl.BENCH_WORKLOAD, choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--op", choices=("qkv_front", "qknorm_rope_kv_insert"), default="qkv_front",
+                    help="qkv_front: the fused decode front (the headline); qknorm_rope_kv_insert: "
+                         "the standalone epilogue on a prefill chunk")
+    ap.add_argument("--workload", default=None,
+                    choices=sorted(wl.WORKLOADS) + sorted(wl.EPI_WORKLOADS))
     ap.add_argument("--graph-calls", type=int, default=96,
                     help="calls per captured CUDA graph (a multiple of the W copies is used)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -61,6 +65,13 @@ def parse_args(argv=None):
     ap.add_argument("--ref-seconds", type=float, default=90.0,
                     help="target duration of the whole --impl reference run")
     a = ap.parse_args(argv)
+    if a.workload is None:
+        a.workload = wl.BENCH_WORKLOAD if a.op == "qkv_front" else wl.EPI_BENCH_WORKLOAD
+    table = wl.WORKLOADS if a.op == "qkv_front" else wl.EPI_WORKLOADS
+    if a.workload not in table:
+        ap.error(f"workload {a.workload} is not a {a.op} workload")
+    if a.op != "qkv_front" and a.impl == "reference":
+        ap.error("the reference arm times the fused front only")
     if a.warmup < 3:
         ap.error("--warmup must be >= 3")
     if a.steps < 1:
@@ -418,10 +429,99 @@ def run_ours(args, w: wl.Workload):
     return line
 
 
+EPI_METRIC = "qknorm_rope_kv_insert achieved HBM GB/s on a prefill chunk, 1 GPU"
+
+
+def run_epilogue(args, w):
+    """The standalone epilogue on a prefill chunk: in place on qkv copies
+    rotated past L2, CUDA-graph replays, CUDA events."""
+    from kv_insert_gb300 import qkv_front as qf
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU (the product path has no CPU fallback)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_init("nccl")
+    qf.load()
+    inp = wl.make_epi_inputs(w)
+    g = {k: v.to(dev) for k, v in inp.items()}
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    q_bytes = g["qkv"].numel() * 2
+    copies = max(2, math.ceil(3 * l2 / q_bytes))
+    qs = [g["qkv"]] + [g["qkv"].clone() for _ in range(copies - 1)]
+    torch.cuda.synchronize(dev)
+    stream = torch.cuda.Stream(device=dev)
+    per_graph = max(copies, (args.graph_calls // copies) * copies)
+
+    def call(i):
+        qf.qknorm_rope_kv_insert(qs[i % copies], g["positions"], g["slots"], g["cos_sin"],
+                                 g["kv_cache"])
+
+    def capture(n):
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(n):
+                call(i)
+        return graph
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            call(i)
+    stream.synchronize()
+    full, rem = divmod(args.steps, per_graph)
+    g_full = capture(per_graph) if full else None
+    g_rem = capture(rem) if rem else None
+    with torch.cuda.stream(stream):
+        for gr in (g_full, g_rem):
+            if gr:
+                gr.replay()
+    stream.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(full):
+            g_full.replay()
+        if g_rem:
+            g_rem.replay()
+        end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clocks = sampler.stop()
+    el_max = max_over_ranks(start.elapsed_time(end) / 1e3, dev)
+    if qf.status():
+        raise RuntimeError("device status raised in the timed region")
+    res = aggregate(w.roofline_bytes(), args.steps, world, el_max)
+    if rank != 0:
+        return None
+    peak, peak_kind = hbm_peak()
+    achieved = w.roofline_bytes() / (el_max / args.steps) / 1e9
+    return {"metric": EPI_METRIC, "value": res["value"], "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
+            "us_per_call": res["us_per_call"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": dict(w.describe(), **{
+                "l2": f"inputs larger than L2: qkv rotated over {copies} copies of "
+                      f"{q_bytes / 1e6:.1f} MB (L2 {l2 / 1e6:.1f} MB)",
+                "graph_calls": per_graph, "parallelism": f"replicas x{world}"}),
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_kind": peak_kind, "traffic": None,
+                         "bytes_per_launch": w.roofline_bytes()},
+            "gpu_launches": args.steps, "clocks": clocks, "e2e": None}
+
+
 def main(argv=None):
     args = parse_args(argv)
-    w = wl.WORKLOADS[args.workload]
-    line = run_reference(args, w) if args.impl == "reference" else run_ours(args, w)
+    if args.op == "qknorm_rope_kv_insert":
+        line = run_epilogue(args, wl.EPI_WORKLOADS[args.workload])
+    else:
+        w = wl.WORKLOADS[args.workload]
+        line = run_reference(args, w) if args.impl == "reference" else run_ours(args, w)
     if line is not None:
         print(json.dumps(line), flush=True)
     if torch.distributed.is_initialized():

@@ -175,6 +175,32 @@ int qkv_front_from_host(const uint16_t *x_host, const int64_t *positions_host,
 /* Device staging bytes qkv_front_from_host needs for M tokens and N columns. */
 uint64_t qkv_front_staging_bytes(int M, int N);
 
+/*
+ * qknorm_rope_kv_insert: the unfused epilogue on its own, for any number of
+ * tokens (fused_muse_spark_qknorm_rope_kv_insert, the kernel the fused front
+ * replaces: page qkv_front, module docstring; page cute_ops, qkv_front
+ * paragraph).  In place on a BF16 projection output:
+ *   qkv        [T, N] bf16 bits, rows [q | k | v | gate]; every q and k head
+ *              is normed and rotated (same arithmetic as qkv_front), v and
+ *              gate heads are not touched.
+ *   positions, slots, cos_sin, cos_sin_rows, kv_cache, num_pages, N,
+ *   num_kv_heads: as for qkv_front, with T entries in positions and slots.
+ *   T          0 .. 2^24 tokens (0: no launch).
+ * Each token's k head g goes to the K half and v head g to the V half of its
+ * slot.  Out-of-range positions and slots follow qkv_front's rules and raise
+ * the same status bits.  Launched with PDL like qkv_front (it waits for the
+ * previous kernel before reading anything).  Allocates nothing.
+ */
+int qknorm_rope_kv_insert(uint16_t *qkv, const int64_t *positions, const int64_t *slots,
+                          const float *cos_sin, int64_t cos_sin_rows, uint16_t *kv_cache,
+                          int64_t num_pages, int T, int N, int num_kv_heads, void *stream);
+
+/* Why qknorm_rope_kv_insert would refuse this call, or NULL (host checks only). */
+const char *qknorm_rope_kv_insert_unsupported(uint16_t *qkv, const int64_t *positions,
+                                              const int64_t *slots, const float *cos_sin,
+                                              int64_t cos_sin_rows, uint16_t *kv_cache,
+                                              int64_t num_pages, int T, int N, int num_kv_heads);
+
 /* Static text of a QKVF_* return code. */
 const char *qkv_front_strerror(int code);
 

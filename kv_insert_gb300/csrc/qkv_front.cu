@@ -404,6 +404,24 @@ __device__ __forceinline__ uint32_t pack_bf16x2(__nv_bfloat16 lo, __nv_bfloat16 
     return (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
 }
 
+// ---- the q / k head epilogue (shared by both kernels) ----------------------
+// Lane l holds the BF16 values (f0, f1) of head columns 2l, 2l+1 and the
+// cos / sin of pair l.  Weightless RMS norm over the 64 columns (butterfly sum:
+// every lane ends with the same bits), then the interleaved rotation of the
+// lane's pair, rounded to BF16.  The whole warp must call it.
+__device__ __forceinline__ uint32_t qk_norm_rope_pair(float f0, float f1, float c, float sn)
+{
+    float ss = __fadd_rn(__fmul_rn(f0, f0), __fmul_rn(f1, f1));
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, off));
+    const float ms = __fdiv_rn(ss, (float)kHeadDim);
+    const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, kEps)));
+    const float a = __fmul_rn(f0, r), b = __fmul_rn(f1, r);
+    const float y0 = __fsub_rn(__fmul_rn(a, c), __fmul_rn(b, sn));
+    const float y1 = __fadd_rn(__fmul_rn(b, c), __fmul_rn(a, sn));
+    return pack_bf16x2(__float2bfloat16_rn(y0), __float2bfloat16_rn(y1));
+}
+
 // ---- the front kernel ------------------------------------------------------
 
 // TC: the contraction runs on tcgen05 (one thread issues M=64 x N=MT x K=16
@@ -729,23 +747,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t word;
         if (kind == kQ || kind == kK) {
             if (!(flag & 1)) continue;   // no table row for this position: nothing written
-            const float f0 = __bfloat162float(p0), f1 = __bfloat162float(p1);
-            // weightless RMS norm over the head's 64 columns (butterfly sum:
-            // every lane ends with the same bits)
-            float ss = __fadd_rn(__fmul_rn(f0, f0), __fmul_rn(f1, f1));
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1)
-                ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, off));
-            const float ms = __fdiv_rn(ss, (float)kHeadDim);
-            const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, kEps)));
-            const float a = __fmul_rn(f0, r), b = __fmul_rn(f1, r);
-            // interleaved RoPE: pair (2 lane, 2 lane + 1), cos in column lane,
-            // sin in column 32 + lane of the position's row
-            const float c = s_cs[u * kHeadDim + lane];
-            const float sn = s_cs[u * kHeadDim + 32 + lane];
-            const float y0 = __fsub_rn(__fmul_rn(a, c), __fmul_rn(b, sn));
-            const float y1 = __fadd_rn(__fmul_rn(b, c), __fmul_rn(a, sn));
-            word = pack_bf16x2(__float2bfloat16_rn(y0), __float2bfloat16_rn(y1));
+            // norm and RoPE: pair (2 lane, 2 lane + 1), cos in column lane, sin
+            // in column 32 + lane of the position's row
+            word = qk_norm_rope_pair(__bfloat162float(p0), __bfloat162float(p1),
+                                     s_cs[u * kHeadDim + lane], s_cs[u * kHeadDim + 32 + lane]);
         } else {
             word = pack_bf16x2(p0, p1);
         }
@@ -1028,6 +1033,8 @@ int launch_front(const uint16_t *x, const uint16_t *W, const int64_t *positions,
 }
 
 }  // namespace qkvf
+
+#include "qknorm_rope_kv_insert.cuh"
 
 using namespace qkvf;
 

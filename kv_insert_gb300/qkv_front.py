@@ -90,6 +90,11 @@ def load() -> ctypes.CDLL:
         lib.qkv_front_from_host.restype = i32
         lib.qkv_front_staging_bytes.argtypes = [i32, i32]
         lib.qkv_front_staging_bytes.restype = ctypes.c_uint64
+        epi_args = [vp, vp, vp, vp, i64, vp, i64, i32, i32, i32]
+        lib.qknorm_rope_kv_insert.argtypes = epi_args + [vp]
+        lib.qknorm_rope_kv_insert.restype = i32
+        lib.qknorm_rope_kv_insert_unsupported.argtypes = epi_args
+        lib.qknorm_rope_kv_insert_unsupported.restype = ctypes.c_char_p
         _lib = lib
         return lib
 
@@ -98,7 +103,7 @@ def header_functions() -> list[str]:
     """Names of the functions include/qkvfront.h declares."""
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(qkv_front\w*)\s*\(", text)))
+    return sorted(set(re.findall(r"\b((?:qkv_front|qknorm_rope_kv_insert)\w*)\s*\(", text)))
 
 
 def strerror(code: int) -> str:
@@ -300,6 +305,56 @@ def qkv_front_from_host(x_host, positions_host, slots_host, out_host, weight, co
         kv_cache.shape[0], staging.data_ptr(), staging.numel() * staging.element_size(), M, N,
         kv_cache.shape[1], _stream(stream)))
     return out_host
+
+
+def _epi_reason(qkv, positions, slots, cos_sin, kv_cache):
+    if not all(t.is_cuda for t in (qkv, positions, slots, cos_sin, kv_cache)):
+        return "tensors on a CUDA device"
+    if any(t.device != qkv.device for t in (positions, slots, cos_sin, kv_cache)):
+        return "tensors on different devices"
+    if qkv.dtype != torch.bfloat16 or qkv.dim() != 2 or not qkv.is_contiguous():
+        return "qkv other than a contiguous bf16 [tokens, N]"
+    T = qkv.shape[0]
+    for name, t in (("positions", positions), ("slots", slots)):
+        if t.dtype != torch.int64 or t.dim() != 1 or t.shape[0] != T or not t.is_contiguous():
+            return f"{name} other than contiguous int64 [{T}]"
+    if (cos_sin.dtype != torch.float32 or cos_sin.dim() != 2 or cos_sin.shape[1] != HEAD_DIM
+            or not cos_sin.is_contiguous()):
+        return "a rotary table other than a contiguous fp32 [*, 64] one"
+    if not kv_cache_layout_ok(kv_cache):
+        return "a KV cache other than contiguous bf16 [pages, num_kv_heads, 16, 128]"
+    if not supports_shape(qkv.shape[1], kv_cache.shape[1]):
+        return f"{qkv.shape[1]} columns for {kv_cache.shape[1]} KV heads"
+    return None
+
+
+def _epi_args(qkv, positions, slots, cos_sin, kv_cache):
+    return (qkv.data_ptr(), positions.data_ptr(), slots.data_ptr(), cos_sin.data_ptr(),
+            cos_sin.shape[0], kv_cache.data_ptr(), kv_cache.shape[0], qkv.shape[0], qkv.shape[1],
+            kv_cache.shape[1])
+
+
+def qknorm_rope_kv_insert_unsupported(qkv, positions, slots, cos_sin, kv_cache) -> str | None:
+    """Why the standalone epilogue cannot take this call, or None."""
+    why = _epi_reason(qkv, positions, slots, cos_sin, kv_cache)
+    if why is not None:
+        return why
+    with torch.cuda.device(qkv.device):
+        r = load().qknorm_rope_kv_insert_unsupported(*_epi_args(qkv, positions, slots, cos_sin,
+                                                                 kv_cache))
+    return None if r is None else r.decode()
+
+
+def qknorm_rope_kv_insert(qkv, positions, slots, cos_sin, kv_cache, stream=None):
+    """In place on a bf16 projection output qkv [T, N]: q and k heads normed and
+    rotated, each token's k / v heads inserted into kv_cache.  Returns qkv."""
+    why = _epi_reason(qkv, positions, slots, cos_sin, kv_cache)
+    if why is not None:
+        raise ValueError(f"qknorm_rope_kv_insert does not support {why}")
+    with torch.cuda.device(qkv.device):
+        _check(load().qknorm_rope_kv_insert(*_epi_args(qkv, positions, slots, cos_sin, kv_cache),
+                                            _stream(stream)))
+    return qkv
 
 
 def selftest_wait(timeout_ns: int, stream=None) -> None:

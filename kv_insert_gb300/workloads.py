@@ -163,3 +163,66 @@ def from_bits(a: np.ndarray) -> torch.Tensor:
     """CPU bf16 tensor with the given uint16 bit patterns."""
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint16).view(np.int16)).view(
         torch.bfloat16)
+
+
+# ---- the standalone epilogue (unfused path; any number of tokens) -----------
+
+@dataclasses.dataclass(frozen=True)
+class EpiWorkload:
+    """Tokens of one prefill chunk: a BF16 projection output qkv [T, N] to be
+    normed, rotated and inserted; positions p0..p0+T-1 and consecutive slots
+    starting at a random page (one request's pages, in order)."""
+    name: str
+    T: int
+    num_kv_heads: int
+    max_pos: int
+    num_pages: int
+    seed: int
+    qkv_std: float = 1.0
+
+    @property
+    def N(self) -> int:
+        return columns_for(self.num_kv_heads)
+
+    def roofline_bytes(self) -> int:
+        """Algorithmic HBM bytes of one call: q/k/v heads read, q/k heads and
+        K/V slot halves written, a table row and two indices per token."""
+        head = HEAD_DIM * 2
+        per_token = (9 + 1 + 9 + 2) * self.num_kv_heads * head + HEAD_DIM * 4 + 16
+        return self.T * per_token
+
+    def describe(self) -> dict:
+        return {"workload": self.name, "T": self.T, "N": self.N, "num_kv_heads": self.num_kv_heads,
+                "head_dim": HEAD_DIM, "cos_sin_rows": self.max_pos, "cache_pages": self.num_pages}
+
+
+EPI_WORKLOADS: dict[str, EpiWorkload] = {}
+for _w in (EpiWorkload("epi_t17_nkv1", T=17, num_kv_heads=1, max_pos=4096, num_pages=16, seed=3001),
+           EpiWorkload("epi_t1000_nkv8", T=1000, num_kv_heads=8, max_pos=32768, num_pages=1024,
+                       seed=3002, qkv_std=3.0),
+           EpiWorkload("prefill_t4096_nkv8", T=4096, num_kv_heads=8, max_pos=32768, num_pages=4096,
+                       seed=3003),
+           EpiWorkload("prefill_t8192_nkv16", T=8192, num_kv_heads=16, max_pos=131072,
+                       num_pages=8192, seed=3004)):
+    EPI_WORKLOADS[_w.name] = _w
+
+EPI_BENCH_WORKLOAD = "prefill_t4096_nkv8"
+
+
+def make_epi_inputs(w: EpiWorkload) -> dict:
+    """CPU tensors: qkv (bf16 [T, N], N(0, qkv_std^2)), positions, slots (int64),
+    cos_sin (fp32), kv_cache (bf16, pre-filled N(0, 1))."""
+    g = torch.Generator().manual_seed(w.seed)
+    qkv = (torch.randn(w.T, w.N, generator=g) * w.qkv_std).to(torch.bfloat16)
+    p0 = int(torch.randint(0, w.max_pos - w.T + 1, (1,), generator=g))
+    positions = torch.arange(p0, p0 + w.T, dtype=torch.int64)
+    pages_needed = (w.T + PAGE_SLOTS - 1) // PAGE_SLOTS + 1
+    first_page = int(torch.randint(0, w.num_pages - pages_needed + 1, (1,), generator=g))
+    o = int(torch.randint(0, PAGE_SLOTS, (1,), generator=g))
+    slots = torch.arange(first_page * PAGE_SLOTS + o, first_page * PAGE_SLOTS + o + w.T,
+                         dtype=torch.int64)
+    cos_sin = rope_table(w.max_pos)
+    kv_cache = torch.randn(w.num_pages, w.num_kv_heads, PAGE_SLOTS, SLOT_WIDTH,
+                           generator=g).to(torch.bfloat16)
+    return {"qkv": qkv, "positions": positions, "slots": slots, "cos_sin": cos_sin,
+            "kv_cache": kv_cache}

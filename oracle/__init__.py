@@ -73,6 +73,8 @@ def _load():
         lib.oracle_qkv_front.argtypes = [vp, vp, vp, vp, vp, i64, vp, vp, i64,
                                          i32, i32, i32, i32, vp]
         lib.oracle_qkv_front.restype = i32
+        lib.oracle_qknorm_rope_kv_insert.argtypes = [vp, vp, vp, vp, i64, vp, i64, i32, i32, i32]
+        lib.oracle_qknorm_rope_kv_insert.restype = i32
         _lib = lib
         return lib
 
@@ -182,3 +184,22 @@ def qkv_front(x_bits, w_bits, positions, slots, cos_sin, kv_cache_bits, num_kv_h
                                    cs.shape[0], _ptr(out), _ptr(kv_cache_bits), num_pages,
                                    M, N, K, num_kv_heads, _ptr(acc))
     return out, int(err)
+
+
+def qknorm_rope_kv_insert(qkv_bits, positions, slots, cos_sin, kv_cache_bits, num_kv_heads):
+    """The unfused epilogue on a BF16 projection output.  Returns
+    ``(qkv_out_bits [T, N], err)``; ``kv_cache_bits`` is updated in place and
+    ``qkv_bits`` is left unchanged (the result is a copy)."""
+    q = _c(qkv_bits, np.uint16).copy()
+    pos = _c(np.asarray(positions, dtype=np.int64), np.int64)
+    sl = _c(np.asarray(slots, dtype=np.int64), np.int64)
+    cs = _c(cos_sin, np.float32)
+    if not kv_cache_bits.flags.c_contiguous or kv_cache_bits.dtype != np.uint16:
+        raise TypeError("cache must be a contiguous uint16 array")
+    T, N = q.shape
+    if T == 0:
+        return q, 0
+    err = _load().oracle_qknorm_rope_kv_insert(_ptr(q), _ptr(pos), _ptr(sl), _ptr(cs), cs.shape[0],
+                                               _ptr(kv_cache_bits), kv_cache_bits.shape[0], T, N,
+                                               num_kv_heads)
+    return q, int(err)

@@ -215,3 +215,47 @@ int oracle_qkv_front(const uint16_t *x, const uint16_t *W, const int64_t *positi
     }
     return err;
 }
+
+/* ---- the unfused epilogue on its own ---------------------------------------
+ * fused_muse_spark_qknorm_rope_kv_insert, the kernel the front replaces
+ * (qkv_front page, module docstring; cute_ops page, qkv_front paragraph): on a
+ * BF16 projection output qkv [T, N] (rows [q | k | v | gate]), in place, every
+ * q and k head is normed and rotated and rounded to BF16; v and gate heads are
+ * left as they are; each token's k and v heads go into its cache slot.  The
+ * same steps as the front after its rounding, for any number of tokens.
+ * Returns 0 or an OR of ORACLE_ERR_* bits (same rules as oracle_qkv_front). */
+int oracle_qknorm_rope_kv_insert(uint16_t *qkv, const int64_t *positions, const int64_t *slots,
+                                 const float *cos_sin, int64_t cos_rows, uint16_t *kv_cache,
+                                 int64_t num_pages, int T, int N, int num_kv_heads)
+{
+    if (num_kv_heads < 1 || N != 2 * (ORACLE_Q_PER_KV + 1) * num_kv_heads * ORACLE_HEAD_DIM)
+        return ORACLE_ERR_SHAPE;
+    int err = 0;
+    int heads = N / ORACLE_HEAD_DIM;
+    float p[ORACLE_HEAD_DIM], u[ORACLE_HEAD_DIM], y[ORACLE_HEAD_DIM];
+    for (int t = 0; t < T; ++t) {
+        int64_t pos = positions[t];
+        int pos_ok = pos >= 0 && pos < cos_rows;
+        if (!pos_ok) err |= ORACLE_ERR_POSITION;
+        uint16_t *row = qkv + (size_t)t * N;
+        for (int h = 0; h < heads; ++h) {
+            int kind = oracle_head_kind(h, num_kv_heads);
+            if (kind != ORACLE_HEAD_Q && kind != ORACLE_HEAD_K) continue;
+            if (!pos_ok) continue;
+            uint16_t *o = row + (size_t)h * ORACLE_HEAD_DIM;
+            for (int j = 0; j < ORACLE_HEAD_DIM; ++j) p[j] = oracle_bf16_to_f32(o[j]);
+            oracle_rms_norm_head(p, ORACLE_EPS, u);
+            oracle_rope_head(u, cos_sin + (size_t)pos * ORACLE_HEAD_DIM, y);
+            for (int j = 0; j < ORACLE_HEAD_DIM; ++j) o[j] = oracle_f32_to_bf16(y[j]);
+        }
+        int64_t slot = slots[t];
+        if (slot < 0) continue;
+        if (slot >= num_pages * ORACLE_PAGE_SLOTS) {
+            err |= ORACLE_ERR_SLOT;
+            continue;
+        }
+        if (!pos_ok) continue;
+        oracle_kv_insert_token(row, slot, kv_cache, num_kv_heads);
+    }
+    return err;
+}

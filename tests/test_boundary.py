@@ -152,3 +152,23 @@ def test_from_host_refusals(lib):
     assert fh(*args(st=OUT + 16)) == 4          # staging not 256-byte aligned
     assert fh(*args(nbytes=need - 256)) == 7    # staging too small
     assert lib.qkv_front_staging_bytes(17, 9216) == 0
+
+
+def test_standalone_epilogue_refusals(lib):
+    f = lib.qknorm_rope_kv_insert
+    base = dict(qkv=X, pos=POS, sl=SL, cs=CS, rows=4096, cache=CACHE, pages=64, T=100, N=9216, nkv=8)
+
+    def call(**kw):
+        a = dict(base, **kw)
+        return f(a["qkv"], a["pos"], a["sl"], a["cs"], a["rows"], a["cache"], a["pages"], a["T"],
+                 a["N"], a["nkv"], None)
+    assert call(T=-1) == 1 and call(T=(1 << 24) + 1) == 1
+    assert call(N=1152) == 2 and call(nkv=0) == 2
+    assert call(qkv=0) == 3 and call(sl=0) == 3
+    assert call(qkv=X + 4) == 4 and call(pos=POS + 4) == 4
+    assert call(rows=0) == 7 and call(pages=0) == 7
+    assert call(cs=X + 128) == 9                     # table inside qkv
+    assert call(T=0, qkv=0) == 0
+    assert call() in (5, 6)                          # valid: reaches the device query
+    why = lib.qknorm_rope_kv_insert_unsupported(X, POS, SL, CS, 4096, CACHE, 64, 100, 1152, 8)
+    assert why is not None and b"1152" in why

@@ -412,3 +412,56 @@ def test_full_refuses_bad_shape(oracle_lib):
     W = np.zeros((1000, 4), np.uint16)
     _, err = oracle.qkv_front(x, W, [0], [0], np.zeros((1, 64), np.float32), cache, 1)
     assert err == oracle.ERR_SHAPE
+
+
+# ---- the unfused epilogue ----------------------------------------------------
+
+def test_unfused_epilogue_composes_to_the_front(oracle_lib):
+    """qkv_front page, module docstring: the front writes what the projection
+    GEMM followed by fused_muse_spark_qknorm_rope_kv_insert writes.  With the
+    same summation order both sides are bitwise equal: out and cache."""
+    w = wl.Workload("compose", M=5, num_kv_heads=2, max_pos=512, num_pages=8, seed=31)
+    inp = wl.make_inputs(w)
+    xb, Wb = wl.bits(inp["x"]), wl.bits(inp["W"])
+    pos, sl, cs = inp["positions"].numpy(), inp["slots"].numpy(), inp["cos_sin"].numpy()
+    cache_a = wl.bits(inp["kv_cache"]).copy()
+    out_a, err_a = oracle.qkv_front(xb, Wb, pos, sl, cs, cache_a, 2)
+    p = oracle.f32_to_bf16_bits(oracle.project_f32(xb, Wb))
+    cache_b = wl.bits(inp["kv_cache"]).copy()
+    out_b, err_b = oracle.qknorm_rope_kv_insert(p, pos, sl, cs, cache_b, 2)
+    assert err_a == err_b == 0
+    assert np.array_equal(out_a, out_b)
+    assert np.array_equal(cache_a, cache_b)
+
+
+def test_unfused_epilogue_leaves_v_and_gate(oracle_lib):
+    """v and gate heads of the projection output are not touched; q and k
+    heads are (the identity row makes them normed copies: RMS 1)."""
+    rng = np.random.default_rng(8)
+    nkv, T = 1, 3
+    N = wl.columns_for(nkv)
+    qkv = _bf(rng.standard_normal((T, N)) * 3).reshape(T, N)
+    cs = _row(np.ones(32), np.zeros(32))[None, :]
+    cache = np.zeros((1, nkv, 16, 128), np.uint16)
+    out, err = oracle.qknorm_rope_kv_insert(qkv, [0, 0, 0], [-1, -1, -1], cs, cache, nkv)
+    assert err == 0
+    assert np.array_equal(out[:, 9 * 64:], qkv[:, 9 * 64:])
+    assert not np.array_equal(out[:, :9 * 64], qkv[:, :9 * 64])
+    vals = wl.from_bits(out[:, :9 * 64]).double().numpy().reshape(T, 9, 64)
+    rms = np.sqrt(np.mean(vals ** 2, axis=2))
+    assert np.all(np.abs(rms - 1.0) < 1e-2)
+    assert not cache.any()
+
+
+def test_unfused_epilogue_index_rules(oracle_lib):
+    nkv, T = 1, 4
+    N = wl.columns_for(nkv)
+    rng = np.random.default_rng(9)
+    qkv = _bf(rng.standard_normal((T, N))).reshape(T, N)
+    cs = wl.rope_table(8).numpy()
+    cache = np.zeros((2, nkv, 16, 128), np.uint16)
+    out, err = oracle.qknorm_rope_kv_insert(qkv, [1, 9, 2, 3], [0, 1, 40, -1], cs, cache, nkv)
+    assert err == oracle.ERR_POSITION | oracle.ERR_SLOT
+    assert np.array_equal(out[1], qkv[1])               # bad position: row untouched
+    assert np.any(cache[0, 0, 0]) and not np.any(cache[0, 0, 1])   # slot 1 skipped
+    assert not np.any(cache[1])                         # slot 40 out of range, -1 padding
