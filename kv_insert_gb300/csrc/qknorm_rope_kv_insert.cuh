@@ -14,11 +14,11 @@
 // does not take (prefill, batches above 16).
 //
 // HBM-bound elementwise work: per token it reads the 9 nkv q/k heads and the
-// nkv v heads (128 B each) and writes the q/k heads back and 2 nkv slot
-// halves.  One warp per task of 4 heads of a token, 16 bytes per lane; tasks
-// are dealt to warps kEpiUnroll at a time and the loads of a round are issued
-// before any is used (head values first, then indices, then table rows), so
-// each warp keeps several 512-byte requests in flight.
+// nkv v heads (contiguous in the row: 1280 nkv bytes) and its cos|sin row,
+// and writes the q/k heads back and 2 nkv slot halves.  A producer warp
+// streams whole token regions into a shared-memory ring with bulk copies
+// (up to ~100 KB in flight per CTA, two CTAs per SM); consumer warps work
+// from shared memory, 16 bytes per lane.
 
 namespace qkvf {
 
@@ -30,14 +30,37 @@ struct EpiParams {
     uint16_t *kv_cache;
     int64_t cos_rows;
     int64_t num_pages;
+    unsigned long long wait_limit_ns;
     int T;
     int N;
     int nkv;
 };
 
-constexpr int kEpiThreads = 256;
-constexpr int kEpiUnroll = 3;            // head groups per warp per round, loads issued first
+constexpr int kEpiConsumerWarps = 8;
+constexpr int kEpiThreads = 32 * (kEpiConsumerWarps + 1);   // warp 0 produces
 constexpr int kEpiMaxTokens = 1 << 24;
+constexpr int kEpiRingBudget = 100 * 1024;   // two CTAs per SM
+constexpr int kEpiMaxSlots = 16;
+
+// bytes of one token's ring slot: its q | k | v heads, its cos|sin row, and a
+// 32-byte header (position, slot, flags), rounded to 128 bytes
+__host__ __device__ inline uint32_t epi_slot_bytes(int nkv)
+{
+    const uint32_t region = (uint32_t)(kQPerKv + 2) * nkv * kHeadDim * 2;
+    return (region + kHeadDim * 4 + 32 + 127u) & ~127u;
+}
+
+__host__ __device__ inline int epi_slots(int nkv)
+{
+    int n = kEpiRingBudget / (int)epi_slot_bytes(nkv);
+    return n < 2 ? 2 : (n > kEpiMaxSlots ? kEpiMaxSlots : n);
+}
+
+__host__ __device__ inline uint32_t epi_smem_bytes(int nkv)
+{
+    // slots, then full and empty barriers and the abort flag, plus alignment slack
+    return (uint32_t)epi_slots(nkv) * epi_slot_bytes(nkv) + 2 * kEpiMaxSlots * 8 + 16 + 128;
+}
 
 // Sum of squares of one head held as 8 lanes x 8 values, in exactly the
 // association of the fused front's warp butterfly (qk_norm_rope_pair), so
@@ -59,115 +82,170 @@ __device__ __forceinline__ float head_sum_sq_front_order(const float (&f)[8])
     return __fadd_rn(__fadd_rn(s[0], s[2]), __fadd_rn(s[1], s[3]));
 }
 
-// One warp per task of 4 consecutive heads of one token (q, k or v heads;
-// gate heads need nothing): lane l handles head 4 g + l / 8, columns
-// 8 (l % 8) .. 8 (l % 8) + 7, as one 16-byte access.
-__global__ void __launch_bounds__(kEpiThreads, 3) qknorm_rope_kv_insert_kernel(const EpiParams p)
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
 {
-    griddep_wait();   // qkv, indices and table are written by the kernels before this one
-    if (threadIdx.x == 0) griddep_launch_dependents();
-    const int lane = threadIdx.x & 31;
-    const int sub = lane >> 3, chunk = lane & 7;
-    const int64_t warp_id = ((int64_t)blockIdx.x * kEpiThreads + threadIdx.x) >> 5;
-    const int64_t nwarps = ((int64_t)gridDim.x * kEpiThreads) >> 5;
-    const int q_heads = kQPerKv * p.nkv;
-    const int qk_heads = q_heads + p.nkv;
-    const int heads = qk_heads + p.nkv;          // q, k and v heads
-    const int groups = (heads + 3) >> 2;         // per token
-    const int64_t total = (int64_t)p.T * groups;
-    const int64_t slot_end = p.num_pages * (int64_t)kPageSlots;
-    unsigned bad = 0u;
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
 
-    for (int64_t base = warp_id * kEpiUnroll; base < total; base += nwarps * kEpiUnroll) {
-        int tok[kEpiUnroll], head[kEpiUnroll];
-        uint4 val[kEpiUnroll];
-        int64_t pos[kEpiUnroll], slot[kEpiUnroll];
-        float4 cv[kEpiUnroll], sv[kEpiUnroll];
-        // the head values first: they depend on nothing
-#pragma unroll
-        for (int u = 0; u < kEpiUnroll; ++u) {
-            const int64_t task = base + u;
-            const bool in = task < total;
-            tok[u] = in ? (int)(task / groups) : 0;
-            head[u] = in ? (int)(task % groups) * 4 + sub : heads;   // heads: nothing to do
-            val[u] = make_uint4(0u, 0u, 0u, 0u);
-            if (head[u] < heads)
-                val[u] = *reinterpret_cast<const uint4 *>(p.qkv + (size_t)tok[u] * p.N +
-                                                          (size_t)head[u] * kHeadDim + 8 * chunk);
+// CTA b takes tokens b, b + G, b + 2G, ... (G = gridDim.x).  Warp 0 copies
+// each token's q | k | v region (contiguous in its row) and its cos|sin row
+// into a ring slot with bulk copies; warps 1..8 take the token's heads in
+// groups of 4 (lane l: head 4 g + l / 8, columns 8 (l % 8) .. + 7), norm and
+// rotate q / k heads in place in global memory and write k / v heads into the
+// cache slot.
+__global__ void __launch_bounds__(kEpiThreads, 2) qknorm_rope_kv_insert_kernel(const EpiParams p)
+{
+    extern __shared__ uint8_t epi_smem_dyn[];
+    uint8_t *smem = epi_smem_dyn + ((128u - (smem_u32(epi_smem_dyn) & 127u)) & 127u);
+    const int nkv = p.nkv;
+    const uint32_t slot_bytes = epi_slot_bytes(nkv);
+    const int nslots = epi_slots(nkv);
+    const uint32_t region = (uint32_t)(kQPerKv + 2) * nkv * kHeadDim * 2;
+    const uint32_t full0 = smem_u32(smem + nslots * slot_bytes);
+    const uint32_t empty0 = full0 + 8 * kEpiMaxSlots;
+    volatile int *s_abort = reinterpret_cast<volatile int *>(smem + nslots * slot_bytes + 16 * kEpiMaxSlots);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t G = gridDim.x;
+    const int q_heads = kQPerKv * nkv, qk_heads = q_heads + nkv, heads = qk_heads + nkv;
+    const int groups = (heads + 3) >> 2;
+    const int64_t slot_end = p.num_pages * (int64_t)kPageSlots;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < nslots; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, kEpiConsumerWarps);
         }
-#pragma unroll
-        for (int u = 0; u < kEpiUnroll; ++u) {
-            pos[u] = -1;
-            slot[u] = -1;
-            if (base + u < total) {
-                pos[u] = p.positions[tok[u]];
-                slot[u] = p.slots[tok[u]];
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < kEpiUnroll; ++u) {
-            cv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-            sv[u] = cv[u];
-            const bool pos_ok = pos[u] >= 0 && pos[u] < p.cos_rows;
-            if (head[u] < qk_heads && pos_ok) {
-                const float *row = p.cos_sin + pos[u] * kHeadDim;
-                cv[u] = *reinterpret_cast<const float4 *>(row + 4 * chunk);
-                sv[u] = *reinterpret_cast<const float4 *>(row + 32 + 4 * chunk);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < kEpiUnroll; ++u) {
-            if (base + u >= total) continue;   // the same for every lane of the warp
-            const bool pos_ok = pos[u] >= 0 && pos[u] < p.cos_rows;
-            const bool ins = slot[u] >= 0 && slot[u] < slot_end && pos_ok;
-            if (head[u] == 0)
+        *s_abort = 0;
+        fence_barrier_init();
+        griddep_launch_dependents();
+    }
+    __syncthreads();
+    griddep_wait();   // qkv, indices and table are written by the kernels before this one
+
+    if (warp == 0) {
+        // ---- produce: 32 tokens' indices per warp load, one bulk copy per row ----
+        unsigned bad = 0u;
+        int i = 0, issued = 0;
+        bool stop = false;
+        for (int64_t tb = blockIdx.x; tb < p.T && !stop; tb += 32 * G) {
+            const int64_t tl = tb + lane * G;
+            int64_t pos_l = -1, slot_l = -1;
+            if (tl < p.T) {
+                pos_l = p.positions[tl];
+                slot_l = p.slots[tl];
+                const bool pos_ok = pos_l >= 0 && pos_l < p.cos_rows;
                 bad |= (pos_ok ? 0u : QKVF_STATUS_BAD_POSITION) |
-                       (slot[u] >= slot_end ? QKVF_STATUS_BAD_SLOT : 0u);
-            const int h = head[u];
-            uint4 word = val[u];
-            // q / k heads of the group: the whole warp runs the shuffles (lanes of
-            // v heads or of heads past the last one compute values they drop)
-            const bool qk_group = (h - sub) < qk_heads;   // the group's first head
-            if (qk_group && pos_ok) {
-                const uint32_t w4[4] = {val[u].x, val[u].y, val[u].z, val[u].w};
-                float f[8];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const __nv_bfloat162 pr = *reinterpret_cast<const __nv_bfloat162 *>(&w4[j]);
-                    f[2 * j] = __low2float(pr);
-                    f[2 * j + 1] = __high2float(pr);
+                       (slot_l >= slot_end ? QKVF_STATUS_BAD_SLOT : 0u);
+            }
+            for (int j = 0; j < 32; ++j, ++i) {
+                const int64_t t = tb + j * G;
+                if (t >= p.T) break;   // the same for every lane
+                const int64_t pos = __shfl_sync(0xffffffffu, pos_l, j);
+                const int64_t sl = __shfl_sync(0xffffffffu, slot_l, j);
+                if (lane == 0) {
+                    const int s = i % nslots, use = i / nslots;
+                    if (use > 0 && !bounded_wait(empty0 + 8 * s, (uint32_t)((use - 1) & 1), s_abort,
+                                                 p.wait_limit_ns, true)) {
+                        stop = true;
+                    } else {
+                        uint8_t *base = smem + (size_t)s * slot_bytes;
+                        const bool pos_ok = pos >= 0 && pos < p.cos_rows;
+                        const bool ins = sl >= 0 && sl < slot_end && pos_ok;
+                        int64_t *hdr = reinterpret_cast<int64_t *>(base + region + kHeadDim * 4);
+                        hdr[0] = pos;
+                        hdr[1] = sl;
+                        hdr[2] = (pos_ok ? 1 : 0) | (ins ? 2 : 0);
+                        const uint32_t bar = full0 + 8 * s;
+                        mbar_expect_tx(bar, region + (pos_ok ? kHeadDim * 4 : 0));
+                        bulk_load(smem_u32(base), p.qkv + (size_t)t * p.N, region, bar);
+                        if (pos_ok)
+                            bulk_load(smem_u32(base + region), p.cos_sin + pos * kHeadDim, kHeadDim * 4,
+                                      bar);
+                        ++issued;
+                    }
                 }
-                const float ss = head_sum_sq_front_order(f);
-                const float ms = __fdiv_rn(ss, (float)kHeadDim);
-                const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, kEps)));
-                const float cc[4] = {cv[u].x, cv[u].y, cv[u].z, cv[u].w};
-                const float ss4[4] = {sv[u].x, sv[u].y, sv[u].z, sv[u].w};
-                uint32_t o[4];
+                stop = __shfl_sync(0xffffffffu, stop ? 1 : 0, 0) != 0;
+                if (stop) break;
+            }
+        }
+        if (lane == 0 && *s_abort) {   // drain our copies before leaving
+            const int first = issued > nslots ? issued - nslots : 0;
+            for (int k = first; k < issued; ++k)
+                bounded_wait(full0 + 8 * (k % nslots), (uint32_t)((k / nslots) & 1), s_abort,
+                             p.wait_limit_ns, false);
+        }
+        bad = __reduce_or_sync(0xffffffffu, bad);
+        if (lane == 0 && bad != 0u) atomicOr(&g_status, bad);
+    } else {
+        // ---- consume ----------------------------------------------------
+        const int cw = warp - 1, sub = lane >> 3, chunk = lane & 7;
+        int i = 0;
+        for (int64_t t = blockIdx.x; t < p.T; t += G, ++i) {
+            const int s = i % nslots;
+            const bool landed = mbar_try_wait(full0 + 8 * s, (uint32_t)((i / nslots) & 1)) ||
+                                bounded_wait(full0 + 8 * s, (uint32_t)((i / nslots) & 1), s_abort,
+                                             p.wait_limit_ns, true);
+            if (__all_sync(0xffffffffu, landed)) {
+                const uint8_t *base = smem + (size_t)s * slot_bytes;
+                const int64_t *hdr = reinterpret_cast<const int64_t *>(base + region + kHeadDim * 4);
+                const int64_t sl = hdr[1];
+                const int flags = (int)hdr[2];
+                const bool pos_ok = flags & 1, ins = flags & 2;
+                const float *row = reinterpret_cast<const float *>(base + region);
+                for (int grp = cw; grp < groups; grp += kEpiConsumerWarps) {
+                    const int h = grp * 4 + sub;
+                    uint4 val = make_uint4(0u, 0u, 0u, 0u);
+                    if (h < heads)
+                        val = *reinterpret_cast<const uint4 *>(base + h * (kHeadDim * 2) + 16 * chunk);
+                    uint4 word = val;
+                    if (grp * 4 < qk_heads && pos_ok) {   // the whole warp: shuffles inside
+                        const uint32_t w4[4] = {val.x, val.y, val.z, val.w};
+                        float f[8];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float a = __fmul_rn(f[2 * j], r), b = __fmul_rn(f[2 * j + 1], r);
-                    const float y0 = __fsub_rn(__fmul_rn(a, cc[j]), __fmul_rn(b, ss4[j]));
-                    const float y1 = __fadd_rn(__fmul_rn(b, cc[j]), __fmul_rn(a, ss4[j]));
-                    o[j] = pack_bf16x2(__float2bfloat16_rn(y0), __float2bfloat16_rn(y1));
-                }
-                if (h < qk_heads) {
-                    word = make_uint4(o[0], o[1], o[2], o[3]);
-                    *reinterpret_cast<uint4 *>(p.qkv + (size_t)tok[u] * p.N + (size_t)h * kHeadDim +
-                                               8 * chunk) = word;
+                        for (int j = 0; j < 4; ++j) {
+                            const __nv_bfloat162 pr = *reinterpret_cast<const __nv_bfloat162 *>(&w4[j]);
+                            f[2 * j] = __low2float(pr);
+                            f[2 * j + 1] = __high2float(pr);
+                        }
+                        const float ss = head_sum_sq_front_order(f);
+                        const float ms = __fdiv_rn(ss, (float)kHeadDim);
+                        const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, kEps)));
+                        const float4 cv = *reinterpret_cast<const float4 *>(row + 4 * chunk);
+                        const float4 sv = *reinterpret_cast<const float4 *>(row + 32 + 4 * chunk);
+                        const float cc[4] = {cv.x, cv.y, cv.z, cv.w};
+                        const float sn[4] = {sv.x, sv.y, sv.z, sv.w};
+                        uint32_t o[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const float a = __fmul_rn(f[2 * j], r), b = __fmul_rn(f[2 * j + 1], r);
+                            const float y0 = __fsub_rn(__fmul_rn(a, cc[j]), __fmul_rn(b, sn[j]));
+                            const float y1 = __fadd_rn(__fmul_rn(b, cc[j]), __fmul_rn(a, sn[j]));
+                            o[j] = pack_bf16x2(__float2bfloat16_rn(y0), __float2bfloat16_rn(y1));
+                        }
+                        if (h < qk_heads) {
+                            word = make_uint4(o[0], o[1], o[2], o[3]);
+                            *reinterpret_cast<uint4 *>(p.qkv + (size_t)t * p.N + (size_t)h * kHeadDim +
+                                                       8 * chunk) = word;
+                        }
+                    }
+                    if (h >= q_heads && h < heads && ins) {   // k or v head of an inserting token
+                        const bool is_v = h >= qk_heads;
+                        const int gkv = h - q_heads - (is_v ? nkv : 0);
+                        const int64_t page = sl / kPageSlots, offs = sl % kPageSlots;
+                        uint16_t *dst = p.kv_cache + ((page * nkv + gkv) * kPageSlots + offs) * kSlotWidth +
+                                        (is_v ? kHeadDim : 0) + 8 * chunk;
+                        *reinterpret_cast<uint4 *>(dst) = word;
+                    }
                 }
             }
-            if (h >= q_heads && h < heads && ins && (h >= qk_heads || pos_ok)) {
-                const bool is_v = h >= qk_heads;
-                const int gkv = h - q_heads - (is_v ? p.nkv : 0);
-                const int64_t page = slot[u] / kPageSlots, offs = slot[u] % kPageSlots;
-                uint16_t *dst = p.kv_cache + ((page * p.nkv + gkv) * kPageSlots + offs) * kSlotWidth +
-                                (is_v ? kHeadDim : 0) + 8 * chunk;
-                *reinterpret_cast<uint4 *>(dst) = word;
-            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8 * s);
         }
     }
-    bad = __reduce_or_sync(0xffffffffu, bad);
-    if (lane == 0 && bad != 0u) atomicOr(&g_status, bad);
 }
 
 const char *check_epi_args(uint16_t *qkv, const int64_t *positions, const int64_t *slots,
@@ -206,6 +284,13 @@ const char *check_epi_args(uint16_t *qkv, const int64_t *positions, const int64_
     return nullptr;
 }
 
+bool prepare_epi_kernel()
+{
+    return cudaFuncSetAttribute((const void *)qknorm_rope_kv_insert_kernel,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)epi_smem_bytes(64)) == cudaSuccess;   // the largest ring (64 KV heads)
+}
+
 int launch_epi(uint16_t *qkv, const int64_t *positions, const int64_t *slots, const float *cos_sin,
                int64_t cos_sin_rows, uint16_t *kv_cache, int64_t num_pages, int T, int N,
                int num_kv_heads, int sms, void *stream)
@@ -221,16 +306,14 @@ int launch_epi(uint16_t *qkv, const int64_t *positions, const int64_t *slots, co
     prm.T = T;
     prm.N = N;
     prm.nkv = num_kv_heads;
-    const int64_t tasks = (int64_t)T * (((kQPerKv + 2) * num_kv_heads + 3) / 4);
-    const int64_t warps_needed = (tasks + kEpiUnroll - 1) / kEpiUnroll;
-    int64_t blocks = (warps_needed + (kEpiThreads / 32) - 1) / (kEpiThreads / 32);
-    const int64_t resident = (int64_t)sms * 3;   // one full wave at 3 blocks per SM
-    if (blocks > resident) blocks = resident;
+    prm.wait_limit_ns = g_wait_limit_ns;
+    int64_t blocks = (int64_t)sms * 2;   // two CTAs per SM, each walking its tokens
+    if (blocks > T) blocks = T;
     if (blocks < 1) blocks = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)blocks, 1, 1);
     cfg.blockDim = dim3(kEpiThreads, 1, 1);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = epi_smem_bytes(num_kv_heads);
     cfg.stream = (cudaStream_t)stream;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -816,6 +816,8 @@ constexpr int kDefaultKB = 4;          // 64-k boxes per ring stage: 256 k, 32 K
 constexpr int kDefaultL2Prefetch = 8;  // W stages prefetched into L2 before the PDL wait
 constexpr bool kDefaultTC = false;     // consumer: tcgen05 (true) or mma.sync
 
+bool prepare_epi_kernel();
+
 int probe_device(DeviceState **out)
 {
     int dev = 0;
@@ -852,6 +854,7 @@ int probe_device(DeviceState **out)
                                      cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
                 return QKVF_ERR_CUDA;
         }
+        if (!prepare_epi_kernel()) return QKVF_ERR_CUDA;
         d.prepared = true;
     }
     *out = &d;
