@@ -62,24 +62,53 @@ __host__ __device__ inline uint32_t epi_smem_bytes(int nkv)
     return (uint32_t)epi_slots(nkv) * epi_slot_bytes(nkv) + 2 * kEpiMaxSlots * 8 + 16 + 128;
 }
 
-// Sum of squares of one head held as 8 lanes x 8 values, in exactly the
-// association of the fused front's warp butterfly (qk_norm_rope_pair), so
-// both kernels give the same bits.  In the front, lane l holds columns
-// (2l, 2l+1) and the butterfly adds across lane bits 4, 3, 2, then 1, 0.  Here
-// lane c of the group holds columns 8c..8c+7, i.e. the front's lanes 4c..4c+3:
-// the front's lane bits 4, 3, 2 are this group's lane bits 2, 1, 0, and its
-// bits 1, 0 are the four pairs inside this lane.
-__device__ __forceinline__ float head_sum_sq_front_order(const float (&f)[8])
+// Sum of squares of one head held by 4 lanes, in exactly the association of
+// the fused front's warp butterfly (qk_norm_rope_pair), so both kernels give
+// the same bits.  In the front, lane l holds pair l (columns 2l, 2l+1) and the
+// butterfly adds across lane bits 4, 3, 2, 1, 0 in that order.  Here lane c of
+// the 4-lane group holds pairs 4c..4c+3 (lo[]) and 16+4c..16+4c+3 (hi[]): the
+// front's lane bit 4 is lo/hi (added in registers), bits 3, 2 are this group's
+// lane bits 1, 0 (two shuffle levels), and bits 1, 0 index the four pairs.
+__device__ __forceinline__ float head_sum_sq_front_order(const float (&lo)[8], const float (&hi)[8])
 {
-    float s[4];
+    float a[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-        s[j] = __fadd_rn(__fmul_rn(f[2 * j], f[2 * j]), __fmul_rn(f[2 * j + 1], f[2 * j + 1]));
+    for (int j = 0; j < 4; ++j) {
+        const float sl = __fadd_rn(__fmul_rn(lo[2 * j], lo[2 * j]), __fmul_rn(lo[2 * j + 1], lo[2 * j + 1]));
+        const float sh = __fadd_rn(__fmul_rn(hi[2 * j], hi[2 * j]), __fmul_rn(hi[2 * j + 1], hi[2 * j + 1]));
+        a[j] = __fadd_rn(sl, sh);
+    }
 #pragma unroll
-    for (int off = 4; off >= 1; off >>= 1)
+    for (int off = 2; off >= 1; off >>= 1)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) s[j] = __fadd_rn(s[j], __shfl_xor_sync(0xffffffffu, s[j], off));
-    return __fadd_rn(__fadd_rn(s[0], s[2]), __fadd_rn(s[1], s[3]));
+        for (int j = 0; j < 4; ++j) a[j] = __fadd_rn(a[j], __shfl_xor_sync(0xffffffffu, a[j], off));
+    return __fadd_rn(__fadd_rn(a[0], a[2]), __fadd_rn(a[1], a[3]));
+}
+
+__device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8])
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const __nv_bfloat162 pr = *reinterpret_cast<const __nv_bfloat162 *>(&w[j]);
+        f[2 * j] = __low2float(pr);
+        f[2 * j + 1] = __high2float(pr);
+    }
+}
+
+// rotate four pairs by (c, s) after scaling by r; pack to BF16
+__device__ __forceinline__ uint4 rope4(const float (&f)[8], float r, const float4 c, const float4 s)
+{
+    const float cc[4] = {c.x, c.y, c.z, c.w}, sn[4] = {s.x, s.y, s.z, s.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float a = __fmul_rn(f[2 * j], r), b = __fmul_rn(f[2 * j + 1], r);
+        const float y0 = __fsub_rn(__fmul_rn(a, cc[j]), __fmul_rn(b, sn[j]));
+        const float y1 = __fadd_rn(__fmul_rn(b, cc[j]), __fmul_rn(a, sn[j]));
+        o[j] = pack_bf16x2(__float2bfloat16_rn(y0), __float2bfloat16_rn(y1));
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
@@ -94,7 +123,8 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
 // CTA b takes tokens b, b + G, b + 2G, ... (G = gridDim.x).  Warp 0 copies
 // each token's q | k | v region (contiguous in its row) and its cos|sin row
 // into a ring slot with bulk copies; warps 1..8 take the token's heads in
-// groups of 4 (lane l: head 4 g + l / 8, columns 8 (l % 8) .. + 7), norm and
+// groups of 8 (lane l: head 8 g + l / 4, columns 8c..8c+7 and 32+8c..32+8c+7
+// with c = l % 4), norm and
 // rotate q / k heads in place in global memory and write k / v heads into the
 // cache slot.
 __global__ void __launch_bounds__(kEpiThreads, 2) qknorm_rope_kv_insert_kernel(const EpiParams p)
@@ -181,8 +211,9 @@ __global__ void __launch_bounds__(kEpiThreads, 2) qknorm_rope_kv_insert_kernel(c
         bad = __reduce_or_sync(0xffffffffu, bad);
         if (lane == 0 && bad != 0u) atomicOr(&g_status, bad);
     } else {
-        // ---- consume ----------------------------------------------------
-        const int cw = warp - 1, sub = lane >> 3, chunk = lane & 7;
+        // ---- consume: groups of 8 heads, 4 lanes x 32 bytes per head ------
+        const int cw = warp - 1, sub = lane >> 2, part = lane & 3;
+        const int groups8 = (heads + 7) >> 3;
         int i = 0;
         for (int64_t t = blockIdx.x; t < p.T; t += G, ++i) {
             const int s = i % nslots;
@@ -196,49 +227,46 @@ __global__ void __launch_bounds__(kEpiThreads, 2) qknorm_rope_kv_insert_kernel(c
                 const int flags = (int)hdr[2];
                 const bool pos_ok = flags & 1, ins = flags & 2;
                 const float *row = reinterpret_cast<const float *>(base + region);
-                for (int grp = cw; grp < groups; grp += kEpiConsumerWarps) {
-                    const int h = grp * 4 + sub;
-                    uint4 val = make_uint4(0u, 0u, 0u, 0u);
-                    if (h < heads)
-                        val = *reinterpret_cast<const uint4 *>(base + h * (kHeadDim * 2) + 16 * chunk);
-                    uint4 word = val;
-                    if (grp * 4 < qk_heads && pos_ok) {   // the whole warp: shuffles inside
-                        const uint32_t w4[4] = {val.x, val.y, val.z, val.w};
-                        float f[8];
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const __nv_bfloat162 pr = *reinterpret_cast<const __nv_bfloat162 *>(&w4[j]);
-                            f[2 * j] = __low2float(pr);
-                            f[2 * j + 1] = __high2float(pr);
-                        }
-                        const float ss = head_sum_sq_front_order(f);
-                        const float ms = __fdiv_rn(ss, (float)kHeadDim);
+                uint16_t *qrow = p.qkv + (size_t)t * p.N + 8 * part;
+                uint16_t *crow = nullptr;
+                if (ins) {
+                    const int64_t page = sl / kPageSlots, offs = sl % kPageSlots;
+                    crow = p.kv_cache + ((page * nkv) * kPageSlots + offs) * kSlotWidth + 8 * part;
+                }
+                for (int grp = cw; grp < groups8; grp += kEpiConsumerWarps) {
+                    // lane: head 8 grp + l / 4; bytes 16 c and 64 + 16 c of the head (c = l % 4)
+                    const int h = grp * 8 + sub;
+                    uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
+                    if (h < heads) {
+                        const uint8_t *src = base + h * (kHeadDim * 2) + 16 * part;
+                        v0 = *reinterpret_cast<const uint4 *>(src);
+                        v1 = *reinterpret_cast<const uint4 *>(src + 64);
+                    }
+                    if (grp * 8 < qk_heads && pos_ok) {   // the whole warp: shuffles inside
+                        float lo[8], hi[8];
+                        unpack8(v0, lo);
+                        unpack8(v1, hi);
+                        const float ss = head_sum_sq_front_order(lo, hi);
+                        const float ms = __fmul_rn(ss, 1.0f / (float)kHeadDim);   // exact: a power of two
                         const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, kEps)));
-                        const float4 cv = *reinterpret_cast<const float4 *>(row + 4 * chunk);
-                        const float4 sv = *reinterpret_cast<const float4 *>(row + 32 + 4 * chunk);
-                        const float cc[4] = {cv.x, cv.y, cv.z, cv.w};
-                        const float sn[4] = {sv.x, sv.y, sv.z, sv.w};
-                        uint32_t o[4];
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const float a = __fmul_rn(f[2 * j], r), b = __fmul_rn(f[2 * j + 1], r);
-                            const float y0 = __fsub_rn(__fmul_rn(a, cc[j]), __fmul_rn(b, sn[j]));
-                            const float y1 = __fadd_rn(__fmul_rn(b, cc[j]), __fmul_rn(a, sn[j]));
-                            o[j] = pack_bf16x2(__float2bfloat16_rn(y0), __float2bfloat16_rn(y1));
-                        }
+                        const uint4 o0 = rope4(lo, r, *reinterpret_cast<const float4 *>(row + 4 * part),
+                                               *reinterpret_cast<const float4 *>(row + 32 + 4 * part));
+                        const uint4 o1 = rope4(hi, r, *reinterpret_cast<const float4 *>(row + 16 + 4 * part),
+                                               *reinterpret_cast<const float4 *>(row + 48 + 4 * part));
                         if (h < qk_heads) {
-                            word = make_uint4(o[0], o[1], o[2], o[3]);
-                            *reinterpret_cast<uint4 *>(p.qkv + (size_t)t * p.N + (size_t)h * kHeadDim +
-                                                       8 * chunk) = word;
+                            v0 = o0;
+                            v1 = o1;
+                            uint16_t *dst = qrow + (size_t)h * kHeadDim;
+                            *reinterpret_cast<uint4 *>(dst) = v0;
+                            *reinterpret_cast<uint4 *>(dst + 32) = v1;
                         }
                     }
                     if (h >= q_heads && h < heads && ins) {   // k or v head of an inserting token
                         const bool is_v = h >= qk_heads;
                         const int gkv = h - q_heads - (is_v ? nkv : 0);
-                        const int64_t page = sl / kPageSlots, offs = sl % kPageSlots;
-                        uint16_t *dst = p.kv_cache + ((page * nkv + gkv) * kPageSlots + offs) * kSlotWidth +
-                                        (is_v ? kHeadDim : 0) + 8 * chunk;
-                        *reinterpret_cast<uint4 *>(dst) = word;
+                        uint16_t *dst = crow + (size_t)gkv * kPageSlots * kSlotWidth + (is_v ? kHeadDim : 0);
+                        *reinterpret_cast<uint4 *>(dst) = v0;
+                        *reinterpret_cast<uint4 *>(dst + 32) = v1;
                     }
                 }
             }
