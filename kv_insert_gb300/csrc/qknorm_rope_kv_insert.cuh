@@ -141,13 +141,12 @@ __global__ void __launch_bounds__(kEpiThreads, 2) qknorm_rope_kv_insert_kernel(c
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t G = gridDim.x;
     const int q_heads = kQPerKv * nkv, qk_heads = q_heads + nkv, heads = qk_heads + nkv;
-    const int groups = (heads + 3) >> 2;
     const int64_t slot_end = p.num_pages * (int64_t)kPageSlots;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < nslots; ++s) {
             mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, kEpiConsumerWarps);
+            mbar_init(empty0 + 8 * s, (heads + 7) >> 3);   // one arrival per 8-head group
         }
         *s_abort = 0;
         fence_barrier_init();
@@ -212,11 +211,19 @@ __global__ void __launch_bounds__(kEpiThreads, 2) qknorm_rope_kv_insert_kernel(c
         if (lane == 0 && bad != 0u) atomicOr(&g_status, bad);
     } else {
         // ---- consume: groups of 8 heads, 4 lanes x 32 bytes per head ------
+        // The CTA's (token, group) items are dealt round robin over the consumer
+        // warps across token boundaries, so a token with fewer groups than warps
+        // does not leave warps idle.  Every warp still waits on every token in
+        // order (the barrier parity never runs more than one phase ahead) and
+        // arrives on the token's empty barrier once per group it processed.
         const int cw = warp - 1, sub = lane >> 2, part = lane & 3;
         const int groups8 = (heads + 7) >> 3;
         int i = 0;
-        for (int64_t t = blockIdx.x; t < p.T; t += G, ++i) {
+        int64_t first = 0;   // item index of this token's first group
+        for (int64_t t = blockIdx.x; t < p.T; t += G, ++i, first += groups8) {
             const int s = i % nslots;
+            const int g0 = (int)(((int64_t)cw - first % kEpiConsumerWarps + kEpiConsumerWarps) %
+                                 kEpiConsumerWarps);
             const bool landed = mbar_try_wait(full0 + 8 * s, (uint32_t)((i / nslots) & 1)) ||
                                 bounded_wait(full0 + 8 * s, (uint32_t)((i / nslots) & 1), s_abort,
                                              p.wait_limit_ns, true);
@@ -233,7 +240,7 @@ __global__ void __launch_bounds__(kEpiThreads, 2) qknorm_rope_kv_insert_kernel(c
                     const int64_t page = sl / kPageSlots, offs = sl % kPageSlots;
                     crow = p.kv_cache + ((page * nkv) * kPageSlots + offs) * kSlotWidth + 8 * part;
                 }
-                for (int grp = cw; grp < groups8; grp += kEpiConsumerWarps) {
+                for (int grp = g0; grp < groups8; grp += kEpiConsumerWarps) {
                     // lane: head 8 grp + l / 4; bytes 16 c and 64 + 16 c of the head (c = l % 4)
                     const int h = grp * 8 + sub;
                     uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
@@ -268,10 +275,13 @@ __global__ void __launch_bounds__(kEpiThreads, 2) qknorm_rope_kv_insert_kernel(c
                         *reinterpret_cast<uint4 *>(dst) = v0;
                         *reinterpret_cast<uint4 *>(dst + 32) = v1;
                     }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(empty0 + 8 * s);
                 }
+            } else {
+                for (int grp = g0; grp < groups8; grp += kEpiConsumerWarps)
+                    if (lane == 0) mbar_arrive(empty0 + 8 * s);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(empty0 + 8 * s);
         }
     }
 }
