@@ -42,8 +42,9 @@ METRIC = "µs/call and achieved HBM GB/s (fraction of GB300 peak) at M=1..16, 1 
 UNIT = "GB/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCE = os.path.join(ROOT, "kv_insert_gb300", "csrc", "qkv_front.cu")
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "qkv_front_traffic.json")
+KERNEL_SOURCES = [os.path.join(ROOT, "kv_insert_gb300", "csrc", f)
+                  for f in ("qkv_front.cu", "qknorm_rope_kv_insert.cuh")]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 
 
 def parse_args(argv=None):
@@ -130,15 +131,15 @@ def hbm_peak():
 
 def source_digest() -> str:
     h = hashlib.sha256()
-    for f in (KERNEL_SOURCE, os.path.join(ROOT, "include", "qkvfront.h")):
+    for f in KERNEL_SOURCES + [os.path.join(ROOT, "include", "qkvfront.h")]:
         with open(f, "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
 
 
-def recorded_traffic(workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    this exact kernel source and workload; else None."""
+def recorded_traffic(op: str, workload: str):
+    """DRAM bytes per launch from the committed ncu record, if it was taken on
+    this exact kernel source, op and workload; else None."""
     try:
         with open(TRAFFIC_FILE) as fh:
             rec = json.load(fh)
@@ -146,7 +147,7 @@ def recorded_traffic(workload: str):
         return None
     if rec.get("source_sha256") != source_digest():
         return None
-    per = rec.get("per_workload", {}).get(workload)
+    per = rec.get("records", {}).get(f"{op}/{workload}")
     return None if per is None else float(per["dram_bytes_per_launch"])
 
 
@@ -405,7 +406,7 @@ def run_ours(args, w: wl.Workload):
     peak, peak_kind = hbm_peak()
     bytes_call = w.roofline_bytes()
     achieved = bytes_call / (el_max / args.steps) / 1e9
-    traffic = recorded_traffic(w.name)
+    traffic = recorded_traffic("qkv_front", w.name)
     line = {
         "metric": METRIC, "value": res["value"], "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
@@ -510,7 +511,8 @@ def run_epilogue(args, w):
                       f"{q_bytes / 1e6:.1f} MB (L2 {l2 / 1e6:.1f} MB)",
                 "graph_calls": per_graph, "parallelism": f"replicas x{world}"}),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "peak_kind": peak_kind, "traffic": None,
+                         "frac": achieved / peak, "peak_kind": peak_kind,
+                         "traffic": recorded_traffic("qknorm_rope_kv_insert", w.name),
                          "bytes_per_launch": w.roofline_bytes()},
             "gpu_launches": args.steps, "clocks": clocks, "e2e": None}
 
