@@ -43,7 +43,7 @@ UNIT = "GB/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = [os.path.join(ROOT, "kv_insert_gb300", "csrc", f)
-                  for f in ("qkv_front.cu", "qknorm_rope_kv_insert.cuh")]
+                  for f in ("qkv_front.cu", "qknorm_rope_kv_insert.cuh", "layer_front.cuh")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 
 
@@ -53,9 +53,11 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--op", choices=("qkv_front", "qknorm_rope_kv_insert"), default="qkv_front",
+    ap.add_argument("--op", choices=("qkv_front", "qknorm_rope_kv_insert", "chain"),
+                    default="qkv_front",
                     help="qkv_front: the fused decode front (the headline); qknorm_rope_kv_insert: "
-                         "the standalone epilogue on a prefill chunk")
+                         "the standalone epilogue on a prefill chunk; chain: layer_front then "
+                         "qkv_front, PDL-linked, against each alone")
     ap.add_argument("--workload", default=None,
                     choices=sorted(wl.WORKLOADS) + sorted(wl.EPI_WORKLOADS))
     ap.add_argument("--graph-calls", type=int, default=96,
@@ -67,8 +69,8 @@ def parse_args(argv=None):
                     help="target duration of the whole --impl reference run")
     a = ap.parse_args(argv)
     if a.workload is None:
-        a.workload = wl.BENCH_WORKLOAD if a.op == "qkv_front" else wl.EPI_BENCH_WORKLOAD
-    table = wl.WORKLOADS if a.op == "qkv_front" else wl.EPI_WORKLOADS
+        a.workload = wl.EPI_BENCH_WORKLOAD if a.op == "qknorm_rope_kv_insert" else wl.BENCH_WORKLOAD
+    table = wl.EPI_WORKLOADS if a.op == "qknorm_rope_kv_insert" else wl.WORKLOADS
     if a.workload not in table:
         ap.error(f"workload {a.workload} is not a {a.op} workload")
     if a.op != "qkv_front" and a.impl == "reference":
@@ -517,9 +519,103 @@ def run_epilogue(args, w):
             "gpu_launches": args.steps, "clocks": clocks, "e2e": None}
 
 
+CHAIN_METRIC = "µs per first-layer front step: layer_front then qkv_front, PDL-linked, 1 GPU"
+
+
+def run_chain(args, w: wl.Workload):
+    """layer_front (embedded tokens -> residual stream + normed x) followed by
+    qkv_front on its output, PDL-linked on one stream: µs per step, against
+    the two kernels timed alone in the same way; the difference is the time
+    the front's weight prefetch hides under its predecessor."""
+    from kv_insert_gb300 import qkv_front as qf
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU (the product path has no CPU fallback)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_init("nccl")
+    qf.load()
+    inp = wl.make_inputs(w)
+    lf = wl.make_layer_front_inputs(w)
+    g = {k: v.to(dev) for k, v in inp.items()}
+    g.update({k: v.to(dev) for k, v in lf.items()})
+    stream_buf = torch.empty(w.M, wl.HIDDEN, device=dev)
+    x_attn = torch.empty(w.M, wl.HIDDEN, dtype=torch.bfloat16, device=dev)
+    out = torch.empty(w.M, w.N, dtype=torch.bfloat16, device=dev)
+    qf.prepare(w.N, w.num_kv_heads)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    w_bytes = w.N * wl.HIDDEN * 2
+    copies = max(2, math.ceil(3 * l2 / w_bytes))
+    Ws = [g["W"]] + [g["W"].clone() for _ in range(copies - 1)]
+    torch.cuda.synchronize(dev)
+    s = torch.cuda.Stream(device=dev)
+    per_graph = max(copies, (args.graph_calls // copies) * copies)
+
+    def lf_call():
+        qf.layer_front(g["x_embed"], stream_buf, x_attn, weight=g["norm_weight"])
+
+    def front_call(i):
+        qf.launch(x_attn, Ws[i % copies], g["positions"], g["slots"], g["cos_sin"], g["kv_cache"],
+                  out)
+
+    legs = {"chain": lambda i: (lf_call(), front_call(i)),
+            "layer_front": lambda i: lf_call(),
+            "qkv_front": front_call}
+    timings = {}
+    for name, fn in legs.items():
+        with torch.cuda.stream(s):
+            for i in range(args.warmup):
+                fn(i)
+        s.synchronize()
+        full, rem = divmod(args.steps, per_graph)
+        graphs = []
+        for n in ([per_graph] if full else []) + ([rem] if rem else []):
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=s):
+                for i in range(n):
+                    fn(i)
+            graphs.append(graph)
+        with torch.cuda.stream(s):
+            for gr in graphs:
+                gr.replay()
+        s.synchronize()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize(dev)
+        with torch.cuda.stream(s):
+            start.record(s)
+            for _ in range(full):
+                graphs[0].replay()
+            if rem:
+                graphs[-1].replay()
+            end.record(s)
+        torch.cuda.synchronize(dev)
+        barrier()
+        timings[name] = max_over_ranks(start.elapsed_time(end) / 1e3, dev) / args.steps * 1e6
+    if qf.status():
+        raise RuntimeError("device status raised in the timed region")
+    if rank != 0:
+        return None
+    return {"metric": CHAIN_METRIC, "value": timings["chain"], "unit": "µs/step", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": timings["chain"] / 1e3,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": dict(w.describe(), **{
+                "l2": f"inputs larger than L2: W rotated over {copies} copies",
+                "graph_calls": per_graph, "parallelism": f"replicas x{world}"}),
+            "layer_front_alone_us": timings["layer_front"],
+            "qkv_front_alone_us": timings["qkv_front"],
+            "sum_alone_us": timings["layer_front"] + timings["qkv_front"],
+            "hidden_by_overlap_us": timings["layer_front"] + timings["qkv_front"] - timings["chain"],
+            "gpu_launches": 2 * args.steps, "e2e": None}
+
+
 def main(argv=None):
     args = parse_args(argv)
-    if args.op == "qknorm_rope_kv_insert":
+    if args.op == "chain":
+        line = run_chain(args, wl.WORKLOADS[args.workload])
+    elif args.op == "qknorm_rope_kv_insert":
         line = run_epilogue(args, wl.EPI_WORKLOADS[args.workload])
     else:
         w = wl.WORKLOADS[args.workload]

@@ -201,6 +201,26 @@ const char *qknorm_rope_kv_insert_unsupported(uint16_t *qkv, const int64_t *posi
                                               int64_t cos_sin_rows, uint16_t *kv_cache,
                                               int64_t num_pages, int T, int N, int num_kv_heads);
 
+/*
+ * layer_front: the kernel before the QKV front in the first decoder layer
+ * (page layer_front, class LayerFront, run): for each of `rows` rows of
+ * 8192 values,
+ *   stream = x as FP32 (the residual stream), aux = stream (if aux is not
+ *   NULL), out = bf16((stream * r) * w), r = 1 / sqrt(mean(stream^2) + eps),
+ *   w the BF16 weight widened to FP32 (out = bf16(stream * r) when weight is
+ *   NULL) — the attention input the QKV front reads as x.
+ *   x          [rows, 8192], bf16 bits (x_is_f32 = 0) or fp32 (x_is_f32 = 1).
+ *   weight     [8192] bf16 bits, or NULL.
+ *   stream, aux [rows, 8192] fp32 (aux may be NULL); out [rows, 8192] bf16 bits.
+ *   rows       0 .. 2^20 (0: no launch); eps in (0, 1].
+ * All arrays are device pointers, 16-byte aligned; outputs must not overlap
+ * each other or the inputs.  Launched with PDL: it waits for the previous
+ * kernel, then at once lets the next kernel on the stream start, so a
+ * qkv_front call issued after it streams its weights while this runs.
+ */
+int layer_front(const void *x, int x_is_f32, const uint16_t *weight, float *stream, float *aux,
+                uint16_t *out, int rows, float eps, void *cuda_stream);
+
 /* Static text of a QKVF_* return code. */
 const char *qkv_front_strerror(int code);
 

@@ -9,7 +9,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 SOURCES = [os.path.join(PKG, "csrc", "qkv_front.cu")]
 HEADERS = [os.path.join(ROOT, "include", "qkvfront.h"),
-           os.path.join(PKG, "csrc", "qknorm_rope_kv_insert.cuh")]
+           os.path.join(PKG, "csrc", "qknorm_rope_kv_insert.cuh"),
+           os.path.join(PKG, "csrc", "layer_front.cuh")]
 LIB_PATH = os.path.join(PKG, "libqkvfront.so")
 
 NVCC_FLAGS = [

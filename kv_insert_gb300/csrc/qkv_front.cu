@@ -1038,6 +1038,7 @@ int launch_front(const uint16_t *x, const uint16_t *W, const int64_t *positions,
 }  // namespace qkvf
 
 #include "qknorm_rope_kv_insert.cuh"
+#include "layer_front.cuh"
 
 using namespace qkvf;
 

@@ -95,6 +95,8 @@ def load() -> ctypes.CDLL:
         lib.qknorm_rope_kv_insert.restype = i32
         lib.qknorm_rope_kv_insert_unsupported.argtypes = epi_args
         lib.qknorm_rope_kv_insert_unsupported.restype = ctypes.c_char_p
+        lib.layer_front.argtypes = [vp, i32, vp, vp, vp, vp, i32, ctypes.c_float, vp]
+        lib.layer_front.restype = i32
         _lib = lib
         return lib
 
@@ -103,7 +105,8 @@ def header_functions() -> list[str]:
     """Names of the functions include/qkvfront.h declares."""
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b((?:qkv_front|qknorm_rope_kv_insert)\w*)\s*\(", text)))
+    return sorted(set(re.findall(r"\b((?:qkv_front|qknorm_rope_kv_insert|layer_front)\w*)\s*\(",
+                                 text)))
 
 
 def strerror(code: int) -> str:
@@ -355,6 +358,30 @@ def qknorm_rope_kv_insert(qkv, positions, slots, cos_sin, kv_cache, stream=None)
         _check(load().qknorm_rope_kv_insert(*_epi_args(qkv, positions, slots, cos_sin, kv_cache),
                                             _stream(stream)))
     return qkv
+
+
+def layer_front(x, stream_out, out, aux=None, weight=None, eps: float = 1e-6, stream=None):
+    """The first layer's front (page layer_front, LayerFront.run): stream_out =
+    x as fp32, aux = stream_out (if given), out = bf16 RMS norm of the row
+    (times weight, if given).  x: bf16 or fp32 [rows, 8192].  Returns out."""
+    if x.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("x must be bf16 or fp32")
+    rows = x.shape[0]
+    checks = [(x, x.dtype, "x"), (stream_out, torch.float32, "stream"),
+              (out, torch.bfloat16, "out")] + ([(aux, torch.float32, "aux")] if aux is not None else [])
+    for t, dt, name in checks:
+        if (not t.is_cuda or t.dtype != dt or tuple(t.shape) != (rows, HIDDEN)
+                or not t.is_contiguous() or t.device != x.device):
+            raise ValueError(f"{name} must be a contiguous {dt} CUDA tensor [{rows}, {HIDDEN}]")
+    if weight is not None and (weight.dtype != torch.bfloat16 or tuple(weight.shape) != (HIDDEN,)
+                               or not weight.is_contiguous() or weight.device != x.device):
+        raise ValueError(f"weight must be a contiguous bf16 CUDA tensor [{HIDDEN}]")
+    with torch.cuda.device(x.device):
+        _check(load().layer_front(x.data_ptr(), 1 if x.dtype == torch.float32 else 0,
+                                  None if weight is None else weight.data_ptr(),
+                                  stream_out.data_ptr(), None if aux is None else aux.data_ptr(),
+                                  out.data_ptr(), rows, float(eps), _stream(stream)))
+    return out
 
 
 def selftest_wait(timeout_ns: int, stream=None) -> None:

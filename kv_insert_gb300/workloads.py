@@ -226,3 +226,14 @@ def make_epi_inputs(w: EpiWorkload) -> dict:
                            generator=g).to(torch.bfloat16)
     return {"qkv": qkv, "positions": positions, "slots": slots, "cos_sin": cos_sin,
             "kv_cache": kv_cache}
+
+
+# ---- the predecessor of the front (first layer's front) ---------------------
+
+def make_layer_front_inputs(w: Workload) -> dict:
+    """Embedded tokens x_embed (bf16 [M, 8192], N(0, 1)) and the pre-QKV norm
+    weight (bf16 [8192], 1 + N(0, 0.1^2)), seeded from the workload's seed."""
+    g = torch.Generator().manual_seed(w.seed + 7919)
+    x_embed = torch.randn(w.M, HIDDEN, generator=g).to(torch.bfloat16)
+    weight = (1.0 + 0.1 * torch.randn(HIDDEN, generator=g)).to(torch.bfloat16)
+    return {"x_embed": x_embed, "norm_weight": weight}

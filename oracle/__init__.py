@@ -75,6 +75,8 @@ def _load():
         lib.oracle_qkv_front.restype = i32
         lib.oracle_qknorm_rope_kv_insert.argtypes = [vp, vp, vp, vp, i64, vp, i64, i32, i32, i32]
         lib.oracle_qknorm_rope_kv_insert.restype = i32
+        lib.oracle_layer_front.argtypes = [vp, i32, vp, vp, vp, vp, i32, i32, f32]
+        lib.oracle_layer_front.restype = None
         _lib = lib
         return lib
 
@@ -203,3 +205,23 @@ def qknorm_rope_kv_insert(qkv_bits, positions, slots, cos_sin, kv_cache_bits, nu
                                                _ptr(kv_cache_bits), kv_cache_bits.shape[0], T, N,
                                                num_kv_heads)
     return q, int(err)
+
+
+def layer_front(x, weight_bits=None, keep_aux=False, eps: float = EPS):
+    """The predecessor: x (uint16 bf16 bits or float32) [rows, hidden] ->
+    (stream f32, aux f32 or None, out bf16 bits)."""
+    x = np.ascontiguousarray(x)
+    if x.dtype not in (np.uint16, np.float32):
+        raise TypeError("x must be bf16 bits (uint16) or float32")
+    rows, hidden = x.shape
+    stream = np.empty((rows, hidden), np.float32)
+    aux = np.empty((rows, hidden), np.float32) if keep_aux else None
+    out = np.empty((rows, hidden), np.uint16)
+    w = None if weight_bits is None else _c(weight_bits, np.uint16)
+    if w is not None and w.shape != (hidden,):
+        raise ValueError("weight must be [hidden]")
+    _load().oracle_layer_front(_ptr(x), 1 if x.dtype == np.float32 else 0,
+                               None if w is None else _ptr(w), _ptr(stream),
+                               None if aux is None else _ptr(aux), _ptr(out), rows, hidden,
+                               float(eps))
+    return stream, aux, out

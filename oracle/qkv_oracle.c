@@ -259,3 +259,38 @@ int oracle_qknorm_rope_kv_insert(uint16_t *qkv, const int64_t *positions, const 
     }
     return err;
 }
+
+/* ---- the predecessor: the first layer's front -----------------------------
+ * Page "vllm.models.muse_spark.nvidia.specialized_decode.cutedsl.boundary.
+ * layer_front", class LayerFront: run(x, stream, out, aux) writes
+ * stream = x as FP32, aux = stream (when kept), and out = the layer's
+ * pre-QKV RMS norm of the stream, in BF16.  x is BF16 or FP32 [rows, 8192].
+ * Reading (the page names the norm, not its formula): the RMS norm of the
+ * whole row, r = 1 / sqrt(mean_j s_j^2 + eps) with the sum sequential in j,
+ * then out_j = bf16((s_j * r) * w_j) with the BF16 weight w widened to FP32
+ * (weightless when w is NULL: out_j = bf16(s_j * r)).  The result of this
+ * step is what the QKV front reads as x. */
+void oracle_layer_front(const void *x, int x_is_f32, const uint16_t *weight, float *stream,
+                        float *aux, uint16_t *out, int rows, int hidden, float eps)
+{
+    for (int t = 0; t < rows; ++t) {
+        float *srow = stream + (size_t)t * hidden;
+        for (int j = 0; j < hidden; ++j) {
+            srow[j] = x_is_f32 ? ((const float *)x)[(size_t)t * hidden + j]
+                               : oracle_bf16_to_f32(((const uint16_t *)x)[(size_t)t * hidden + j]);
+            if (aux) aux[(size_t)t * hidden + j] = srow[j];
+        }
+        float ss = 0.0f;
+        for (int j = 0; j < hidden; ++j) {
+            float sq = srow[j] * srow[j];
+            ss = ss + sq;
+        }
+        float ms = ss / (float)hidden;
+        float r = 1.0f / sqrtf(ms + eps);
+        for (int j = 0; j < hidden; ++j) {
+            float y = srow[j] * r;
+            if (weight) y = y * oracle_bf16_to_f32(weight[j]);
+            out[(size_t)t * hidden + j] = oracle_f32_to_bf16(y);
+        }
+    }
+}

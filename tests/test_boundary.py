@@ -172,3 +172,21 @@ def test_standalone_epilogue_refusals(lib):
     assert call() in (5, 6)                          # valid: reaches the device query
     why = lib.qknorm_rope_kv_insert_unsupported(X, POS, SL, CS, 4096, CACHE, 64, 100, 1152, 8)
     assert why is not None and b"1152" in why
+
+
+def test_layer_front_refusals(lib):
+    f = lib.layer_front
+    ok = dict(x=X, f32=0, w=0, s=SL, a=0, o=OUT, rows=8, eps=1e-6)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["x"], a["f32"], a["w"] or None, a["s"], a["a"] or None, a["o"], a["rows"],
+                 a["eps"], None)
+    assert call(rows=-1) == 1 and call(rows=(1 << 20) + 1) == 1
+    assert call(f32=2) == 9 and call(eps=0.0) == 9 and call(eps=-1.0) == 9
+    assert call(x=0) == 3 and call(o=0) == 3
+    assert call(x=X + 8) == 4 and call(a=CACHE + 4) == 4
+    assert call(o=SL + 64) == 9            # out inside stream
+    assert call(a=SL) == 9                 # aux is stream
+    assert call(rows=0, x=0) == 0
+    assert call() in (5, 6)                # valid: reaches the device query

@@ -465,3 +465,44 @@ def test_unfused_epilogue_index_rules(oracle_lib):
     assert np.array_equal(out[1], qkv[1])               # bad position: row untouched
     assert np.any(cache[0, 0, 0]) and not np.any(cache[0, 0, 1])   # slot 1 skipped
     assert not np.any(cache[1])                         # slot 40 out of range, -1 padding
+
+
+# ---- the predecessor (layer front) -------------------------------------------
+
+def test_layer_front_stream_is_exact_widening(oracle_lib):
+    """stream = x as FP32: bf16 widening and fp32 copies are exact; aux = stream."""
+    rng = np.random.default_rng(40)
+    xb = _bf(rng.standard_normal((3, 256)) * 5).reshape(3, 256)
+    stream, aux, _ = oracle.layer_front(xb, keep_aux=True)
+    assert np.array_equal(stream.view(np.uint32), (xb.astype(np.uint32) << 16))
+    assert np.array_equal(aux, stream)
+    xf = rng.standard_normal((2, 256)).astype(np.float32)
+    stream, aux, _ = oracle.layer_front(xf)
+    assert np.array_equal(stream, xf) and aux is None
+
+
+@pytest.mark.parametrize("c", [2.0 ** -10, 0.3, 7.0])
+def test_layer_front_constant_row_closed_form(oracle_lib, c):
+    """A constant row c with weight w: out = bf16(c / sqrt(c^2 + eps) * w) —
+    a mean over the row (not a sum), eps inside the root, the weight applied."""
+    hidden = 8192
+    x = np.full((1, hidden), c, np.float32)
+    w_vals = np.linspace(-2, 2, hidden).astype(np.float32)
+    wb = _bf(w_vals)
+    _, _, out = oracle.layer_front(x, wb)
+    wf = wl.from_bits(wb).double().numpy()
+    want = (c / math.sqrt(c * c + 1e-6)) * wf
+    got = wl.from_bits(out).double().numpy()[0]
+    assert np.all(np.abs(got - want) <= 2.0 ** -8 * np.abs(want) + 1e-30)
+
+
+def test_layer_front_rms_and_weight_linearity(oracle_lib):
+    """Weightless rows come out with RMS 1 (to BF16 rounding); a weight of 2
+    doubles every output exactly (power of two)."""
+    rng = np.random.default_rng(41)
+    x = (rng.standard_normal((4, 8192)) * 3).astype(np.float32)
+    _, _, out1 = oracle.layer_front(x)
+    v = wl.from_bits(out1).double().numpy()
+    assert np.all(np.abs(np.sqrt(np.mean(v ** 2, axis=1)) - 1.0) < 4e-3)
+    _, _, out2 = oracle.layer_front(x, _bf(np.full(8192, 2.0)))
+    assert np.array_equal(wl.from_bits(out2).double().numpy(), 2 * v)
