@@ -560,10 +560,12 @@ def run_chain(args, w: wl.Workload):
                   out)
 
     legs = {"chain": lambda i: (lf_call(), front_call(i)),
+            "chain_no_pdl": lambda i: (lf_call(), front_call(i)),
             "layer_front": lambda i: lf_call(),
             "qkv_front": front_call}
     timings = {}
     for name, fn in legs.items():
+        qf.set_pdl(name != "chain_no_pdl")
         with torch.cuda.stream(s):
             for i in range(args.warmup):
                 fn(i)
@@ -593,6 +595,7 @@ def run_chain(args, w: wl.Workload):
         torch.cuda.synchronize(dev)
         barrier()
         timings[name] = max_over_ranks(start.elapsed_time(end) / 1e3, dev) / args.steps * 1e6
+    qf.set_pdl(True)
     if qf.status():
         raise RuntimeError("device status raised in the timed region")
     if rank != 0:
@@ -608,7 +611,9 @@ def run_chain(args, w: wl.Workload):
             "qkv_front_alone_us": timings["qkv_front"],
             "sum_alone_us": timings["layer_front"] + timings["qkv_front"],
             "hidden_by_overlap_us": timings["layer_front"] + timings["qkv_front"] - timings["chain"],
-            "gpu_launches": 2 * args.steps, "e2e": None}
+            "chain_without_pdl_us": timings["chain_no_pdl"],
+            "pdl_gain_us": timings["chain_no_pdl"] - timings["chain"],
+            "gpu_launches": 2 * args.steps, "e2e": None}  # launches of the PDL chain leg
 
 
 def main(argv=None):

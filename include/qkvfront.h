@@ -233,6 +233,17 @@ const char *qkv_front_strerror(int code);
  */
 int qkv_front_selftest_wait(int64_t timeout_ns, void *stream);
 
+/*
+ * qkv_front_set_pdl: launch this library's kernels with programmatic stream
+ * serialization (enable = 1, the default) or as plain stream-ordered launches
+ * (0).  With PDL a kernel may start while the previous kernel on its stream
+ * still runs and streams its weights before waiting for it; turn it off when
+ * a kernel that may still be running writes W (or, for measurement, to see
+ * what the overlap gains).  Other values: QKVF_ERR_ARG.  Applies to launches
+ * made after the call, on every device.
+ */
+int qkv_front_set_pdl(int enable);
+
 /* Bounded-wait limit of the front's barrier waits in nanoseconds
  * (default 2e9); values outside 1e3..1e10 are refused with QKVF_ERR_ARG. */
 int qkv_front_set_wait_limit(int64_t ns);

@@ -5,9 +5,14 @@
 // boundary.layer_front", class LayerFront: run(x, stream, out, aux) writes
 // stream = x as FP32 (the residual stream), aux = stream when the layer keeps
 // one, and out = the layer's pre-QKV RMS norm of the stream in BF16 — the x
-// the QKV front reads.  x is BF16 or FP32 [rows, 8192].  With PDL it releases
-// its dependents right after its own wait, and the QKV front waits for this
-// grid before it reads out (page layer_front, module docstring).
+// the QKV front reads.  x is BF16 or FP32 [rows, 8192].  With PDL the page's
+// kernel releases its dependents right after its own wait, and the QKV front
+// waits for this grid before it reads out (page layer_front, module
+// docstring).  This one releases them at entry, before its wait: the front
+// reads only its weights before its own wait, which covers this grid and so,
+// transitively, the kernel before it; releasing early lets the next front's
+// CTAs take SMs the moment the previous front's CTAs leave, so its weight
+// stream also overlaps the previous front's tail, not only this kernel.
 //
 // The norm (the page names it, not its formula; the plainest reading): over
 // the whole row, r = 1 / sqrt(mean_j s_j^2 + eps); out_j = bf16((s_j r) w_j)
@@ -36,9 +41,9 @@ struct LayerFrontParams {
 __global__ void __launch_bounds__(kLfThreads) layer_front_kernel(const LayerFrontParams p)
 {
     __shared__ float warp_ss[kLfThreads / 32];
-    griddep_wait();   // x is written by the kernel before this one
-    // release dependents now: until their own wait they read only weights
+    // release dependents at once: until their own wait they read only weights
     if (threadIdx.x == 0) griddep_launch_dependents();
+    griddep_wait();   // x is written by the kernel before this one
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const size_t row = (size_t)blockIdx.x * kHidden;
     float v[4][8];
@@ -172,7 +177,7 @@ int layer_front(const void *x, int x_is_f32, const uint16_t *weight, float *stre
     cfg.stream = (cudaStream_t)cuda_stream;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr.val.programmaticStreamSerializationAllowed = 1;
+    attr.val.programmaticStreamSerializationAllowed = qkvf::g_pdl ? 1 : 0;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     if (cudaLaunchKernelEx(&cfg, qkvf::layer_front_kernel, prm) != cudaSuccess) {

@@ -355,7 +355,7 @@ int launch_epi(uint16_t *qkv, const int64_t *positions, const int64_t *slots, co
     cfg.stream = (cudaStream_t)stream;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr.val.programmaticStreamSerializationAllowed = 1;
+    attr.val.programmaticStreamSerializationAllowed = g_pdl ? 1 : 0;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     if (cudaLaunchKernelEx(&cfg, qknorm_rope_kv_insert_kernel, prm) != cudaSuccess) {

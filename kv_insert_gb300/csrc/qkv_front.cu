@@ -804,6 +804,7 @@ std::mutex g_mutex;
 DeviceState g_devices[kMaxDevices];
 EncodeTiledFn g_encode = nullptr;
 unsigned long long g_wait_limit_ns = 2000000000ull;
+bool g_pdl = true;   // launch with programmatic stream serialization
 
 using KernelFn = void (*)(CUtensorMap, CUtensorMap, FrontParams);
 
@@ -1023,7 +1024,7 @@ int launch_front(const uint16_t *x, const uint16_t *W, const int64_t *positions,
         ++na;
     }
     attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attrs[na].val.programmaticStreamSerializationAllowed = 1;
+    attrs[na].val.programmaticStreamSerializationAllowed = g_pdl ? 1 : 0;
     ++na;
     cfg.attrs = attrs;
     cfg.numAttrs = (unsigned)na;
@@ -1235,6 +1236,14 @@ int qkv_front_selftest_wait(int64_t timeout_ns, void *stream)
     if (rc != QKVF_OK) return rc;
     wait_selftest_kernel<<<1, 32, 0, (cudaStream_t)stream>>>((unsigned long long)timeout_ns);
     return cudaGetLastError() == cudaSuccess ? QKVF_OK : QKVF_ERR_CUDA;
+}
+
+int qkv_front_set_pdl(int enable)
+{
+    if (enable != 0 && enable != 1) return QKVF_ERR_ARG;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    g_pdl = enable != 0;
+    return QKVF_OK;
 }
 
 int qkv_front_set_wait_limit(int64_t ns)

@@ -97,6 +97,8 @@ def load() -> ctypes.CDLL:
         lib.qknorm_rope_kv_insert_unsupported.restype = ctypes.c_char_p
         lib.layer_front.argtypes = [vp, i32, vp, vp, vp, vp, i32, ctypes.c_float, vp]
         lib.layer_front.restype = i32
+        lib.qkv_front_set_pdl.argtypes = [i32]
+        lib.qkv_front_set_pdl.restype = i32
         _lib = lib
         return lib
 
@@ -386,6 +388,11 @@ def layer_front(x, stream_out, out, aux=None, weight=None, eps: float = 1e-6, st
 
 def selftest_wait(timeout_ns: int, stream=None) -> None:
     _check(load().qkv_front_selftest_wait(int(timeout_ns), _stream(stream)))
+
+
+def set_pdl(enable: bool) -> None:
+    """Launch the library's kernels with PDL (default) or plainly stream-ordered."""
+    _check(load().qkv_front_set_pdl(1 if enable else 0))
 
 
 def set_wait_limit(ns: int) -> None:

@@ -190,3 +190,8 @@ def test_layer_front_refusals(lib):
     assert call(a=SL) == 9                 # aux is stream
     assert call(rows=0, x=0) == 0
     assert call() in (5, 6)                # valid: reaches the device query
+
+
+def test_set_pdl_refusals(lib):
+    assert lib.qkv_front_set_pdl(2) == 9 and lib.qkv_front_set_pdl(-1) == 9
+    assert lib.qkv_front_set_pdl(0) == 0 and lib.qkv_front_set_pdl(1) == 0

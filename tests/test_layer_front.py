@@ -98,6 +98,18 @@ def test_pdl_chain_equals_serialized_calls(name):
     assert qf.status() == 0
 
 
+def test_chain_without_pdl_gives_the_same_bits():
+    w, inp, lf, g1 = _chain_inputs("m8_nkv8_n9216")
+    _chain(g1, sync_between=False)
+    _, _, _, g2 = _chain_inputs("m8_nkv8_n9216")
+    qf.set_pdl(False)
+    try:
+        _chain(g2, sync_between=False)
+    finally:
+        qf.set_pdl(True)
+    assert torch.equal(g2["out"].view(torch.int16), g1["out"].view(torch.int16))
+
+
 def test_pdl_chain_in_a_graph_matches_oracle():
     """The chain captured in a CUDA graph (PDL edges kept) against the oracle
     chain: oracle layer_front, then the oracle front on its output."""
