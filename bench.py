@@ -62,6 +62,8 @@ def parse_args(argv=None):
                     choices=sorted(wl.WORKLOADS) + sorted(wl.EPI_WORKLOADS))
     ap.add_argument("--graph-calls", type=int, default=96,
                     help="calls per captured CUDA graph (a multiple of the W copies is used)")
+    ap.add_argument("--front-stages", type=int, default=0,
+                    help="chain op: run the front at this ring depth (0: the library's choice)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -555,9 +557,15 @@ def run_chain(args, w: wl.Workload):
     def lf_call():
         qf.layer_front(g["x_embed"], stream_buf, x_attn, weight=g["norm_weight"])
 
+    v = qf.variant_full(w.N, w.M)
+
     def front_call(i):
-        qf.launch(x_attn, Ws[i % copies], g["positions"], g["slots"], g["cos_sin"], g["kv_cache"],
-                  out)
+        if args.front_stages:
+            qf.launch_variant(x_attn, Ws[i % copies], g["positions"], g["slots"], g["cos_sin"],
+                              g["kv_cache"], out, v["splits"], args.front_stages, kb=v["kb"])
+        else:
+            qf.launch(x_attn, Ws[i % copies], g["positions"], g["slots"], g["cos_sin"],
+                      g["kv_cache"], out)
 
     legs = {"chain": lambda i: (lf_call(), front_call(i)),
             "chain_no_pdl": lambda i: (lf_call(), front_call(i)),
@@ -606,6 +614,7 @@ def run_chain(args, w: wl.Workload):
             "data": "synthetic",
             "config": dict(w.describe(), **{
                 "l2": f"inputs larger than L2: W rotated over {copies} copies",
+                "front_variant": dict(v, stages=args.front_stages or v["stages"]),
                 "graph_calls": per_graph, "parallelism": f"replicas x{world}"}),
             "layer_front_alone_us": timings["layer_front"],
             "qkv_front_alone_us": timings["qkv_front"],
