@@ -237,3 +237,80 @@ def make_layer_front_inputs(w: Workload) -> dict:
     x_embed = torch.randn(w.M, HIDDEN, generator=g).to(torch.bfloat16)
     weight = (1.0 + 0.1 * torch.randn(HIDDEN, generator=g)).to(torch.bfloat16)
     return {"x_embed": x_embed, "norm_weight": weight}
+
+
+# ---- the cache's consumer: verify-step paged attention (attn2) --------------
+
+@dataclasses.dataclass(frozen=True)
+class AttnWorkload:
+    """R requests of the 8-token verify step (rows 8r..8r+7 of qkv), each with
+    its context length and its pages scattered over the cache."""
+    name: str
+    R: int
+    num_kv_heads: int
+    context: tuple          # one length per request (>= 8)
+    num_pages: int
+    seed: int
+    window: int = 0
+
+    @property
+    def N(self) -> int:
+        return columns_for(self.num_kv_heads)
+
+    def max_blocks(self) -> int:
+        return max((L + PAGE_SLOTS - 1) // PAGE_SLOTS for L in self.context)
+
+    def roofline_bytes(self) -> int:
+        """Algorithmic HBM bytes of one call: the K | V slots each request's
+        rows can see (read once per KV head), the q and gate heads read, the
+        output written, the block table and lengths."""
+        kv = 0
+        for L in self.context:
+            lo = max(0, L - 8 - self.window + 1) if self.window else 0
+            kv += (L - lo) * self.num_kv_heads * SLOT_WIDTH * 2
+        q_gate = self.R * 8 * 2 * Q_PER_KV * self.num_kv_heads * HEAD_DIM * 2
+        out = self.R * 8 * Q_PER_KV * self.num_kv_heads * HEAD_DIM * 2
+        return kv + q_gate + out + self.R * (self.max_blocks() * 4 + 4)
+
+    def describe(self) -> dict:
+        return {"workload": self.name, "requests": self.R, "query_rows": 8 * self.R,
+                "num_kv_heads": self.num_kv_heads, "context": list(self.context),
+                "window": self.window, "cache_pages": self.num_pages}
+
+
+ATTN_WORKLOADS: dict[str, AttnWorkload] = {}
+for _a in (AttnWorkload("attn_r1_l8_nkv1", R=1, num_kv_heads=1, context=(8,), num_pages=4, seed=5001),
+           AttnWorkload("attn_r3_mixed_nkv2", R=3, num_kv_heads=2, context=(8, 37, 300),
+                        num_pages=64, seed=5002),
+           AttnWorkload("attn_r2_window_nkv8", R=2, num_kv_heads=8, context=(700, 2051),
+                        num_pages=512, seed=5003, window=128),
+           AttnWorkload("attn_r1_l32k_nkv8", R=1, num_kv_heads=8, context=(32768,), num_pages=4096,
+                        seed=5004),
+           AttnWorkload("attn_r8_l4k_nkv8", R=8, num_kv_heads=8, context=(4096,) * 8,
+                        num_pages=4096, seed=5005)):
+    ATTN_WORKLOADS[_a.name] = _a
+
+ATTN_BENCH_WORKLOAD = "attn_r1_l32k_nkv8"
+
+
+def make_attn_inputs(w: AttnWorkload) -> dict:
+    """qkv (bf16 [8R, N], N(0, 1): q heads, gate heads and the rest), the
+    cache (bf16, N(0, 1)), a block table (int32 [R, max_blocks]) giving each
+    request distinct pages in random order, context lengths (int32 [R])."""
+    g = torch.Generator().manual_seed(w.seed)
+    qkv = torch.randn(8 * w.R, w.N, generator=g).to(torch.bfloat16)
+    kv_cache = torch.randn(w.num_pages, w.num_kv_heads, PAGE_SLOTS, SLOT_WIDTH,
+                           generator=g).to(torch.bfloat16)
+    mb = w.max_blocks()
+    need = sum((L + PAGE_SLOTS - 1) // PAGE_SLOTS for L in w.context)
+    if need > w.num_pages:
+        raise ValueError("not enough cache pages for the contexts")
+    perm = torch.randperm(w.num_pages, generator=g)[:need]
+    table = torch.full((w.R, mb), -1, dtype=torch.int32)
+    k = 0
+    for r, L in enumerate(w.context):
+        nb = (L + PAGE_SLOTS - 1) // PAGE_SLOTS
+        table[r, :nb] = perm[k:k + nb].to(torch.int32)
+        k += nb
+    lens = torch.tensor(w.context, dtype=torch.int32)
+    return {"qkv": qkv, "kv_cache": kv_cache, "block_table": table, "context_lens": lens}

@@ -29,7 +29,7 @@ SLOT_WIDTH = 128
 EPS = 1e-6
 
 HEAD_Q, HEAD_K, HEAD_V, HEAD_GATE = 0, 1, 2, 3
-ERR_SLOT, ERR_POSITION, ERR_SHAPE = 1, 2, 4
+ERR_SLOT, ERR_POSITION, ERR_SHAPE, ERR_ATTN_REQUEST = 1, 2, 4, 8
 
 _lock = threading.Lock()
 _lib = None
@@ -77,6 +77,9 @@ def _load():
         lib.oracle_qknorm_rope_kv_insert.restype = i32
         lib.oracle_layer_front.argtypes = [vp, i32, vp, vp, vp, vp, i32, i32, f32]
         lib.oracle_layer_front.restype = None
+        lib.oracle_attn2.argtypes = [vp, i32, i32, vp, i64, vp, i32, vp, i32, i32,
+                                     ctypes.c_double, ctypes.c_double, vp]
+        lib.oracle_attn2.restype = i32
         _lib = lib
         return lib
 
@@ -225,3 +228,26 @@ def layer_front(x, weight_bits=None, keep_aux=False, eps: float = EPS):
                                None if aux is None else _ptr(aux), _ptr(out), rows, hidden,
                                float(eps))
     return stream, aux, out
+
+
+def attn2(qkv_bits, kv_cache_bits, block_table, context_lens, num_kv_heads, window=0,
+          scale=0.125, eps=EPS, out_bits=None):
+    """Paged verify-step attention with o-norm and sigmoid gate.  qkv: uint16
+    [8 R, N]; block_table int32 [R, max_blocks]; context_lens int32 [R].
+    Returns (out uint16 [8 R, 8 nkv 64], err)."""
+    q = _c(qkv_bits, np.uint16)
+    cache = _c(kv_cache_bits, np.uint16)
+    bt = _c(np.asarray(block_table, dtype=np.int32), np.int32)
+    cl = _c(np.asarray(context_lens, dtype=np.int32), np.int32)
+    R = cl.shape[0]
+    T, N = q.shape
+    if T != 8 * R:
+        raise ValueError("qkv must hold 8 rows per request")
+    cols = Q_PER_KV * num_kv_heads * HEAD_DIM
+    out = np.zeros((T, cols), np.uint16) if out_bits is None else _c(out_bits, np.uint16).copy()
+    if R == 0:
+        return out, 0
+    err = _load().oracle_attn2(_ptr(q), N, num_kv_heads, _ptr(cache), cache.shape[0], _ptr(bt),
+                               bt.shape[1], _ptr(cl), R, int(window), float(scale), float(eps),
+                               _ptr(out))
+    return out, int(err)

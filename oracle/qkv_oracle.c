@@ -34,6 +34,7 @@
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #define ORACLE_HEAD_DIM 64        /* qkv_front page, module docstring: "one head (64 output columns)" */
@@ -293,4 +294,102 @@ void oracle_layer_front(const void *x, int x_is_f32, const uint16_t *weight, flo
             out[(size_t)t * hidden + j] = oracle_f32_to_bf16(y);
         }
     }
+}
+
+/* ---- the cache's consumer: attn2 ---------------------------------------------
+ * Page "...runtime.cute_ops", attn2 paragraph: paged decode attention of the
+ * 8-token verify step (one request: 1 + 7 draft tokens), head_dim 64, 8 query
+ * heads per KV head, the bf16 cache [pages, num_kv_heads, 16, 128] (K | V per
+ * slot), fused with the attention output's weightless RMS norm and sigmoid
+ * gate: the o_proj input.  Context length L >= 8, optional sliding window.
+ * Readings (the pages name these, not their formulas):
+ *   - request r owns rows 8r .. 8r+7 of qkv; row i is the token at position
+ *     L - 8 + i and attends keys j <= L - 8 + i (causal), and with a window W
+ *     only keys j > (L - 8 + i) - W;
+ *   - key j of request r is slot j % 16 of page block_table[r][j / 16];
+ *   - q head h (< 8 nkv) uses KV head h / 8; its gate is gate head h of the
+ *     same row ([q | k | v | gate] layout);
+ *   - o = softmax(scale q K^T) V, then out = bf16( o / sqrt(mean(o^2) + eps)
+ *     * sigmoid(gate) );
+ *   - all of it in double here (the pages fix no precision for it).
+ * A request with L < 8 or L beyond its block table, or a page index outside
+ * the cache, is skipped (its rows untouched) and reported (bit 8). */
+enum { ORACLE_ERR_ATTN_REQUEST = 8 };
+
+int oracle_attn2(const uint16_t *qkv, int N, int num_kv_heads, const uint16_t *kv_cache,
+                 int64_t num_pages, const int32_t *block_table, int max_blocks,
+                 const int32_t *context_lens, int R, int window, double scale, double eps,
+                 uint16_t *out)
+{
+    if (num_kv_heads < 1 || N != 2 * (ORACLE_Q_PER_KV + 1) * num_kv_heads * ORACLE_HEAD_DIM)
+        return ORACLE_ERR_SHAPE;
+    const int q_heads = ORACLE_Q_PER_KV * num_kv_heads;
+    const int gate_col = q_heads * ORACLE_HEAD_DIM + 2 * num_kv_heads * ORACLE_HEAD_DIM;
+    const int out_cols = q_heads * ORACLE_HEAD_DIM;
+    int err = 0;
+    int max_len = 0;
+    for (int r = 0; r < R; ++r)
+        if (context_lens[r] > max_len) max_len = context_lens[r];
+    double *sc = (double *)malloc(sizeof(double) * (size_t)(max_len > 0 ? max_len : 1));
+    if (!sc) return ORACLE_ERR_SHAPE;
+    for (int r = 0; r < R; ++r) {
+        const int L = context_lens[r];
+        int ok = L >= 8 && (L + ORACLE_PAGE_SLOTS - 1) / ORACLE_PAGE_SLOTS <= max_blocks;
+        for (int b = 0; ok && b < (L + ORACLE_PAGE_SLOTS - 1) / ORACLE_PAGE_SLOTS; ++b) {
+            int32_t pg = block_table[(size_t)r * max_blocks + b];
+            if (pg < 0 || pg >= num_pages) ok = 0;
+        }
+        if (!ok) {
+            err |= ORACLE_ERR_ATTN_REQUEST;
+            continue;
+        }
+        for (int i = 0; i < 8; ++i) {
+            const size_t row = (size_t)r * 8 + i;
+            const int pos = L - 8 + i;
+            const int lo = window > 0 && pos - window + 1 > 0 ? pos - window + 1 : 0;
+            for (int h = 0; h < q_heads; ++h) {
+                const int g = h / ORACLE_Q_PER_KV;
+                const uint16_t *q = qkv + row * N + (size_t)h * ORACLE_HEAD_DIM;
+                double m = -INFINITY;
+                /* scores, then their maximum */
+                for (int j = lo; j <= pos; ++j) {
+                    const int32_t pg = block_table[(size_t)r * max_blocks + j / ORACLE_PAGE_SLOTS];
+                    const uint16_t *k = kv_cache
+                        + (((size_t)pg * num_kv_heads + g) * ORACLE_PAGE_SLOTS + j % ORACLE_PAGE_SLOTS)
+                          * ORACLE_SLOT_WIDTH;
+                    double d = 0.0;
+                    for (int e = 0; e < ORACLE_HEAD_DIM; ++e)
+                        d += (double)oracle_bf16_to_f32(q[e]) * (double)oracle_bf16_to_f32(k[e]);
+                    sc[j - lo] = scale * d;
+                    if (sc[j - lo] > m) m = sc[j - lo];
+                }
+                double o[ORACLE_HEAD_DIM] = {0};
+                double l = 0.0;
+                for (int j = lo; j <= pos; ++j) {
+                    const int32_t pg = block_table[(size_t)r * max_blocks + j / ORACLE_PAGE_SLOTS];
+                    const uint16_t *v = kv_cache
+                        + (((size_t)pg * num_kv_heads + g) * ORACLE_PAGE_SLOTS + j % ORACLE_PAGE_SLOTS)
+                          * ORACLE_SLOT_WIDTH + ORACLE_HEAD_DIM;
+                    const double p = exp(sc[j - lo] - m);
+                    l += p;
+                    for (int e = 0; e < ORACLE_HEAD_DIM; ++e) o[e] += p * (double)oracle_bf16_to_f32(v[e]);
+                }
+                double ms = 0.0;
+                for (int e = 0; e < ORACLE_HEAD_DIM; ++e) {
+                    o[e] /= l;
+                    ms += o[e] * o[e];
+                }
+                ms /= ORACLE_HEAD_DIM;
+                const double rn = 1.0 / sqrt(ms + eps);
+                const uint16_t *gt = qkv + row * N + gate_col + (size_t)h * ORACLE_HEAD_DIM;
+                uint16_t *dst = out + row * out_cols + (size_t)h * ORACLE_HEAD_DIM;
+                for (int e = 0; e < ORACLE_HEAD_DIM; ++e) {
+                    const double sg = 1.0 / (1.0 + exp(-(double)oracle_bf16_to_f32(gt[e])));
+                    dst[e] = oracle_f32_to_bf16((float)(o[e] * rn * sg));
+                }
+            }
+        }
+    }
+    free(sc);
+    return err;
 }

@@ -506,3 +506,115 @@ def test_layer_front_rms_and_weight_linearity(oracle_lib):
     assert np.all(np.abs(np.sqrt(np.mean(v ** 2, axis=1)) - 1.0) < 4e-3)
     _, _, out2 = oracle.layer_front(x, _bf(np.full(8192, 2.0)))
     assert np.array_equal(wl.from_bits(out2).double().numpy(), 2 * v)
+
+
+# ---- verify-step paged attention (attn2) -------------------------------------
+
+def _torch_attn2(inp, nkv, window, scale, eps):
+    """The same op through torch's scaled_dot_product_attention in float64
+    (a library routine), gathering K and V through the block table."""
+    qkv = inp["qkv"].double()
+    cache = inp["kv_cache"].double()
+    R = inp["context_lens"].shape[0]
+    qh = 8 * nkv
+    out = torch.empty(8 * R, qh * 64, dtype=torch.float64)
+    gate0 = qh * 64 + 2 * nkv * 64
+    for r in range(R):
+        L = int(inp["context_lens"][r])
+        pages = inp["block_table"][r, : (L + 15) // 16].long()
+        kv = cache[pages].permute(1, 0, 2, 3).reshape(nkv, -1, 128)[:, :L]   # [nkv, L, 128]
+        pos = torch.arange(L - 8, L)[:, None]
+        j = torch.arange(L)[None, :]
+        ok = j <= pos
+        if window:
+            ok &= j > pos - window
+        for h in range(qh):
+            q = qkv[8 * r: 8 * r + 8, h * 64:(h + 1) * 64]
+            k, v = kv[h // 8, :, :64], kv[h // 8, :, 64:]
+            o = torch.nn.functional.scaled_dot_product_attention(
+                q[None], k[None], v[None], attn_mask=ok[None], scale=scale)[0]
+            o = o / torch.sqrt(torch.mean(o * o, dim=1, keepdim=True) + eps)
+            gt = qkv[8 * r: 8 * r + 8, gate0 + h * 64: gate0 + (h + 1) * 64]
+            out[8 * r: 8 * r + 8, h * 64:(h + 1) * 64] = o * torch.sigmoid(gt)
+    return out
+
+
+@pytest.mark.parametrize("name", ["attn_r1_l8_nkv1", "attn_r3_mixed_nkv2"])
+def test_attn2_matches_torch_sdpa(oracle_lib, name):
+    w = wl.ATTN_WORKLOADS[name]
+    inp = wl.make_attn_inputs(w)
+    out, err = oracle.attn2(wl.bits(inp["qkv"]), wl.bits(inp["kv_cache"]), inp["block_table"].numpy(),
+                            inp["context_lens"].numpy(), w.num_kv_heads, w.window)
+    assert err == 0
+    ref = _torch_attn2(inp, w.num_kv_heads, w.window, 0.125, 1e-6)
+    got = wl.from_bits(out).double()
+    assert torch.all((got - ref).abs() <= 2.0 ** -8 * ref.abs() + 1e-12)
+
+
+def test_attn2_window_matches_torch_sdpa(oracle_lib):
+    w = wl.AttnWorkload("win", R=2, num_kv_heads=1, context=(40, 100), num_pages=16, seed=77,
+                        window=20)
+    inp = wl.make_attn_inputs(w)
+    out, err = oracle.attn2(wl.bits(inp["qkv"]), wl.bits(inp["kv_cache"]), inp["block_table"].numpy(),
+                            inp["context_lens"].numpy(), 1, 20)
+    ref = _torch_attn2(inp, 1, 20, 0.125, 1e-6)
+    assert err == 0
+    assert torch.all((wl.from_bits(out).double() - ref).abs() <= 2.0 ** -8 * ref.abs() + 1e-12)
+
+
+def test_attn2_window_one_is_own_value(oracle_lib):
+    """A window of 1 leaves each row its own key: o = V of position L-8+i, so
+    out = bf16(norm(V) * sigmoid(gate)) (closed form, no softmax)."""
+    w = wl.AttnWorkload("w1", R=1, num_kv_heads=1, context=(20,), num_pages=4, seed=78, window=1)
+    inp = wl.make_attn_inputs(w)
+    out, err = oracle.attn2(wl.bits(inp["qkv"]), wl.bits(inp["kv_cache"]), inp["block_table"].numpy(),
+                            inp["context_lens"].numpy(), 1, 1)
+    assert err == 0
+    cache = inp["kv_cache"].double()
+    for i in range(8):
+        p = 12 + i
+        page = int(inp["block_table"][0, p // 16])
+        v = cache[page, 0, p % 16, 64:]
+        o = v / torch.sqrt(torch.mean(v * v) + 1e-6)
+        for h in range(8):
+            gt = inp["qkv"][i, 512 + 128 + h * 64: 512 + 128 + (h + 1) * 64].double()
+            want = (o * torch.sigmoid(gt)).float().to(torch.bfloat16)
+            assert torch.equal(wl.from_bits(out[i, h * 64:(h + 1) * 64]), want)
+
+
+def test_attn2_causal_and_page_remap(oracle_lib):
+    """Keys after a row's position do not change it; moving the request's
+    pages elsewhere in the cache (same contents) changes nothing."""
+    w = wl.AttnWorkload("c", R=1, num_kv_heads=1, context=(50,), num_pages=16, seed=79)
+    inp = wl.make_attn_inputs(w)
+    args = (inp["block_table"].numpy(), inp["context_lens"].numpy(), 1)
+    base, _ = oracle.attn2(wl.bits(inp["qkv"]), wl.bits(inp["kv_cache"]), *args)
+    cache = wl.bits(inp["kv_cache"]).copy()
+    last = 49
+    pg = int(inp["block_table"][0, last // 16])
+    cache[pg, 0, last % 16, :] ^= 0x0101                     # perturb key/value 49
+    pert, _ = oracle.attn2(wl.bits(inp["qkv"]), cache, *args)
+    assert np.array_equal(pert[:7], base[:7])                # rows 0..6 cannot see key 49
+    assert not np.array_equal(pert[7], base[7])              # row 7 can
+    table = inp["block_table"].numpy().copy()
+    used = table[0, :4]
+    free = np.setdiff1d(np.arange(16), used)[:4]
+    moved = wl.bits(inp["kv_cache"]).copy()
+    moved[free] = moved[used]
+    table[0, :4] = free
+    remap, _ = oracle.attn2(wl.bits(inp["qkv"]), moved, table, inp["context_lens"].numpy(), 1)
+    assert np.array_equal(remap, base)
+
+
+def test_attn2_bad_requests_are_skipped(oracle_lib):
+    w = wl.AttnWorkload("bad", R=2, num_kv_heads=1, context=(20, 20), num_pages=8, seed=80)
+    inp = wl.make_attn_inputs(w)
+    lens = inp["context_lens"].numpy().copy()
+    lens[0] = 5                                             # shorter than the 8 rows
+    table = inp["block_table"].numpy().copy()
+    table[1, 1] = 99                                        # page outside the cache
+    start = np.full((16, 512), 0x1234, np.uint16)
+    out, err = oracle.attn2(wl.bits(inp["qkv"]), wl.bits(inp["kv_cache"]), table, lens, 1,
+                            out_bits=start)
+    assert err == oracle.ERR_ATTN_REQUEST
+    assert np.all(out == 0x1234)
