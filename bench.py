@@ -43,7 +43,8 @@ UNIT = "GB/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = [os.path.join(ROOT, "kv_insert_gb300", "csrc", f)
-                  for f in ("qkv_front.cu", "qknorm_rope_kv_insert.cuh", "layer_front.cuh")]
+                  for f in ("qkv_front.cu", "qknorm_rope_kv_insert.cuh", "layer_front.cuh",
+                            "attn2.cuh")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 
 

@@ -59,6 +59,7 @@ extern "C" {
 #define QKVF_STATUS_BAD_SLOT 1u      /* a slot >= num_pages * 16: that token's insert skipped */
 #define QKVF_STATUS_BAD_POSITION 2u  /* a position outside [0, cos_sin_rows): its q/k heads and insert skipped */
 #define QKVF_STATUS_WAIT_TIMEOUT 4u  /* a bounded wait in the kernel gave up: outputs of that call are invalid */
+#define QKVF_STATUS_BAD_REQUEST 8u   /* attn2: a request with L < 8, L beyond its table, or a page outside the cache: its rows skipped */
 
 /*
  * qkv_front: check the call, then launch the fused front.
@@ -220,6 +221,46 @@ const char *qknorm_rope_kv_insert_unsupported(uint16_t *qkv, const int64_t *posi
  */
 int layer_front(const void *x, int x_is_f32, const uint16_t *weight, float *stream, float *aux,
                 uint16_t *out, int rows, float eps, void *cuda_stream);
+
+/*
+ * attn2: paged decode attention of the 8-token verify step fused with the
+ * output's weightless RMS norm and sigmoid gate — the o_proj input (page
+ * cute_ops, attn2 paragraph).  For each request r (query rows 8r .. 8r+7 of
+ * qkv, row i the token at position L_r - 8 + i):
+ *   out[8r+i, head h] = bf16( o / sqrt(mean(o^2) + eps) * sigmoid(gate) ),
+ *   o = softmax(scale * q K^T) V over keys j <= L_r - 8 + i (and, with a
+ *   window W > 0, j > L_r - 8 + i - W); q = q head h of the row, gate = gate
+ *   head h of the row, K and V from KV head h / 8 of the cache.
+ *   qkv          [8 R, N] bf16 bits, rows [q | k | v | gate] (the front's out).
+ *   kv_cache     [num_pages, num_kv_heads, 16, 128] bf16 bits (K | V per slot).
+ *   block_table  [R, max_blocks] int32: key j of request r is slot j % 16 of
+ *                page block_table[r][j / 16].
+ *   context_lens [R] int32, each >= 8.
+ *   out          [8 R, 512 num_kv_heads] bf16 bits.
+ *   window       0 (none) or W >= 1; scale > 0 (1/8 for head_dim 64);
+ *   eps in (0, 1].  num_reqs 0 .. 65535.
+ * A request whose length is < 8 or needs more than max_blocks pages, or
+ * whose table names a page outside the cache, is skipped (its rows left as
+ * they were) and raises QKVF_STATUS_BAD_REQUEST.  Long contexts are split
+ * over up to 16 CTAs of a cluster, chosen from num_reqs, num_kv_heads and
+ * max_blocks (not from the lengths, which stay on the device); the split
+ * partials are merged through distributed shared memory in a fixed order.
+ * Allocates nothing; launched with PDL like qkv_front.
+ */
+int attn2(const uint16_t *qkv, const uint16_t *kv_cache, int64_t num_pages,
+          const int32_t *block_table, int max_blocks, const int32_t *context_lens, int num_reqs,
+          int N, int num_kv_heads, int window, float scale, float eps, uint16_t *out,
+          void *stream);
+
+/* attn2 at an explicit split (1, 2, 4, 8 or 16 CTAs per request and KV head;
+ * otherwise QKVF_ERR_VARIANT), for tests and tuning. */
+int attn2_launch_splits(const uint16_t *qkv, const uint16_t *kv_cache, int64_t num_pages,
+                        const int32_t *block_table, int max_blocks, const int32_t *context_lens,
+                        int num_reqs, int N, int num_kv_heads, int window, float scale, float eps,
+                        uint16_t *out, int splits, void *stream);
+
+/* The split attn2 uses for this shape on the current device (0 on bad input). */
+int attn2_splits(int num_reqs, int num_kv_heads, int max_blocks);
 
 /* Static text of a QKVF_* return code. */
 const char *qkv_front_strerror(int code);

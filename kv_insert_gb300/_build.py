@@ -10,7 +10,8 @@ ROOT = os.path.dirname(PKG)
 SOURCES = [os.path.join(PKG, "csrc", "qkv_front.cu")]
 HEADERS = [os.path.join(ROOT, "include", "qkvfront.h"),
            os.path.join(PKG, "csrc", "qknorm_rope_kv_insert.cuh"),
-           os.path.join(PKG, "csrc", "layer_front.cuh")]
+           os.path.join(PKG, "csrc", "layer_front.cuh"),
+           os.path.join(PKG, "csrc", "attn2.cuh")]
 LIB_PATH = os.path.join(PKG, "libqkvfront.so")
 
 NVCC_FLAGS = [

@@ -1,0 +1,543 @@
+// attn2: the consumer of the paged cache the front fills — decode attention of
+// the 8-token verify step fused with the output's weightless RMS norm and
+// sigmoid gate (included by qkv_front.cu: one translation unit).
+//
+// Source: page "vllm.models.muse_spark.nvidia.specialized_decode.runtime.
+// cute_ops", attn2 paragraph: one request = 1 + 7 draft tokens = 8 query rows,
+// head_dim 64, 8 query heads per KV head, the bf16 cache [pages, num_kv_heads,
+// 16, 128] (K | V per slot), any context length L >= 8, an optional sliding
+// window, one launch for the rank's KV heads; the result is the o_proj input.
+// Readings where the page is silent (the same in the oracle): row i of a
+// request is the token at position L - 8 + i and sees keys j <= L - 8 + i
+// (and j > L - 8 + i - W with a window W); key j is slot j % 16 of page
+// block_table[r][j / 16]; q head h reads KV head h / 8 and is gated by gate
+// head h of its row; out = bf16(o / sqrt(mean(o^2) + eps) * sigmoid(gate))
+// with o = softmax(scale q K^T) V.
+//
+// Design: a CTA per (request r, KV head g, split z).  Its 64 query rows
+// (8 tokens x 8 heads, row 8 i + j) stay in registers as mma.sync A
+// fragments; a producer warp streams the CTA's pages (pages p0 + z,
+// p0 + z + S, ...) as two 16 x 64 TMA boxes each (K and V halves, 128-byte
+// swizzle) into a ring; four compute warps (16 rows each) run QK^T, the online
+// softmax (base 2) and PV with mma.sync, P going from the S accumulators
+// straight into the A fragments.  The S CTAs of a (request, KV head) form a
+// cluster and merge their (max, sum, O) through distributed shared memory in
+// rank order — no global workspace, deterministic for a launch shape — then
+// each rank finishes 64 / S rows: o-norm, gate, BF16 store.
+
+namespace qkvf {
+
+constexpr int kA2ComputeWarps = 4;
+constexpr int kA2Threads = 32 * (kA2ComputeWarps + 1);   // warp 4 produces
+constexpr int kA2Stages = 8;                              // pages in flight per CTA
+constexpr uint32_t kA2PageBytes = 4096;                   // K box + V box
+constexpr int kA2OStride = 68;                            // floats per row of the O partial
+constexpr int kA2MaxSplits = 16;
+constexpr int kA2MaxRequests = 65535;   // grid z
+
+struct A2Layout {
+    uint32_t q, ring, full, empty, o, m, l, flags, total;
+};
+
+__host__ __device__ inline A2Layout a2_layout()
+{
+    A2Layout L;
+    uint32_t off = 0;
+    L.q = off;
+    off += 64 * 128;
+    L.ring = off;
+    off += kA2Stages * kA2PageBytes;
+    L.full = off;
+    off += kA2Stages * 8;
+    L.empty = off;
+    off += kA2Stages * 8;
+    L.o = off;
+    off += 64 * kA2OStride * 4;
+    L.m = off;
+    off += 64 * 4;
+    L.l = off;
+    off += 64 * 4;
+    L.flags = off;
+    off += 16;
+    L.total = off + 1024;   // alignment slack
+    return L;
+}
+
+struct Attn2Params {
+    const uint16_t *qkv;
+    const int32_t *block_table;
+    const int32_t *context_lens;
+    uint16_t *out;
+    int64_t num_pages;
+    unsigned long long wait_limit_ns;
+    int max_blocks;
+    int N;
+    int nkv;
+    int window;
+    int splits;
+    float scale_log2;   // softmax scale times log2(e)
+    float eps;
+};
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *m, uint32_t bar, int c0,
+                                            int c1, int c2, int c3)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                              uint32_t &r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ uint32_t pack_f2bf(float lo, float hi)
+{
+    return pack_bf16x2(__float2bfloat16_rn(lo), __float2bfloat16_rn(hi));
+}
+
+__global__ void __launch_bounds__(kA2Threads, 1)
+    attn2_kernel(const __grid_constant__ CUtensorMap tmKV, const Attn2Params p)
+{
+    extern __shared__ uint8_t a2_smem_dyn[];
+    uint8_t *smem = a2_smem_dyn + ((1024u - (smem_u32(a2_smem_dyn) & 1023u)) & 1023u);
+    const A2Layout LY = a2_layout();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int S = p.splits;
+    const uint32_t z = S > 1 ? cluster_rank() : 0u;
+    const int g = blockIdx.y, r = blockIdx.z;
+    const uint32_t sQ = smem_u32(smem + LY.q), sRing = smem_u32(smem + LY.ring);
+    const uint32_t full0 = smem_u32(smem + LY.full), empty0 = smem_u32(smem + LY.empty);
+    float *o_part = reinterpret_cast<float *>(smem + LY.o);
+    float *m_part = reinterpret_cast<float *>(smem + LY.m);
+    float *l_part = reinterpret_cast<float *>(smem + LY.l);
+    volatile int *s_flags = reinterpret_cast<volatile int *>(smem + LY.flags);   // [0] abort, [1] request ok
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kA2Stages; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, kA2ComputeWarps);
+        }
+        s_flags[0] = 0;
+        fence_barrier_init();
+        griddep_launch_dependents();
+    }
+    __syncthreads();
+    griddep_wait();   // q, the cache, the table and the lengths come from earlier kernels
+
+    // ---- the request: length, visible pages, table entries in range --------
+    const int L = p.context_lens[r];
+    const int nblk = (L + kPageSlots - 1) / kPageSlots;
+    const bool len_ok = L >= 8 && nblk <= p.max_blocks;
+    const int p_first = (p.window > 0 && L - 8 - p.window + 1 > 0) ? (L - 8 - p.window + 1) / kPageSlots : 0;
+    const int p_last = len_ok ? (L - 1) / kPageSlots : -1;
+    const int32_t *bt = p.block_table + (size_t)r * p.max_blocks;
+    if (warp == kA2ComputeWarps) {
+        unsigned bad = len_ok ? 0u : 1u;
+        for (int b = p_first + lane; b <= p_last; b += 32) {
+            const int32_t pg = bt[b];
+            if (pg < 0 || pg >= p.num_pages) bad = 1u;
+        }
+        bad = __reduce_or_sync(0xffffffffu, bad);
+        if (lane == 0) {
+            s_flags[1] = bad ? 0 : 1;
+            if (bad && z == 0 && g == 0) atomicOr(&g_status, QKVF_STATUS_BAD_REQUEST);
+        }
+    }
+    __syncthreads();
+    const bool req_ok = s_flags[1] != 0;
+    const int first_mine = p_first + (int)z;
+    const int npages = (req_ok && first_mine <= p_last) ? (p_last - first_mine) / S + 1 : 0;
+
+    if (warp == kA2ComputeWarps) {
+        // ---- produce: K and V boxes of this CTA's pages -------------------
+        if (lane == 0) {
+            tma_prefetch_map(&tmKV);
+            int issued = 0;
+            for (int k = 0; k < npages; ++k) {
+                const int s = k % kA2Stages, use = k / kA2Stages;
+                if (use > 0 && !bounded_wait(empty0 + 8 * s, (uint32_t)((use - 1) & 1),
+                                             s_flags, p.wait_limit_ns, true))
+                    break;
+                const int page = bt[first_mine + k * S];
+                const uint32_t dst = sRing + (uint32_t)s * kA2PageBytes;
+                mbar_expect_tx(full0 + 8 * s, kA2PageBytes);
+                tma_load_4d(dst, &tmKV, full0 + 8 * s, 0, 0, 0, page * p.nkv + g);          // K half
+                tma_load_4d(dst + 2048, &tmKV, full0 + 8 * s, 0, 1, 0, page * p.nkv + g);   // V half
+                ++issued;
+            }
+            if (s_flags[0]) {   // drain our copies before leaving
+                const int first = issued > kA2Stages ? issued - kA2Stages : 0;
+                for (int k = first; k < issued; ++k)
+                    bounded_wait(full0 + 8 * (k % kA2Stages), (uint32_t)((k / kA2Stages) & 1),
+                                 s_flags, p.wait_limit_ns, false);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---- compute ------------------------------------------------------
+        const int tid = threadIdx.x;   // 0..127
+        if (req_ok) {
+            // Q tile [64 rows][64 dims], row 8 i + j = token i, head 8 g + j;
+            // 128-byte rows with the chunk XORed by row % 8 (as TMA would)
+            for (int c = tid; c < 512; c += 128) {
+                const int row = c >> 3, cc = c & 7;
+                const uint4 v = *reinterpret_cast<const uint4 *>(
+                    p.qkv + ((size_t)r * 8 + (row >> 3)) * p.N + (size_t)(8 * g + (row & 7)) * kHeadDim + 8 * cc);
+                *reinterpret_cast<uint4 *>(smem + LY.q + row * 128 + ((cc ^ (row & 7)) << 4)) = v;
+            }
+        }
+        consumer_bar_sync();
+        const int gq = lane >> 2, t = lane & 3;
+        uint32_t qa[4][4];
+        const uint32_t a_row = (uint32_t)(warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            ldsm_x4(sQ + a_row * 128u + ((((uint32_t)(2 * kk) + (uint32_t)(lane >> 4)) ^ (uint32_t)(lane & 7)) << 4),
+                    qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+
+        // this thread's rows: 16 w + gq (token 2 w) and 16 w + gq + 8 (token 2 w + 1)
+        const int pos_a = L - 8 + 2 * warp, pos_b = pos_a + 1;
+        const int lo_a = p.window > 0 ? pos_a - p.window + 1 : 0;
+        const int lo_b = p.window > 0 ? pos_b - p.window + 1 : 0;
+        float o[8][4];
+#pragma unroll
+        for (int nd = 0; nd < 8; ++nd)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o[nd][e] = 0.f;
+        float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
+
+        const uint32_t k_key = (uint32_t)((lane & 7) + ((lane >> 4) << 3));   // K: ldmatrix row
+        const uint32_t k_hi = (uint32_t)((lane >> 3) & 1);
+        const uint32_t v_key = (uint32_t)((lane & 7) + ((lane >> 3) & 1) * 8); // V: ldmatrix.trans row
+        const uint32_t v_hi = (uint32_t)(lane >> 4);
+        const uint32_t sw = (uint32_t)(lane & 7);
+
+        for (int k = 0; k < npages; ++k) {
+            const int s = k % kA2Stages;
+            const uint32_t ph = (uint32_t)((k / kA2Stages) & 1);
+            const bool landed = mbar_try_wait(full0 + 8 * s, ph) ||
+                                bounded_wait(full0 + 8 * s, ph, s_flags, p.wait_limit_ns, true);
+            if (__all_sync(0xffffffffu, landed)) {
+                const uint32_t kbox = sRing + (uint32_t)s * kA2PageBytes, vbox = kbox + 2048;
+                const int key0 = (first_mine + k * S) * kPageSlots;
+                float sc[2][4];
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) sc[nt][e] = 0.f;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(kbox + k_key * 128u + ((((uint32_t)(2 * kk) + k_hi) ^ sw) << 4), b0, b1, b2, b3);
+                    mma_bf16_16816(sc[0], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
+                    mma_bf16_16816(sc[1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
+                }
+                // scale into base 2 and mask: element e of tile nt is key key0 + 8 nt + 2 t + (e & 1),
+                // row a for e < 2, row b otherwise
+                float mx_a = -INFINITY, mx_b = -INFINITY;
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int key = key0 + 8 * nt + 2 * t + (e & 1);
+                        const bool rb = e >= 2;
+                        const bool ok = rb ? (key >= lo_b && key <= pos_b) : (key >= lo_a && key <= pos_a);
+                        const float v = ok ? sc[nt][e] * p.scale_log2 : -INFINITY;
+                        sc[nt][e] = v;
+                        if (rb) mx_b = fmaxf(mx_b, v);
+                        else mx_a = fmaxf(mx_a, v);
+                    }
+#pragma unroll
+                for (int off = 1; off <= 2; off <<= 1) {
+                    mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, off));
+                    mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, off));
+                }
+                const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
+                const float base_a = mn_a == -INFINITY ? 0.f : mn_a;
+                const float base_b = mn_b == -INFINITY ? 0.f : mn_b;
+                const float al_a = exp2f(m_a - base_a), al_b = exp2f(m_b - base_b);
+                float pv[2][4];
+                float sum_a = 0.f, sum_b = 0.f;
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float pe = exp2f(sc[nt][e] - (e >= 2 ? base_b : base_a));
+                        pv[nt][e] = pe;
+                        if (e >= 2) sum_b += pe;
+                        else sum_a += pe;
+                    }
+                l_a = l_a * al_a + sum_a;
+                l_b = l_b * al_b + sum_b;
+                m_a = mn_a;
+                m_b = mn_b;
+#pragma unroll
+                for (int nd = 0; nd < 8; ++nd) {
+                    o[nd][0] *= al_a;
+                    o[nd][1] *= al_a;
+                    o[nd][2] *= al_b;
+                    o[nd][3] *= al_b;
+                }
+                // P (rows a / b x 16 keys) as the A fragment of PV
+                const uint32_t pa0 = pack_f2bf(pv[0][0], pv[0][1]), pa1 = pack_f2bf(pv[0][2], pv[0][3]);
+                const uint32_t pa2 = pack_f2bf(pv[1][0], pv[1][1]), pa3 = pack_f2bf(pv[1][2], pv[1][3]);
+#pragma unroll
+                for (int q2 = 0; q2 < 4; ++q2) {   // dims 16 q2 .. 16 q2 + 15
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_trans(vbox + v_key * 128u + ((((uint32_t)(2 * q2) + v_hi) ^ sw) << 4), b0, b1, b2, b3);
+                    mma_bf16_16816(o[2 * q2], pa0, pa1, pa2, pa3, b0, b1);
+                    mma_bf16_16816(o[2 * q2 + 1], pa0, pa1, pa2, pa3, b2, b3);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8 * s);
+        }
+        // whole-row sums across the four threads of a row
+#pragma unroll
+        for (int off = 1; off <= 2; off <<= 1) {
+            l_a += __shfl_xor_sync(0xffffffffu, l_a, off);
+            l_b += __shfl_xor_sync(0xffffffffu, l_b, off);
+        }
+        consumer_bar_sync();   // the partials do not alias the ring, but keep one order
+        const int ra = warp * 16 + gq, rb = ra + 8;
+#pragma unroll
+        for (int nd = 0; nd < 8; ++nd) {
+            o_part[ra * kA2OStride + 8 * nd + 2 * t] = o[nd][0];
+            o_part[ra * kA2OStride + 8 * nd + 2 * t + 1] = o[nd][1];
+            o_part[rb * kA2OStride + 8 * nd + 2 * t] = o[nd][2];
+            o_part[rb * kA2OStride + 8 * nd + 2 * t + 1] = o[nd][3];
+        }
+        if (t == 0) {
+            m_part[ra] = m_a;
+            m_part[rb] = m_b;
+            l_part[ra] = l_a;
+            l_part[rb] = l_b;
+        }
+    }
+    __syncthreads();
+    if (S > 1) cluster_sync_all();
+
+    // ---- merge the ranks' partials, o-norm, gate, store (64 / S rows each) ----
+    if (req_ok) {
+        const int rows = 64 / S;
+        const int q_heads = kQPerKv * p.nkv;
+        const int gate_col = q_heads * kHeadDim + 2 * p.nkv * kHeadDim;
+        const int out_cols = q_heads * kHeadDim;
+        const uint32_t o_addr = smem_u32(o_part), m_addr = smem_u32(m_part), l_addr = smem_u32(l_part);
+        for (int i = warp; i < rows; i += kA2ComputeWarps + 1) {
+            const int row = (int)z * rows + i;
+            float M = -INFINITY;
+            for (int src = 0; src < S; ++src) {
+                const float mk = S > 1 ? ld_cluster_f32(map_to_rank(m_addr + 4u * row, (uint32_t)src))
+                                       : m_part[row];
+                M = fmaxf(M, mk);
+            }
+            const float base = M == -INFINITY ? 0.f : M;
+            float lt = 0.f, o0 = 0.f, o1 = 0.f;
+            for (int src = 0; src < S; ++src) {
+                float mk, lk;
+                float2 ok;
+                if (S > 1) {
+                    mk = ld_cluster_f32(map_to_rank(m_addr + 4u * row, (uint32_t)src));
+                    lk = ld_cluster_f32(map_to_rank(l_addr + 4u * row, (uint32_t)src));
+                    ok = ld_cluster_f2(map_to_rank(o_addr + 4u * (row * kA2OStride + 2 * lane), (uint32_t)src));
+                } else {
+                    mk = m_part[row];
+                    lk = l_part[row];
+                    ok = *reinterpret_cast<const float2 *>(o_part + row * kA2OStride + 2 * lane);
+                }
+                const float w = exp2f(mk - base);
+                lt = lt + lk * w;
+                o0 = o0 + ok.x * w;
+                o1 = o1 + ok.y * w;
+            }
+            const float inv = lt > 0.f ? 1.0f / lt : 0.f;
+            o0 *= inv;
+            o1 *= inv;
+            float ss = o0 * o0 + o1 * o1;
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            const float rn = 1.0f / sqrtf(ss * (1.0f / kHeadDim) + p.eps);
+            const int tok = row >> 3, hj = 8 * g + (row & 7);
+            const size_t qrow = (size_t)r * 8 + tok;
+            const __nv_bfloat162 gt = *reinterpret_cast<const __nv_bfloat162 *>(
+                p.qkv + qrow * p.N + gate_col + (size_t)hj * kHeadDim + 2 * lane);
+            const float s0 = 1.0f / (1.0f + expf(-__low2float(gt)));
+            const float s1 = 1.0f / (1.0f + expf(-__high2float(gt)));
+            reinterpret_cast<uint32_t *>(p.out + qrow * out_cols + (size_t)hj * kHeadDim)[lane] =
+                pack_f2bf(o0 * rn * s0, o1 * rn * s1);
+        }
+    }
+    if (S > 1) cluster_sync_all();   // no CTA leaves while its partials may still be read
+}
+
+int encode_kv_map(const uint16_t *kv_cache, int64_t num_pages, int nkv, CUtensorMap *m)
+{
+    // [pages * nkv][16 slots][2 halves][64]: dim 0 = 64 elements of a half,
+    // dim 1 = K / V half, dim 2 = slot, dim 3 = (page, KV head)
+    const cuuint64_t dims[4] = {64, 2, (cuuint64_t)kPageSlots, (cuuint64_t)num_pages * nkv};
+    const cuuint64_t strides[3] = {128, 256, (cuuint64_t)kPageSlots * kSlotWidth * 2};
+    const cuuint32_t box[4] = {64, 1, (cuuint32_t)kPageSlots, 1};
+    const cuuint32_t es[4] = {1, 1, 1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, (void *)kv_cache, dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+               ? QKVF_OK
+               : QKVF_ERR_CUDA;
+}
+
+const char *check_attn2_args(const uint16_t *qkv, const uint16_t *kv_cache, int64_t num_pages,
+                             const int32_t *block_table, int max_blocks, const int32_t *context_lens,
+                             int num_reqs, int N, int num_kv_heads, int window, float scale, float eps,
+                             uint16_t *out, int *code)
+{
+    *code = QKVF_ERR_TOKENS;
+    if (num_reqs < 0 || num_reqs > kA2MaxRequests) return "num_reqs must be 0..65535";
+    *code = QKVF_ERR_SHAPE;
+    if (num_kv_heads < 1 || num_kv_heads > 64) return "num_kv_heads must be 1..64";
+    if (N != 2 * (kQPerKv + 1) * kHeadDim * num_kv_heads)
+        return "N must be 1152 * num_kv_heads: rows [q | k | v | gate]";
+    *code = QKVF_ERR_SIZES;
+    if (num_pages < 1 || num_pages * num_kv_heads > (int64_t(1) << 31)) return "num_pages * num_kv_heads must be 1..2^31";
+    if (max_blocks < 1 || max_blocks > (1 << 24)) return "max_blocks must be 1..2^24";
+    *code = QKVF_ERR_ARG;
+    if (window < 0) return "window must be >= 0 (0: none)";
+    if (!(scale > 0.f) || !(eps > 0.f) || eps > 1.f) return "scale must be > 0 and eps in (0, 1]";
+    *code = QKVF_OK;
+    if (num_reqs == 0) return nullptr;
+    *code = QKVF_ERR_NULL;
+    if (!qkv || !kv_cache || !block_table || !context_lens || !out) return "a required pointer is NULL";
+    *code = QKVF_ERR_ALIGN;
+    if (!aligned(qkv, 16) || !aligned(kv_cache, 16) || !aligned(out, 16))
+        return "qkv, kv_cache and out must be 16-byte aligned";
+    if (!aligned(block_table, 4) || !aligned(context_lens, 4)) return "block_table and context_lens must be int32-aligned";
+    *code = QKVF_ERR_ARG;
+    const size_t out_b = (size_t)num_reqs * 8 * kQPerKv * num_kv_heads * kHeadDim * 2;
+    const size_t qkv_b = (size_t)num_reqs * 8 * N * 2;
+    const size_t cache_b = (size_t)num_pages * num_kv_heads * kPageSlots * kSlotWidth * 2;
+    const void *ins[] = {qkv, kv_cache, block_table, context_lens};
+    const size_t in_b[] = {qkv_b, cache_b, (size_t)num_reqs * max_blocks * 4, (size_t)num_reqs * 4};
+    for (int i = 0; i < 4; ++i)
+        if (overlap(ins[i], in_b[i], out, out_b)) return "an input overlaps out";
+    *code = QKVF_OK;
+    return nullptr;
+}
+
+int attn2_splits_for(int num_reqs, int nkv, int max_blocks, int sms)
+{
+    int s = 1;
+    while (s < kA2MaxSplits && num_reqs * nkv * s * 2 <= sms && max_blocks >= 4 * s * 2) s *= 2;
+    return s;
+}
+
+bool prepare_attn2_kernel()
+{
+    return cudaFuncSetAttribute((const void *)attn2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)a2_layout().total) == cudaSuccess &&
+           cudaFuncSetAttribute((const void *)attn2_kernel,
+                                cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+}
+
+int launch_attn2(const uint16_t *qkv, const uint16_t *kv_cache, int64_t num_pages,
+                 const int32_t *block_table, int max_blocks, const int32_t *context_lens, int num_reqs,
+                 int N, int num_kv_heads, int window, float scale, float eps, uint16_t *out, int splits,
+                 void *stream)
+{
+    CUtensorMap m;
+    int rc = encode_kv_map(kv_cache, num_pages, num_kv_heads, &m);
+    if (rc != QKVF_OK) return rc;
+    Attn2Params prm;
+    prm.qkv = qkv;
+    prm.block_table = block_table;
+    prm.context_lens = context_lens;
+    prm.out = out;
+    prm.num_pages = num_pages;
+    prm.wait_limit_ns = g_wait_limit_ns;
+    prm.max_blocks = max_blocks;
+    prm.N = N;
+    prm.nkv = num_kv_heads;
+    prm.window = window;
+    prm.splits = splits;
+    prm.scale_log2 = scale * 1.4426950408889634f;
+    prm.eps = eps;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)splits, (unsigned)num_kv_heads, (unsigned)num_reqs);
+    cfg.blockDim = dim3(kA2Threads, 1, 1);
+    cfg.dynamicSmemBytes = a2_layout().total;
+    cfg.stream = (cudaStream_t)stream;
+    cudaLaunchAttribute attrs[2];
+    int na = 0;
+    if (splits > 1) {
+        attrs[na].id = cudaLaunchAttributeClusterDimension;
+        attrs[na].val.clusterDim.x = (unsigned)splits;
+        attrs[na].val.clusterDim.y = 1;
+        attrs[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[na].val.programmaticStreamSerializationAllowed = g_pdl ? 1 : 0;
+    ++na;
+    cfg.attrs = attrs;
+    cfg.numAttrs = (unsigned)na;
+    if (cudaLaunchKernelEx(&cfg, attn2_kernel, m, prm) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return QKVF_ERR_CUDA;
+    }
+    return QKVF_OK;
+}
+
+}  // namespace qkvf
+
+extern "C" {
+
+int attn2(const uint16_t *qkv, const uint16_t *kv_cache, int64_t num_pages,
+          const int32_t *block_table, int max_blocks, const int32_t *context_lens, int num_reqs,
+          int N, int num_kv_heads, int window, float scale, float eps, uint16_t *out, void *stream)
+{
+    int code;
+    if (qkvf::check_attn2_args(qkv, kv_cache, num_pages, block_table, max_blocks, context_lens,
+                               num_reqs, N, num_kv_heads, window, scale, eps, out, &code))
+        return code;
+    if (num_reqs == 0) return QKVF_OK;
+    qkvf::DeviceState *d;
+    const int rc = qkvf::probe_device(&d);
+    if (rc != QKVF_OK) return rc;
+    const int splits = qkvf::attn2_splits_for(num_reqs, num_kv_heads, max_blocks, d->sms);
+    return qkvf::launch_attn2(qkv, kv_cache, num_pages, block_table, max_blocks, context_lens,
+                              num_reqs, N, num_kv_heads, window, scale, eps, out, splits, stream);
+}
+
+int attn2_launch_splits(const uint16_t *qkv, const uint16_t *kv_cache, int64_t num_pages,
+                        const int32_t *block_table, int max_blocks, const int32_t *context_lens,
+                        int num_reqs, int N, int num_kv_heads, int window, float scale, float eps,
+                        uint16_t *out, int splits, void *stream)
+{
+    int code;
+    if (qkvf::check_attn2_args(qkv, kv_cache, num_pages, block_table, max_blocks, context_lens,
+                               num_reqs, N, num_kv_heads, window, scale, eps, out, &code))
+        return code;
+    if (splits != 1 && splits != 2 && splits != 4 && splits != 8 && splits != 16) return QKVF_ERR_VARIANT;
+    if (num_reqs == 0) return QKVF_OK;
+    qkvf::DeviceState *d;
+    const int rc = qkvf::probe_device(&d);
+    if (rc != QKVF_OK) return rc;
+    return qkvf::launch_attn2(qkv, kv_cache, num_pages, block_table, max_blocks, context_lens,
+                              num_reqs, N, num_kv_heads, window, scale, eps, out, splits, stream);
+}
+
+int attn2_splits(int num_reqs, int num_kv_heads, int max_blocks)
+{
+    if (num_reqs < 1 || num_kv_heads < 1 || max_blocks < 1) return 0;
+    qkvf::DeviceState *d;
+    if (qkvf::probe_device(&d) != QKVF_OK) return 0;
+    return qkvf::attn2_splits_for(num_reqs, num_kv_heads, max_blocks, d->sms);
+}
+
+}  // extern "C"

@@ -399,6 +399,13 @@ __device__ __forceinline__ float2 ld_cluster_f2(uint32_t addr)
     return v;
 }
 
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr)
+{
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(__nv_bfloat16 lo, __nv_bfloat16 hi)
 {
     return (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
@@ -818,6 +825,7 @@ constexpr int kDefaultL2Prefetch = 8;  // W stages prefetched into L2 before the
 constexpr bool kDefaultTC = false;     // consumer: tcgen05 (true) or mma.sync
 
 bool prepare_epi_kernel();
+bool prepare_attn2_kernel();
 
 int probe_device(DeviceState **out)
 {
@@ -855,7 +863,7 @@ int probe_device(DeviceState **out)
                                      cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
                 return QKVF_ERR_CUDA;
         }
-        if (!prepare_epi_kernel()) return QKVF_ERR_CUDA;
+        if (!prepare_epi_kernel() || !prepare_attn2_kernel()) return QKVF_ERR_CUDA;
         d.prepared = true;
     }
     *out = &d;
@@ -1040,6 +1048,7 @@ int launch_front(const uint16_t *x, const uint16_t *W, const int64_t *positions,
 
 #include "qknorm_rope_kv_insert.cuh"
 #include "layer_front.cuh"
+#include "attn2.cuh"
 
 using namespace qkvf;
 

@@ -35,6 +35,7 @@ CONSUMER_DEFAULT, CONSUMER_MMA_SYNC, CONSUMER_TCGEN05 = 0, 1, 2
 STATUS_BAD_SLOT = 1
 STATUS_BAD_POSITION = 2
 STATUS_WAIT_TIMEOUT = 4
+STATUS_BAD_REQUEST = 8
 
 HEADER = os.path.join(_build.ROOT, "include", "qkvfront.h")
 
@@ -97,6 +98,13 @@ def load() -> ctypes.CDLL:
         lib.qknorm_rope_kv_insert_unsupported.restype = ctypes.c_char_p
         lib.layer_front.argtypes = [vp, i32, vp, vp, vp, vp, i32, ctypes.c_float, vp]
         lib.layer_front.restype = i32
+        a2 = [vp, vp, i64, vp, i32, vp, i32, i32, i32, i32, ctypes.c_float, ctypes.c_float, vp]
+        lib.attn2.argtypes = a2 + [vp]
+        lib.attn2.restype = i32
+        lib.attn2_launch_splits.argtypes = a2 + [i32, vp]
+        lib.attn2_launch_splits.restype = i32
+        lib.attn2_splits.argtypes = [i32, i32, i32]
+        lib.attn2_splits.restype = i32
         lib.qkv_front_set_pdl.argtypes = [i32]
         lib.qkv_front_set_pdl.restype = i32
         _lib = lib
@@ -107,8 +115,8 @@ def header_functions() -> list[str]:
     """Names of the functions include/qkvfront.h declares."""
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b((?:qkv_front|qknorm_rope_kv_insert|layer_front)\w*)\s*\(",
-                                 text)))
+    return sorted(set(re.findall(
+        r"\b((?:qkv_front|qknorm_rope_kv_insert|layer_front|attn2)\w*)\s*\(", text)))
 
 
 def strerror(code: int) -> str:
@@ -384,6 +392,43 @@ def layer_front(x, stream_out, out, aux=None, weight=None, eps: float = 1e-6, st
                                   stream_out.data_ptr(), None if aux is None else aux.data_ptr(),
                                   out.data_ptr(), rows, float(eps), _stream(stream)))
     return out
+
+
+def attn2(qkv, kv_cache, block_table, context_lens, out=None, window: int = 0,
+          scale: float = 0.125, eps: float = 1e-6, splits=None, stream=None):
+    """Verify-step paged attention with o-norm and sigmoid gate (the o_proj
+    input).  qkv bf16 [8 R, N]; block_table int32 [R, max_blocks];
+    context_lens int32 [R]; returns out bf16 [8 R, 512 num_kv_heads]."""
+    R = context_lens.shape[0]
+    nkv = kv_cache.shape[1]
+    N = qkv.shape[1]
+    cols = Q_PER_KV * nkv * HEAD_DIM
+    if out is None:
+        out = torch.empty(8 * R, cols, dtype=torch.bfloat16, device=qkv.device)
+    for t, dt, shape, name in ((qkv, torch.bfloat16, (8 * R, N), "qkv"),
+                               (out, torch.bfloat16, (8 * R, cols), "out"),
+                               (context_lens, torch.int32, (R,), "context_lens")):
+        if (not t.is_cuda or t.dtype != dt or tuple(t.shape) != shape or not t.is_contiguous()
+                or t.device != qkv.device):
+            raise ValueError(f"{name} must be a contiguous {dt} CUDA tensor {shape}")
+    if (block_table.dtype != torch.int32 or block_table.dim() != 2 or block_table.shape[0] != R
+            or not block_table.is_contiguous() or not block_table.is_cuda):
+        raise ValueError("block_table must be a contiguous int32 CUDA tensor [R, max_blocks]")
+    if not kv_cache_layout_ok(kv_cache) or not supports_shape(N, nkv):
+        raise ValueError("cache must be bf16 [pages, nkv, 16, 128] and N = 1152 nkv")
+    args = (qkv.data_ptr(), kv_cache.data_ptr(), kv_cache.shape[0], block_table.data_ptr(),
+            block_table.shape[1], context_lens.data_ptr(), R, N, nkv, int(window), float(scale),
+            float(eps), out.data_ptr())
+    with torch.cuda.device(qkv.device):
+        if splits is None:
+            _check(load().attn2(*args, _stream(stream)))
+        else:
+            _check(load().attn2_launch_splits(*args, int(splits), _stream(stream)))
+    return out
+
+
+def attn2_splits(num_reqs: int, num_kv_heads: int, max_blocks: int) -> int:
+    return int(load().attn2_splits(num_reqs, num_kv_heads, max_blocks))
 
 
 def selftest_wait(timeout_ns: int, stream=None) -> None:

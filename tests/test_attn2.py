@@ -1,0 +1,134 @@
+"""attn2 (verify-step paged attention + o-norm + sigmoid gate) through the C
+ABI against the oracle: every workload, every cluster split, windows, bad
+requests, and the decode layer's order — the front fills the cache and its
+q / gate columns, attn2 reads them."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from kv_insert_gb300 import qkv_front as qf
+from kv_insert_gb300 import workloads as wl
+
+from _parity import assert_values
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    qf.status()
+
+
+def _dev(inp):
+    return {k: v.to("cuda:0") for k, v in inp.items()}
+
+
+def _oracle(inp, w, window=None, out_bits=None):
+    return oracle.attn2(wl.bits(inp["qkv"]), wl.bits(inp["kv_cache"]), inp["block_table"].numpy(),
+                        inp["context_lens"].numpy(), w.num_kv_heads,
+                        w.window if window is None else window, out_bits=out_bits)
+
+
+@pytest.mark.parametrize("name", list(wl.ATTN_WORKLOADS))
+def test_attn2_workloads_match_oracle(name):
+    w = wl.ATTN_WORKLOADS[name]
+    inp = wl.make_attn_inputs(w)
+    g = _dev(inp)
+    out = qf.attn2(g["qkv"], g["kv_cache"], g["block_table"], g["context_lens"], window=w.window)
+    torch.cuda.synchronize()
+    assert qf.status() == 0
+    ref, err = _oracle(inp, w)
+    assert err == 0
+    assert_values(wl.bits(out.cpu()), ref, what=f"attn2 {name}")
+
+
+@pytest.mark.parametrize("splits", [1, 2, 4, 8, 16])
+def test_attn2_every_split(splits):
+    w = wl.ATTN_WORKLOADS["attn_r2_window_nkv8"]
+    inp = wl.make_attn_inputs(w)
+    g = _dev(inp)
+    outs = []
+    for _ in range(2):
+        outs.append(qf.attn2(g["qkv"], g["kv_cache"], g["block_table"], g["context_lens"],
+                             window=w.window, splits=splits).clone())
+    torch.cuda.synchronize()
+    assert qf.status() == 0
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    ref, _ = _oracle(inp, w)
+    assert_values(wl.bits(outs[0].cpu()), ref, what=f"attn2 splits={splits}")
+
+
+@pytest.mark.parametrize("window", [1, 7, 16, 33])
+def test_attn2_windows(window):
+    w = wl.AttnWorkload(f"w{window}", R=3, num_kv_heads=2, context=(8, 45, 130), num_pages=64,
+                        seed=6000 + window, window=window)
+    inp = wl.make_attn_inputs(w)
+    g = _dev(inp)
+    out = qf.attn2(g["qkv"], g["kv_cache"], g["block_table"], g["context_lens"], window=window)
+    torch.cuda.synchronize()
+    ref, _ = _oracle(inp, w)
+    assert_values(wl.bits(out.cpu()), ref, what=f"attn2 window={window}")
+
+
+@pytest.mark.parametrize("L", [8, 9, 15, 16, 17, 31, 33, 255, 257])
+def test_attn2_lengths_around_page_edges(L):
+    w = wl.AttnWorkload(f"l{L}", R=1, num_kv_heads=1, context=(L,), num_pages=32, seed=6100 + L)
+    inp = wl.make_attn_inputs(w)
+    g = _dev(inp)
+    out = qf.attn2(g["qkv"], g["kv_cache"], g["block_table"], g["context_lens"])
+    torch.cuda.synchronize()
+    ref, _ = _oracle(inp, w)
+    assert_values(wl.bits(out.cpu()), ref, what=f"attn2 L={L}")
+
+
+def test_attn2_bad_requests_skipped_and_flagged():
+    w = wl.AttnWorkload("bad", R=3, num_kv_heads=1, context=(40, 40, 40), num_pages=16, seed=6200)
+    inp = wl.make_attn_inputs(w)
+    inp["context_lens"][0] = 5                      # fewer than 8 tokens
+    inp["block_table"][1, 1] = 999                  # a page outside the cache
+    g = _dev(inp)
+    out = torch.full((24, 512), 7.0, dtype=torch.bfloat16, device="cuda:0")
+    qf.attn2(g["qkv"], g["kv_cache"], g["block_table"], g["context_lens"], out=out)
+    torch.cuda.synchronize()
+    assert qf.status() == qf.STATUS_BAD_REQUEST
+    got = wl.bits(out.cpu())
+    assert np.all(got[:16] == wl.bits(torch.tensor([7.0]).to(torch.bfloat16))[0])
+    ref, err = _oracle(inp, w)
+    assert err == oracle.ERR_ATTN_REQUEST
+    assert_values(got[16:], ref[16:], what="the good request")
+
+
+def test_decode_layer_front_then_attn2():
+    """The order of a decode layer: the front writes q / gate and inserts K / V
+    for the 8 verify tokens, then attn2 reads them (PDL-linked on one stream),
+    against the oracle front followed by the oracle attn2."""
+    nkv, L = 2, 300
+    w = wl.Workload("layer", M=8, num_kv_heads=nkv, max_pos=4096, num_pages=64, seed=6300)
+    inp = wl.make_inputs(w)
+    table = torch.randperm(w.num_pages, generator=torch.Generator().manual_seed(1))[:(L + 15) // 16]
+    table = table.to(torch.int32)[None, :]
+    slots = torch.tensor([int(table[0, j // 16]) * 16 + j % 16 for j in range(L - 8, L)])
+    inp["slots"] = slots
+    inp["positions"] = torch.arange(L - 8, L)
+    lens = torch.tensor([L], dtype=torch.int32)
+    g = _dev(inp)
+    gt, gl = table.to("cuda:0"), lens.to("cuda:0")
+    qkv = qf.qkv_front(g["x"], g["W"], g["positions"], g["slots"], g["cos_sin"], g["kv_cache"])
+    o = qf.attn2(qkv, g["kv_cache"], gt, gl)
+    torch.cuda.synchronize()
+    assert qf.status() == 0
+    cache_ref = wl.bits(inp["kv_cache"]).copy()
+    out_ref, err = oracle.qkv_front(wl.bits(inp["x"]), wl.bits(inp["W"]), inp["positions"].numpy(),
+                                    slots.numpy(), inp["cos_sin"].numpy(), cache_ref, nkv)
+    assert err == 0
+    # attn2 against the oracle on the GPU's own front output and cache (isolates attn2)
+    o_ref, err = oracle.attn2(wl.bits(qkv.cpu()), wl.bits(g["kv_cache"].cpu()), table.numpy(),
+                              lens.numpy(), nkv)
+    assert err == 0
+    assert_values(wl.bits(o.cpu()), o_ref, what="attn2 after the front")
+    # and the whole layer against the all-oracle chain
+    o_chain, _ = oracle.attn2(out_ref, cache_ref, table.numpy(), lens.numpy(), nkv)
+    assert_values(wl.bits(o.cpu()), o_chain, what="front + attn2 vs the oracle chain")

@@ -195,3 +195,25 @@ def test_layer_front_refusals(lib):
 def test_set_pdl_refusals(lib):
     assert lib.qkv_front_set_pdl(2) == 9 and lib.qkv_front_set_pdl(-1) == 9
     assert lib.qkv_front_set_pdl(0) == 0 and lib.qkv_front_set_pdl(1) == 0
+
+
+def test_attn2_refusals(lib):
+    f = lib.attn2
+    ok = dict(q=X, c=CACHE, pages=64, bt=POS, mb=8, cl=SL, R=2, N=2304, nkv=2, win=0, sc=0.125,
+              eps=1e-6, out=OUT)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["q"], a["c"], a["pages"], a["bt"], a["mb"], a["cl"], a["R"], a["N"], a["nkv"],
+                 a["win"], a["sc"], a["eps"], a["out"], None)
+    assert call(R=-1) == 1 and call(R=65536) == 1
+    assert call(N=1152) == 2 and call(nkv=0) == 2
+    assert call(pages=0) == 7 and call(mb=0) == 7
+    assert call(win=-1) == 9 and call(sc=0.0) == 9 and call(eps=2.0) == 9
+    assert call(q=0) == 3 and call(bt=0) == 3
+    assert call(q=X + 8) == 4 and call(cl=SL + 2) == 4
+    assert call(out=X) == 9                           # out on top of qkv
+    assert call(R=0, q=0) == 0
+    assert call() in (5, 6)
+    assert lib.attn2_launch_splits(X, CACHE, 64, POS, 8, SL, 2, 2304, 2, 0, 0.125, 1e-6, OUT, 3,
+                                   None) == 8
