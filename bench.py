@@ -54,13 +54,14 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--op", choices=("qkv_front", "qknorm_rope_kv_insert", "chain"),
+    ap.add_argument("--op", choices=("qkv_front", "qknorm_rope_kv_insert", "chain", "attn2"),
                     default="qkv_front",
                     help="qkv_front: the fused decode front (the headline); qknorm_rope_kv_insert: "
                          "the standalone epilogue on a prefill chunk; chain: layer_front then "
-                         "qkv_front, PDL-linked, against each alone")
+                         "qkv_front, PDL-linked, against each alone; attn2: verify-step paged "
+                         "attention reading the cache")
     ap.add_argument("--workload", default=None,
-                    choices=sorted(wl.WORKLOADS) + sorted(wl.EPI_WORKLOADS))
+                    choices=sorted(wl.WORKLOADS) + sorted(wl.EPI_WORKLOADS) + sorted(wl.ATTN_WORKLOADS))
     ap.add_argument("--graph-calls", type=int, default=96,
                     help="calls per captured CUDA graph (a multiple of the W copies is used)")
     ap.add_argument("--front-stages", type=int, default=0,
@@ -71,9 +72,11 @@ def parse_args(argv=None):
     ap.add_argument("--ref-seconds", type=float, default=90.0,
                     help="target duration of the whole --impl reference run")
     a = ap.parse_args(argv)
+    defaults = {"qknorm_rope_kv_insert": wl.EPI_BENCH_WORKLOAD, "attn2": wl.ATTN_BENCH_WORKLOAD}
+    tables = {"qknorm_rope_kv_insert": wl.EPI_WORKLOADS, "attn2": wl.ATTN_WORKLOADS}
     if a.workload is None:
-        a.workload = wl.EPI_BENCH_WORKLOAD if a.op == "qknorm_rope_kv_insert" else wl.BENCH_WORKLOAD
-    table = wl.EPI_WORKLOADS if a.op == "qknorm_rope_kv_insert" else wl.WORKLOADS
+        a.workload = defaults.get(a.op, wl.BENCH_WORKLOAD)
+    table = tables.get(a.op, wl.WORKLOADS)
     if a.workload not in table:
         ap.error(f"workload {a.workload} is not a {a.op} workload")
     if a.op != "qkv_front" and a.impl == "reference":
@@ -522,6 +525,92 @@ def run_epilogue(args, w):
             "gpu_launches": args.steps, "clocks": clocks, "e2e": None}
 
 
+ATTN_METRIC = "attn2 achieved HBM GB/s (verify-step paged attention), 1 GPU"
+
+
+def run_attn2(args, w):
+    """attn2 over cache copies rotated past L2, CUDA-graph replays, events."""
+    from kv_insert_gb300 import qkv_front as qf
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU (the product path has no CPU fallback)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_init("nccl")
+    qf.load()
+    inp = wl.make_attn_inputs(w)
+    g = {k: v.to(dev) for k, v in inp.items()}
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    c_bytes = g["kv_cache"].numel() * 2
+    copies = max(2, math.ceil(3 * l2 / c_bytes))
+    caches = [g["kv_cache"]] + [g["kv_cache"].clone() for _ in range(copies - 1)]
+    out = torch.empty(8 * w.R, 512 * w.num_kv_heads, dtype=torch.bfloat16, device=dev)
+    torch.cuda.synchronize(dev)
+    stream = torch.cuda.Stream(device=dev)
+    per_graph = max(copies, (args.graph_calls // copies) * copies)
+    splits = qf.attn2_splits(w.R, w.num_kv_heads, w.max_blocks())
+
+    def call(i):
+        qf.attn2(g["qkv"], caches[i % copies], g["block_table"], g["context_lens"], out=out,
+                 window=w.window)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            call(i)
+    stream.synchronize()
+    full, rem = divmod(args.steps, per_graph)
+    graphs = []
+    for n in ([per_graph] if full else []) + ([rem] if rem else []):
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(n):
+                call(i)
+        graphs.append(graph)
+    with torch.cuda.stream(stream):
+        for gr in graphs:
+            gr.replay()
+    stream.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(full):
+            graphs[0].replay()
+        if rem:
+            graphs[-1].replay()
+        end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clocks = sampler.stop()
+    el_max = max_over_ranks(start.elapsed_time(end) / 1e3, dev)
+    if qf.status():
+        raise RuntimeError("device status raised in the timed region")
+    res = aggregate(w.roofline_bytes(), args.steps, world, el_max)
+    if rank != 0:
+        return None
+    peak, peak_kind = hbm_peak()
+    achieved = w.roofline_bytes() / (el_max / args.steps) / 1e9
+    return {"metric": ATTN_METRIC, "value": res["value"], "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
+            "us_per_call": res["us_per_call"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": dict(w.describe(), **{
+                "splits": splits,
+                "l2": f"inputs larger than L2: cache rotated over {copies} copies of "
+                      f"{c_bytes / 1e6:.1f} MB (L2 {l2 / 1e6:.1f} MB)",
+                "graph_calls": per_graph, "parallelism": f"replicas x{world}"}),
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_kind": peak_kind,
+                         "traffic": recorded_traffic("attn2", w.name),
+                         "bytes_per_launch": w.roofline_bytes()},
+            "gpu_launches": args.steps, "clocks": clocks, "e2e": None}
+
+
 CHAIN_METRIC = "µs per first-layer front step: layer_front then qkv_front, PDL-linked, 1 GPU"
 
 
@@ -630,6 +719,8 @@ def main(argv=None):
     args = parse_args(argv)
     if args.op == "chain":
         line = run_chain(args, wl.WORKLOADS[args.workload])
+    elif args.op == "attn2":
+        line = run_attn2(args, wl.ATTN_WORKLOADS[args.workload])
     elif args.op == "qknorm_rope_kv_insert":
         line = run_epilogue(args, wl.EPI_WORKLOADS[args.workload])
     else:
