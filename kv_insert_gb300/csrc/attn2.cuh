@@ -29,7 +29,8 @@ namespace qkvf {
 
 constexpr int kA2ComputeWarps = 4;
 constexpr int kA2Threads = 32 * (kA2ComputeWarps + 1);   // warp 4 produces
-constexpr int kA2Stages = 8;                              // pages in flight per CTA
+constexpr int kA2Stages = 16;                             // pages in flight per CTA
+constexpr int kA2Block = 4;                               // pages per softmax step (64 keys)
 constexpr uint32_t kA2PageBytes = 4096;                   // K box + V box
 constexpr int kA2OStride = 68;                            // floats per row of the O partial
 constexpr int kA2MaxSplits = 16;
@@ -219,41 +220,56 @@ __global__ void __launch_bounds__(kA2Threads, 1)
         const uint32_t v_hi = (uint32_t)(lane >> 4);
         const uint32_t sw = (uint32_t)(lane & 7);
 
-        for (int k = 0; k < npages; ++k) {
-            const int s = k % kA2Stages;
-            const uint32_t ph = (uint32_t)((k / kA2Stages) & 1);
-            const bool landed = mbar_try_wait(full0 + 8 * s, ph) ||
-                                bounded_wait(full0 + 8 * s, ph, s_flags, p.wait_limit_ns, true);
+        // blocks of up to kA2Block pages (16 kA2Block keys): one softmax
+        // reduction and one rescale of O per block, independent mma chains
+        for (int k0 = 0; k0 < npages; k0 += kA2Block) {
+            const int nb = npages - k0 < kA2Block ? npages - k0 : kA2Block;   // same for every lane
+            bool landed = true;
+            for (int b = 0; b < nb; ++b) {
+                const int k = k0 + b, s = k % kA2Stages;
+                const uint32_t ph = (uint32_t)((k / kA2Stages) & 1);
+                landed = landed && (mbar_try_wait(full0 + 8 * s, ph) ||
+                                    bounded_wait(full0 + 8 * s, ph, s_flags, p.wait_limit_ns, true));
+            }
             if (__all_sync(0xffffffffu, landed)) {
-                const uint32_t kbox = sRing + (uint32_t)s * kA2PageBytes, vbox = kbox + 2048;
-                const int key0 = (first_mine + k * S) * kPageSlots;
-                float sc[2][4];
+                float sc[2 * kA2Block][4];
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
+                for (int nt = 0; nt < 2 * kA2Block; ++nt)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) sc[nt][e] = 0.f;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(kbox + k_key * 128u + ((((uint32_t)(2 * kk) + k_hi) ^ sw) << 4), b0, b1, b2, b3);
-                    mma_bf16_16816(sc[0], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
-                    mma_bf16_16816(sc[1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
+#pragma unroll
+                    for (int b = 0; b < kA2Block; ++b) {
+                        if (b < nb) {
+                            const uint32_t kbox = sRing + (uint32_t)((k0 + b) % kA2Stages) * kA2PageBytes;
+                            uint32_t b0, b1, b2, b3;
+                            ldsm_x4(kbox + k_key * 128u + ((((uint32_t)(2 * kk) + k_hi) ^ sw) << 4), b0, b1, b2, b3);
+                            mma_bf16_16816(sc[2 * b], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
+                            mma_bf16_16816(sc[2 * b + 1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
+                        }
+                    }
                 }
-                // scale into base 2 and mask: element e of tile nt is key key0 + 8 nt + 2 t + (e & 1),
-                // row a for e < 2, row b otherwise
+                // scale into base 2 and mask: element e of tile nt = 2 b + h is key
+                // key0(b) + 8 h + 2 t + (e & 1), of row a for e < 2, else row b
                 float mx_a = -INFINITY, mx_b = -INFINITY;
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
+                for (int b = 0; b < kA2Block; ++b) {
+                    const int key0 = (first_mine + (k0 + b) * S) * kPageSlots;
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int key = key0 + 8 * nt + 2 * t + (e & 1);
-                        const bool rb = e >= 2;
-                        const bool ok = rb ? (key >= lo_b && key <= pos_b) : (key >= lo_a && key <= pos_a);
-                        const float v = ok ? sc[nt][e] * p.scale_log2 : -INFINITY;
-                        sc[nt][e] = v;
-                        if (rb) mx_b = fmaxf(mx_b, v);
-                        else mx_a = fmaxf(mx_a, v);
-                    }
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int key = key0 + 8 * h + 2 * t + (e & 1);
+                            const bool rb = e >= 2;
+                            const bool ok = b < nb &&
+                                            (rb ? (key >= lo_b && key <= pos_b) : (key >= lo_a && key <= pos_a));
+                            const float v = ok ? sc[2 * b + h][e] * p.scale_log2 : -INFINITY;
+                            sc[2 * b + h][e] = v;
+                            if (rb) mx_b = fmaxf(mx_b, v);
+                            else mx_a = fmaxf(mx_a, v);
+                        }
+                }
 #pragma unroll
                 for (int off = 1; off <= 2; off <<= 1) {
                     mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, off));
@@ -263,14 +279,13 @@ __global__ void __launch_bounds__(kA2Threads, 1)
                 const float base_a = mn_a == -INFINITY ? 0.f : mn_a;
                 const float base_b = mn_b == -INFINITY ? 0.f : mn_b;
                 const float al_a = exp2f(m_a - base_a), al_b = exp2f(m_b - base_b);
-                float pv[2][4];
                 float sum_a = 0.f, sum_b = 0.f;
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
+                for (int nt = 0; nt < 2 * kA2Block; ++nt)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const float pe = exp2f(sc[nt][e] - (e >= 2 ? base_b : base_a));
-                        pv[nt][e] = pe;
+                        sc[nt][e] = pe;
                         if (e >= 2) sum_b += pe;
                         else sum_a += pe;
                     }
@@ -285,19 +300,28 @@ __global__ void __launch_bounds__(kA2Threads, 1)
                     o[nd][2] *= al_b;
                     o[nd][3] *= al_b;
                 }
-                // P (rows a / b x 16 keys) as the A fragment of PV
-                const uint32_t pa0 = pack_f2bf(pv[0][0], pv[0][1]), pa1 = pack_f2bf(pv[0][2], pv[0][3]);
-                const uint32_t pa2 = pack_f2bf(pv[1][0], pv[1][1]), pa3 = pack_f2bf(pv[1][2], pv[1][3]);
 #pragma unroll
-                for (int q2 = 0; q2 < 4; ++q2) {   // dims 16 q2 .. 16 q2 + 15
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4_trans(vbox + v_key * 128u + ((((uint32_t)(2 * q2) + v_hi) ^ sw) << 4), b0, b1, b2, b3);
-                    mma_bf16_16816(o[2 * q2], pa0, pa1, pa2, pa3, b0, b1);
-                    mma_bf16_16816(o[2 * q2 + 1], pa0, pa1, pa2, pa3, b2, b3);
+                for (int b = 0; b < kA2Block; ++b) {
+                    if (b < nb) {
+                        const uint32_t vbox = sRing + (uint32_t)((k0 + b) % kA2Stages) * kA2PageBytes + 2048;
+                        // P (rows a / b x the page's 16 keys) as the A fragment of PV
+                        const uint32_t pa0 = pack_f2bf(sc[2 * b][0], sc[2 * b][1]);
+                        const uint32_t pa1 = pack_f2bf(sc[2 * b][2], sc[2 * b][3]);
+                        const uint32_t pa2 = pack_f2bf(sc[2 * b + 1][0], sc[2 * b + 1][1]);
+                        const uint32_t pa3 = pack_f2bf(sc[2 * b + 1][2], sc[2 * b + 1][3]);
+#pragma unroll
+                        for (int q2 = 0; q2 < 4; ++q2) {   // dims 16 q2 .. 16 q2 + 15
+                            uint32_t b0, b1, b2, b3;
+                            ldsm_x4_trans(vbox + v_key * 128u + ((((uint32_t)(2 * q2) + v_hi) ^ sw) << 4), b0, b1, b2, b3);
+                            mma_bf16_16816(o[2 * q2], pa0, pa1, pa2, pa3, b0, b1);
+                            mma_bf16_16816(o[2 * q2 + 1], pa0, pa1, pa2, pa3, b2, b3);
+                        }
+                    }
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(empty0 + 8 * s);
+            if (lane == 0)
+                for (int b = 0; b < nb; ++b) mbar_arrive(empty0 + 8 * ((k0 + b) % kA2Stages));
         }
         // whole-row sums across the four threads of a row
 #pragma unroll
