@@ -14,23 +14,30 @@
 // head h of its row; out = bf16(o / sqrt(mean(o^2) + eps) * sigmoid(gate))
 // with o = softmax(scale q K^T) V.
 //
-// Design: a CTA per (request r, KV head g, split z).  Its 64 query rows
-// (8 tokens x 8 heads, row 8 i + j) stay in registers as mma.sync A
-// fragments; a producer warp streams the CTA's pages (pages p0 + z,
-// p0 + z + S, ...) as two 16 x 64 TMA boxes each (K and V halves, 128-byte
-// swizzle) into a ring; four compute warps (16 rows each) run QK^T, the online
-// softmax (base 2) and PV with mma.sync, P going from the S accumulators
-// straight into the A fragments.  The S CTAs of a (request, KV head) form a
-// cluster and merge their (max, sum, O) through distributed shared memory in
-// rank order — no global workspace, deterministic for a launch shape — then
-// each rank finishes 64 / S rows: o-norm, gate, BF16 store.
+// Design: a CTA per (request r, KV head g, split z).  A producer warp streams
+// the CTA's pages (p0 + z, p0 + z + S, ...) as two 16 x 64 TMA boxes each (K
+// and V halves, 128-byte swizzle) into a ring.  Groups of four compute warps
+// (16 of the 64 query rows each — 8 tokens x 8 heads, row 8 i + j — held in
+// registers as mma.sync A fragments) take blocks of 4 pages in turn and run
+// QK^T, the online softmax (base 2; masks only near the causal / window
+// edges) and PV with mma.sync, P going from the S accumulators straight into
+// the A fragments.  Each group keeps its own (max, sum, O); the S CTAs of a
+// (request, KV head) form a cluster and all S x G partials are merged through
+// distributed shared memory in a fixed order — no global workspace,
+// deterministic for a launch shape — then each rank finishes 64 / S rows:
+// o-norm, gate, BF16 store.
+
+#ifndef A2_GROUPS
+#define A2_GROUPS 3
+#endif
 
 namespace qkvf {
 
-constexpr int kA2ComputeWarps = 4;
-constexpr int kA2Threads = 32 * (kA2ComputeWarps + 1);   // warp 4 produces
-constexpr int kA2Stages = 16;                             // pages in flight per CTA
+constexpr int kA2Groups = A2_GROUPS;                      // groups of 4 compute warps
+constexpr int kA2ComputeWarps = 4 * kA2Groups;
+constexpr int kA2Threads = 32 * (kA2ComputeWarps + 1);   // the last warp produces
 constexpr int kA2Block = 4;                               // pages per softmax step (64 keys)
+constexpr int kA2Stages = kA2Groups * kA2Block;           // ring slot k % stages always serves group (k / block) % groups
 constexpr uint32_t kA2PageBytes = 4096;                   // K box + V box
 constexpr int kA2OStride = 68;                            // floats per row of the O partial
 constexpr int kA2MaxSplits = 16;
@@ -53,11 +60,11 @@ __host__ __device__ inline A2Layout a2_layout()
     L.empty = off;
     off += kA2Stages * 8;
     L.o = off;
-    off += 64 * kA2OStride * 4;
+    off += kA2Groups * 64 * kA2OStride * 4;
     L.m = off;
-    off += 64 * 4;
+    off += kA2Groups * 64 * 4;
     L.l = off;
-    off += 64 * 4;
+    off += kA2Groups * 64 * 4;
     L.flags = off;
     off += 16;
     L.total = off + 1024;   // alignment slack
@@ -98,6 +105,12 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t &r0, uint3
                  : "r"(addr));
 }
 
+// named barrier 2 over the compute warps only
+__device__ __forceinline__ void a2_compute_bar_sync()
+{
+    asm volatile("bar.sync 2, %0;" ::"n"(32 * kA2ComputeWarps) : "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_f2bf(float lo, float hi)
 {
     return pack_bf16x2(__float2bfloat16_rn(lo), __float2bfloat16_rn(hi));
@@ -123,7 +136,7 @@ __global__ void __launch_bounds__(kA2Threads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < kA2Stages; ++s) {
             mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, kA2ComputeWarps);
+            mbar_init(empty0 + 8 * s, 4);   // the 4 warps of the group that owns the slot
         }
         s_flags[0] = 0;
         fence_barrier_init();
@@ -182,31 +195,34 @@ __global__ void __launch_bounds__(kA2Threads, 1)
         }
         __syncwarp();
     } else {
-        // ---- compute ------------------------------------------------------
-        const int tid = threadIdx.x;   // 0..127
+        // ---- compute: group grp = warp / 4 takes blocks grp, grp + G, ... ----
+        const int tid = threadIdx.x;
+        const int grp = warp >> 2, wig = warp & 3;   // group, warp in group (rows 16 wig ..)
         if (req_ok) {
             // Q tile [64 rows][64 dims], row 8 i + j = token i, head 8 g + j;
             // 128-byte rows with the chunk XORed by row % 8 (as TMA would)
-            for (int c = tid; c < 512; c += 128) {
+            for (int c = tid; c < 512; c += 32 * kA2ComputeWarps) {
                 const int row = c >> 3, cc = c & 7;
                 const uint4 v = *reinterpret_cast<const uint4 *>(
                     p.qkv + ((size_t)r * 8 + (row >> 3)) * p.N + (size_t)(8 * g + (row & 7)) * kHeadDim + 8 * cc);
                 *reinterpret_cast<uint4 *>(smem + LY.q + row * 128 + ((cc ^ (row & 7)) << 4)) = v;
             }
         }
-        consumer_bar_sync();
+        a2_compute_bar_sync();
         const int gq = lane >> 2, t = lane & 3;
         uint32_t qa[4][4];
-        const uint32_t a_row = (uint32_t)(warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8);
+        const uint32_t a_row = (uint32_t)(wig * 16 + (lane & 7) + ((lane >> 3) & 1) * 8);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
             ldsm_x4(sQ + a_row * 128u + ((((uint32_t)(2 * kk) + (uint32_t)(lane >> 4)) ^ (uint32_t)(lane & 7)) << 4),
                     qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
 
-        // this thread's rows: 16 w + gq (token 2 w) and 16 w + gq + 8 (token 2 w + 1)
-        const int pos_a = L - 8 + 2 * warp, pos_b = pos_a + 1;
+        // this thread's rows: 16 wig + gq (token 2 wig) and 16 wig + gq + 8 (token 2 wig + 1)
+        const int pos_a = L - 8 + 2 * wig, pos_b = pos_a + 1;
         const int lo_a = p.window > 0 ? pos_a - p.window + 1 : 0;
         const int lo_b = p.window > 0 ? pos_b - p.window + 1 : 0;
+        // keys every row sees: [edge_lo, edge_hi]; a page inside needs no mask
+        const int edge_lo = p.window > 0 ? L - p.window : 0, edge_hi = L - 8;
         float o[8][4];
 #pragma unroll
         for (int nd = 0; nd < 8; ++nd)
@@ -222,15 +238,19 @@ __global__ void __launch_bounds__(kA2Threads, 1)
 
         // blocks of up to kA2Block pages (16 kA2Block keys): one softmax
         // reduction and one rescale of O per block, independent mma chains
-        for (int k0 = 0; k0 < npages; k0 += kA2Block) {
+        for (int k0 = grp * kA2Block; k0 < npages; k0 += kA2Groups * kA2Block) {
             const int nb = npages - k0 < kA2Block ? npages - k0 : kA2Block;   // same for every lane
             bool landed = true;
+            bool inside = true;
             for (int b = 0; b < nb; ++b) {
                 const int k = k0 + b, s = k % kA2Stages;
                 const uint32_t ph = (uint32_t)((k / kA2Stages) & 1);
+                const int key0 = (first_mine + k * S) * kPageSlots;
+                inside = inside && key0 >= edge_lo && key0 + kPageSlots - 1 <= edge_hi;
                 landed = landed && (mbar_try_wait(full0 + 8 * s, ph) ||
                                     bounded_wait(full0 + 8 * s, ph, s_flags, p.wait_limit_ns, true));
             }
+            inside = inside && nb == kA2Block;
             if (__all_sync(0xffffffffu, landed)) {
                 float sc[2 * kA2Block][4];
 #pragma unroll
@@ -250,25 +270,37 @@ __global__ void __launch_bounds__(kA2Threads, 1)
                         }
                     }
                 }
-                // scale into base 2 and mask: element e of tile nt = 2 b + h is key
-                // key0(b) + 8 h + 2 t + (e & 1), of row a for e < 2, else row b
+                // scale into base 2 and (near the edges) mask: element e of tile
+                // nt = 2 b + h is key key0(b) + 8 h + 2 t + (e & 1), row a for e < 2
                 float mx_a = -INFINITY, mx_b = -INFINITY;
+                if (inside) {
 #pragma unroll
-                for (int b = 0; b < kA2Block; ++b) {
-                    const int key0 = (first_mine + (k0 + b) * S) * kPageSlots;
-#pragma unroll
-                    for (int h = 0; h < 2; ++h)
+                    for (int nt = 0; nt < 2 * kA2Block; ++nt)
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const int key = key0 + 8 * h + 2 * t + (e & 1);
-                            const bool rb = e >= 2;
-                            const bool ok = b < nb &&
-                                            (rb ? (key >= lo_b && key <= pos_b) : (key >= lo_a && key <= pos_a));
-                            const float v = ok ? sc[2 * b + h][e] * p.scale_log2 : -INFINITY;
-                            sc[2 * b + h][e] = v;
-                            if (rb) mx_b = fmaxf(mx_b, v);
+                            const float v = sc[nt][e] * p.scale_log2;
+                            sc[nt][e] = v;
+                            if (e >= 2) mx_b = fmaxf(mx_b, v);
                             else mx_a = fmaxf(mx_a, v);
                         }
+                } else {
+#pragma unroll
+                    for (int b = 0; b < kA2Block; ++b) {
+                        const int key0 = (first_mine + (k0 + b) * S) * kPageSlots;
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int key = key0 + 8 * h + 2 * t + (e & 1);
+                                const bool rb = e >= 2;
+                                const bool ok = b < nb &&
+                                                (rb ? (key >= lo_b && key <= pos_b) : (key >= lo_a && key <= pos_a));
+                                const float v = ok ? sc[2 * b + h][e] * p.scale_log2 : -INFINITY;
+                                sc[2 * b + h][e] = v;
+                                if (rb) mx_b = fmaxf(mx_b, v);
+                                else mx_a = fmaxf(mx_a, v);
+                            }
+                    }
                 }
 #pragma unroll
                 for (int off = 1; off <= 2; off <<= 1) {
@@ -329,20 +361,21 @@ __global__ void __launch_bounds__(kA2Threads, 1)
             l_a += __shfl_xor_sync(0xffffffffu, l_a, off);
             l_b += __shfl_xor_sync(0xffffffffu, l_b, off);
         }
-        consumer_bar_sync();   // the partials do not alias the ring, but keep one order
-        const int ra = warp * 16 + gq, rb = ra + 8;
+        // this group's partial: rows of the CTA, the group's own slice
+        float *og = o_part + grp * (64 * kA2OStride);
+        const int ra = wig * 16 + gq, rb = ra + 8;
 #pragma unroll
         for (int nd = 0; nd < 8; ++nd) {
-            o_part[ra * kA2OStride + 8 * nd + 2 * t] = o[nd][0];
-            o_part[ra * kA2OStride + 8 * nd + 2 * t + 1] = o[nd][1];
-            o_part[rb * kA2OStride + 8 * nd + 2 * t] = o[nd][2];
-            o_part[rb * kA2OStride + 8 * nd + 2 * t + 1] = o[nd][3];
+            og[ra * kA2OStride + 8 * nd + 2 * t] = o[nd][0];
+            og[ra * kA2OStride + 8 * nd + 2 * t + 1] = o[nd][1];
+            og[rb * kA2OStride + 8 * nd + 2 * t] = o[nd][2];
+            og[rb * kA2OStride + 8 * nd + 2 * t + 1] = o[nd][3];
         }
         if (t == 0) {
-            m_part[ra] = m_a;
-            m_part[rb] = m_b;
-            l_part[ra] = l_a;
-            l_part[rb] = l_b;
+            m_part[grp * 64 + ra] = m_a;
+            m_part[grp * 64 + rb] = m_b;
+            l_part[grp * 64 + ra] = l_a;
+            l_part[grp * 64 + rb] = l_b;
         }
     }
     __syncthreads();
@@ -357,31 +390,36 @@ __global__ void __launch_bounds__(kA2Threads, 1)
         const uint32_t o_addr = smem_u32(o_part), m_addr = smem_u32(m_part), l_addr = smem_u32(l_part);
         for (int i = warp; i < rows; i += kA2ComputeWarps + 1) {
             const int row = (int)z * rows + i;
+            // partials in the fixed order (rank 0, group 0), (0, 1), ..., (S-1, G-1)
             float M = -INFINITY;
-            for (int src = 0; src < S; ++src) {
-                const float mk = S > 1 ? ld_cluster_f32(map_to_rank(m_addr + 4u * row, (uint32_t)src))
-                                       : m_part[row];
-                M = fmaxf(M, mk);
-            }
+            for (int src = 0; src < S; ++src)
+                for (int gg = 0; gg < kA2Groups; ++gg) {
+                    const uint32_t ma = m_addr + 4u * (gg * 64 + row);
+                    const float mk = S > 1 ? ld_cluster_f32(map_to_rank(ma, (uint32_t)src)) : m_part[gg * 64 + row];
+                    M = fmaxf(M, mk);
+                }
             const float base = M == -INFINITY ? 0.f : M;
             float lt = 0.f, o0 = 0.f, o1 = 0.f;
-            for (int src = 0; src < S; ++src) {
-                float mk, lk;
-                float2 ok;
-                if (S > 1) {
-                    mk = ld_cluster_f32(map_to_rank(m_addr + 4u * row, (uint32_t)src));
-                    lk = ld_cluster_f32(map_to_rank(l_addr + 4u * row, (uint32_t)src));
-                    ok = ld_cluster_f2(map_to_rank(o_addr + 4u * (row * kA2OStride + 2 * lane), (uint32_t)src));
-                } else {
-                    mk = m_part[row];
-                    lk = l_part[row];
-                    ok = *reinterpret_cast<const float2 *>(o_part + row * kA2OStride + 2 * lane);
+            for (int src = 0; src < S; ++src)
+                for (int gg = 0; gg < kA2Groups; ++gg) {
+                    const uint32_t ma = m_addr + 4u * (gg * 64 + row), la = l_addr + 4u * (gg * 64 + row);
+                    const uint32_t oa = o_addr + 4u * (gg * 64 * kA2OStride + row * kA2OStride + 2 * lane);
+                    float mk, lk;
+                    float2 ok;
+                    if (S > 1) {
+                        mk = ld_cluster_f32(map_to_rank(ma, (uint32_t)src));
+                        lk = ld_cluster_f32(map_to_rank(la, (uint32_t)src));
+                        ok = ld_cluster_f2(map_to_rank(oa, (uint32_t)src));
+                    } else {
+                        mk = m_part[gg * 64 + row];
+                        lk = l_part[gg * 64 + row];
+                        ok = *reinterpret_cast<const float2 *>(o_part + gg * 64 * kA2OStride + row * kA2OStride + 2 * lane);
+                    }
+                    const float w = exp2f(mk - base);
+                    lt = lt + lk * w;
+                    o0 = o0 + ok.x * w;
+                    o1 = o1 + ok.y * w;
                 }
-                const float w = exp2f(mk - base);
-                lt = lt + lk * w;
-                o0 = o0 + ok.x * w;
-                o1 = o1 + ok.y * w;
-            }
             const float inv = lt > 0.f ? 1.0f / lt : 0.f;
             o0 *= inv;
             o1 *= inv;
