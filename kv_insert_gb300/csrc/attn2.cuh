@@ -21,11 +21,11 @@
 // registers as mma.sync A fragments) take blocks of 4 pages in turn and run
 // QK^T, the online softmax (base 2; masks only near the causal / window
 // edges) and PV with mma.sync, P going from the S accumulators straight into
-// the A fragments.  Each group keeps its own (max, sum, O); the S CTAs of a
-// (request, KV head) form a cluster and all S x G partials are merged through
-// distributed shared memory in a fixed order — no global workspace,
-// deterministic for a launch shape — then each rank finishes 64 / S rows:
-// o-norm, gate, BF16 store.
+// the A fragments.  Each group keeps its own (max, sum, O), folded into one
+// per CTA in group order; the S CTAs of a (request, KV head) form a cluster
+// and merge their partials through distributed shared memory in rank order —
+// no global workspace, deterministic for a launch shape — then each rank
+// finishes 64 / S rows: o-norm, gate, BF16 store.
 
 #ifndef A2_GROUPS
 #define A2_GROUPS 3
@@ -377,6 +377,38 @@ __global__ void __launch_bounds__(kA2Threads, 1)
             l_part[grp * 64 + ra] = l_a;
             l_part[grp * 64 + rb] = l_b;
         }
+        if (kA2Groups > 1) {
+            // fold the groups' partials into group 0's, in group order
+            a2_compute_bar_sync();
+            for (int it = tid; it < 64 * 32; it += 32 * kA2ComputeWarps) {
+                const int row = it >> 5, d = 2 * (it & 31);
+                float M = -INFINITY;
+#pragma unroll
+                for (int gg = 0; gg < kA2Groups; ++gg) M = fmaxf(M, m_part[gg * 64 + row]);
+                const float base = M == -INFINITY ? 0.f : M;
+                float o0 = 0.f, o1 = 0.f;
+#pragma unroll
+                for (int gg = 0; gg < kA2Groups; ++gg) {
+                    const float w = exp2f(m_part[gg * 64 + row] - base);
+                    const float2 v = *reinterpret_cast<const float2 *>(o_part + gg * 64 * kA2OStride + row * kA2OStride + d);
+                    o0 = o0 + v.x * w;
+                    o1 = o1 + v.y * w;
+                }
+                *reinterpret_cast<float2 *>(o_part + row * kA2OStride + d) = make_float2(o0, o1);
+            }
+            a2_compute_bar_sync();   // every O item used the groups' maxima
+            if (tid < 64) {
+                float M = -INFINITY;
+#pragma unroll
+                for (int gg = 0; gg < kA2Groups; ++gg) M = fmaxf(M, m_part[gg * 64 + tid]);
+                const float base = M == -INFINITY ? 0.f : M;
+                float lt = 0.f;
+#pragma unroll
+                for (int gg = 0; gg < kA2Groups; ++gg) lt = lt + l_part[gg * 64 + tid] * exp2f(m_part[gg * 64 + tid] - base);
+                m_part[tid] = M;
+                l_part[tid] = lt;
+            }
+        }
     }
     __syncthreads();
     if (S > 1) cluster_sync_all();
@@ -390,36 +422,38 @@ __global__ void __launch_bounds__(kA2Threads, 1)
         const uint32_t o_addr = smem_u32(o_part), m_addr = smem_u32(m_part), l_addr = smem_u32(l_part);
         for (int i = warp; i < rows; i += kA2ComputeWarps + 1) {
             const int row = (int)z * rows + i;
-            // partials in the fixed order (rank 0, group 0), (0, 1), ..., (S-1, G-1)
-            float M = -INFINITY;
-            for (int src = 0; src < S; ++src)
-                for (int gg = 0; gg < kA2Groups; ++gg) {
-                    const uint32_t ma = m_addr + 4u * (gg * 64 + row);
-                    const float mk = S > 1 ? ld_cluster_f32(map_to_rank(ma, (uint32_t)src)) : m_part[gg * 64 + row];
-                    M = fmaxf(M, mk);
+            // the ranks' partials in rank order; all remote loads issued first
+            float mk[kA2MaxSplits], lk[kA2MaxSplits];
+            float2 ov[kA2MaxSplits];
+#pragma unroll
+            for (int src = 0; src < kA2MaxSplits; ++src) {
+                if (src < S) {
+                    if (S > 1) {
+                        mk[src] = ld_cluster_f32(map_to_rank(m_addr + 4u * row, (uint32_t)src));
+                        lk[src] = ld_cluster_f32(map_to_rank(l_addr + 4u * row, (uint32_t)src));
+                        ov[src] = ld_cluster_f2(map_to_rank(o_addr + 4u * (row * kA2OStride + 2 * lane), (uint32_t)src));
+                    } else {
+                        mk[src] = m_part[row];
+                        lk[src] = l_part[row];
+                        ov[src] = *reinterpret_cast<const float2 *>(o_part + row * kA2OStride + 2 * lane);
+                    }
                 }
+            }
+            float M = -INFINITY;
+#pragma unroll
+            for (int src = 0; src < kA2MaxSplits; ++src)
+                if (src < S) M = fmaxf(M, mk[src]);
             const float base = M == -INFINITY ? 0.f : M;
             float lt = 0.f, o0 = 0.f, o1 = 0.f;
-            for (int src = 0; src < S; ++src)
-                for (int gg = 0; gg < kA2Groups; ++gg) {
-                    const uint32_t ma = m_addr + 4u * (gg * 64 + row), la = l_addr + 4u * (gg * 64 + row);
-                    const uint32_t oa = o_addr + 4u * (gg * 64 * kA2OStride + row * kA2OStride + 2 * lane);
-                    float mk, lk;
-                    float2 ok;
-                    if (S > 1) {
-                        mk = ld_cluster_f32(map_to_rank(ma, (uint32_t)src));
-                        lk = ld_cluster_f32(map_to_rank(la, (uint32_t)src));
-                        ok = ld_cluster_f2(map_to_rank(oa, (uint32_t)src));
-                    } else {
-                        mk = m_part[gg * 64 + row];
-                        lk = l_part[gg * 64 + row];
-                        ok = *reinterpret_cast<const float2 *>(o_part + gg * 64 * kA2OStride + row * kA2OStride + 2 * lane);
-                    }
-                    const float w = exp2f(mk - base);
-                    lt = lt + lk * w;
-                    o0 = o0 + ok.x * w;
-                    o1 = o1 + ok.y * w;
+#pragma unroll
+            for (int src = 0; src < kA2MaxSplits; ++src) {
+                if (src < S) {
+                    const float w = exp2f(mk[src] - base);
+                    lt = lt + lk[src] * w;
+                    o0 = o0 + ov[src].x * w;
+                    o1 = o1 + ov[src].y * w;
                 }
+            }
             const float inv = lt > 0.f ? 1.0f / lt : 0.f;
             o0 *= inv;
             o1 *= inv;
