@@ -549,7 +549,7 @@ def run_attn2(args, w):
     torch.cuda.synchronize(dev)
     stream = torch.cuda.Stream(device=dev)
     per_graph = max(copies, (args.graph_calls // copies) * copies)
-    splits = qf.attn2_splits(w.R, w.num_kv_heads, w.max_blocks())
+    splits = qf.attn2_splits(w.R, w.num_kv_heads, w.max_blocks(), w.window)
 
     def call(i):
         qf.attn2(g["qkv"], caches[i % copies], g["block_table"], g["context_lens"], out=out,

@@ -242,9 +242,12 @@ int layer_front(const void *x, int x_is_f32, const uint16_t *weight, float *stre
  * A request whose length is < 8 or needs more than max_blocks pages, or
  * whose table names a page outside the cache, is skipped (its rows left as
  * they were) and raises QKVF_STATUS_BAD_REQUEST.  Long contexts are split
- * over up to 16 CTAs of a cluster, chosen from num_reqs, num_kv_heads and
- * max_blocks (not from the lengths, which stay on the device); the split
- * partials are merged through distributed shared memory in a fixed order.
+ * over up to 8 CTAs of a cluster (attn2_launch_splits reaches 16), chosen
+ * from num_reqs, num_kv_heads, max_blocks and window (not from the lengths,
+ * which stay on the device): doubled while num_reqs * num_kv_heads * splits
+ * stays within the SM count and each split keeps two or more of the pages a
+ * row can see; the split partials are merged through distributed shared
+ * memory in a fixed order.
  * Allocates nothing; launched with PDL like qkv_front.
  */
 int attn2(const uint16_t *qkv, const uint16_t *kv_cache, int64_t num_pages,
@@ -259,8 +262,9 @@ int attn2_launch_splits(const uint16_t *qkv, const uint16_t *kv_cache, int64_t n
                         int num_reqs, int N, int num_kv_heads, int window, float scale, float eps,
                         uint16_t *out, int splits, void *stream);
 
-/* The split attn2 uses for this shape on the current device (0 on bad input). */
-int attn2_splits(int num_reqs, int num_kv_heads, int max_blocks);
+/* The split attn2 uses for this shape (window 0: none) on the current device
+ * (0 on bad input). */
+int attn2_splits(int num_reqs, int num_kv_heads, int max_blocks, int window);
 
 /* Static text of a QKVF_* return code. */
 const char *qkv_front_strerror(int code);

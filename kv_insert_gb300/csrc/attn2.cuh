@@ -15,8 +15,9 @@
 // with o = softmax(scale q K^T) V.
 //
 // Design: a CTA per (request r, KV head g, split z).  A producer warp streams
-// the CTA's pages (p0 + z, p0 + z + S, ...) as two 16 x 64 TMA boxes each (K
-// and V halves, 128-byte swizzle) into a ring.  Groups of four compute warps
+// the CTA's pages (p0 + z, p0 + z + S, ...) into a ring, one TMA box per page
+// (16 K rows then 16 V rows of 64, 128-byte swizzle), blocks of 4 pages
+// sharing one full / empty barrier pair.  Groups of four compute warps
 // (16 of the 64 query rows each — 8 tokens x 8 heads, row 8 i + j — held in
 // registers as mma.sync A fragments) take blocks of 4 pages in turn and run
 // QK^T, the online softmax (base 2; masks only near the causal / window
@@ -30,22 +31,38 @@
 #ifndef A2_GROUPS
 #define A2_GROUPS 3
 #endif
+#ifndef A2_RING_BLOCKS
+#define A2_RING_BLOCKS 12
+#endif
+#ifndef A2_BLOCK
+#define A2_BLOCK 4
+#endif
 
 namespace qkvf {
 
 constexpr int kA2Groups = A2_GROUPS;                      // groups of 4 compute warps
 constexpr int kA2ComputeWarps = 4 * kA2Groups;
 constexpr int kA2Threads = 32 * (kA2ComputeWarps + 1);   // the last warp produces
-constexpr int kA2Block = 4;                               // pages per softmax step (64 keys)
-constexpr int kA2Stages = kA2Groups * kA2Block;           // ring slot k % stages always serves group (k / block) % groups
+constexpr int kA2Block = A2_BLOCK;                        // pages per softmax step (16 per page)
+constexpr int kA2RingBlocks = A2_RING_BLOCKS;
+constexpr int kA2Stages = kA2RingBlocks * kA2Block;       // pages in flight per CTA
+// ring slot k % stages always serves group (k / block) % groups: each group
+// waits on its own slots in order, so a full barrier's parity never aliases
+static_assert(kA2RingBlocks % kA2Groups == 0, "ring blocks must be a multiple of the groups");
+static_assert(32 % kA2Block == 0, "a block's table entries lie in one 32-entry chunk");
 constexpr uint32_t kA2PageBytes = 4096;                   // K box + V box
 constexpr int kA2OStride = 68;                            // floats per row of the O partial
 constexpr int kA2MaxSplits = 16;
+constexpr int kA2AutoSplits = 8;   // the largest split chosen by default
 constexpr int kA2MaxRequests = 65535;   // grid z
 
 struct A2Layout {
     uint32_t q, ring, full, empty, o, m, l, flags, total;
 };
+
+// the groups' O partials overlay the ring: written only once every page has
+// been consumed and every copy has landed
+static_assert(kA2Groups * 64 * kA2OStride * 4 <= kA2Stages * kA2PageBytes, "O partials must fit the ring");
 
 __host__ __device__ inline A2Layout a2_layout()
 {
@@ -54,13 +71,12 @@ __host__ __device__ inline A2Layout a2_layout()
     L.q = off;
     off += 64 * 128;
     L.ring = off;
+    L.o = off;
     off += kA2Stages * kA2PageBytes;
     L.full = off;
-    off += kA2Stages * 8;
+    off += kA2RingBlocks * 8;
     L.empty = off;
-    off += kA2Stages * 8;
-    L.o = off;
-    off += kA2Groups * 64 * kA2OStride * 4;
+    off += kA2RingBlocks * 8;
     L.m = off;
     off += kA2Groups * 64 * 4;
     L.l = off;
@@ -111,6 +127,21 @@ __device__ __forceinline__ void a2_compute_bar_sync()
     asm volatile("bar.sync 2, %0;" ::"n"(32 * kA2ComputeWarps) : "memory");
 }
 
+// named barrier 3 over every warp: the ring is drained and free
+__device__ __forceinline__ void a2_ring_done_sync()
+{
+    asm volatile("bar.sync 3, %0;" ::"n"(kA2Threads) : "memory");
+}
+
+// 2^x for x <= 0 (softmax weights): the hardware approximation, subnormal
+// results flushed to zero — weights below 2^-126 of the row maximum
+__device__ __forceinline__ float a2_ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ uint32_t pack_f2bf(float lo, float hi)
 {
     return pack_bf16x2(__float2bfloat16_rn(lo), __float2bfloat16_rn(hi));
@@ -131,69 +162,94 @@ __global__ void __launch_bounds__(kA2Threads, 1)
     float *o_part = reinterpret_cast<float *>(smem + LY.o);
     float *m_part = reinterpret_cast<float *>(smem + LY.m);
     float *l_part = reinterpret_cast<float *>(smem + LY.l);
-    volatile int *s_flags = reinterpret_cast<volatile int *>(smem + LY.flags);   // [0] abort, [1] request ok
+    // [0] abort, [1] a table entry of this CTA's pages is outside the cache
+    volatile int *s_flags = reinterpret_cast<volatile int *>(smem + LY.flags);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kA2Stages; ++s) {
+        for (int s = 0; s < kA2RingBlocks; ++s) {   // one full / empty pair per block of pages
             mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, 4);   // the 4 warps of the group that owns the slot
+            mbar_init(empty0 + 8 * s, 4);   // the 4 warps of the group that owns the block
         }
         s_flags[0] = 0;
+        s_flags[1] = 0;
         fence_barrier_init();
         griddep_launch_dependents();
     }
     __syncthreads();
     griddep_wait();   // q, the cache, the table and the lengths come from earlier kernels
 
-    // ---- the request: length, visible pages, table entries in range --------
+    // ---- the request: length and visible pages ----------------------------
     const int L = p.context_lens[r];
     const int nblk = (L + kPageSlots - 1) / kPageSlots;
     const bool len_ok = L >= 8 && nblk <= p.max_blocks;
+    if (!len_ok && threadIdx.x == 0 && z == 0 && g == 0) atomicOr(&g_status, QKVF_STATUS_BAD_REQUEST);
     const int p_first = (p.window > 0 && L - 8 - p.window + 1 > 0) ? (L - 8 - p.window + 1) / kPageSlots : 0;
     const int p_last = len_ok ? (L - 1) / kPageSlots : -1;
     const int32_t *bt = p.block_table + (size_t)r * p.max_blocks;
-    if (warp == kA2ComputeWarps) {
-        unsigned bad = len_ok ? 0u : 1u;
-        for (int b = p_first + lane; b <= p_last; b += 32) {
-            const int32_t pg = bt[b];
-            if (pg < 0 || pg >= p.num_pages) bad = 1u;
-        }
-        bad = __reduce_or_sync(0xffffffffu, bad);
-        if (lane == 0) {
-            s_flags[1] = bad ? 0 : 1;
-            if (bad && z == 0 && g == 0) atomicOr(&g_status, QKVF_STATUS_BAD_REQUEST);
-        }
-    }
-    __syncthreads();
-    const bool req_ok = s_flags[1] != 0;
+    const bool req_ok = len_ok;
     const int first_mine = p_first + (int)z;
-    const int npages = (req_ok && first_mine <= p_last) ? (p_last - first_mine) / S + 1 : 0;
+    const int npages = (len_ok && first_mine <= p_last) ? (p_last - first_mine) / S + 1 : 0;
 
     if (warp == kA2ComputeWarps) {
         // ---- produce: K and V boxes of this CTA's pages -------------------
-        if (lane == 0) {
-            tma_prefetch_map(&tmKV);
-            int issued = 0;
-            for (int k = 0; k < npages; ++k) {
-                const int s = k % kA2Stages, use = k / kA2Stages;
-                if (use > 0 && !bounded_wait(empty0 + 8 * s, (uint32_t)((use - 1) & 1),
-                                             s_flags, p.wait_limit_ns, true))
+        // The table entries come in 32 at a time (lane l holds page c + l of
+        // chunk c), one chunk ahead of the copies, so no copy waits on a
+        // table read.  Per block of 4 pages: lane 0 waits for the ring block
+        // and arms its full barrier with the block's bytes, then the lanes
+        // holding the block's pages issue their copies side by side.  An
+        // entry outside the cache is flagged (the request's rows are then
+        // skipped by every rank) and page 0 copied instead, so the ring's
+        // accounting does not change.
+        if (lane == 0) tma_prefetch_map(&tmKV);
+        int issued = 0;   // blocks
+        unsigned bad = 0u;
+        bool stop = false;
+        int next = lane < npages ? bt[first_mine + lane * S] : 0;
+        for (int c = 0; c < npages && !stop; c += 32) {
+            int page = next;
+            if (c + 32 + lane < npages) next = bt[first_mine + (c + 32 + lane) * S];
+            if (c + lane < npages && (page < 0 || page >= p.num_pages)) {
+                bad = 1u;
+                page = 0;
+            }
+            const int c_end = npages - c < 32 ? npages : c + 32;
+            for (int k0 = c; k0 < c_end; k0 += kA2Block) {
+                const int jb = k0 / kA2Block, rb = jb % kA2RingBlocks, use = jb / kA2RingBlocks;
+                const int nb = npages - k0 < kA2Block ? npages - k0 : kA2Block;
+                int ok = 1;
+                if (lane == 0) {
+                    ok = use == 0 || bounded_wait(empty0 + 8 * rb, (uint32_t)((use - 1) & 1),
+                                                  s_flags, p.wait_limit_ns, true);
+                    if (ok) mbar_expect_tx(full0 + 8 * rb, (uint32_t)nb * kA2PageBytes);
+                }
+                if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                    stop = true;
                     break;
-                const int page = bt[first_mine + k * S];
-                const uint32_t dst = sRing + (uint32_t)s * kA2PageBytes;
-                mbar_expect_tx(full0 + 8 * s, kA2PageBytes);
-                tma_load_4d(dst, &tmKV, full0 + 8 * s, 0, 0, 0, page * p.nkv + g);          // K half
-                tma_load_4d(dst + 2048, &tmKV, full0 + 8 * s, 0, 1, 0, page * p.nkv + g);   // V half
+                }
+                const int b = c + lane - k0;   // this lane's page within the block
+                if (b >= 0 && b < nb) {
+                    const uint32_t dst = sRing + (uint32_t)(rb * kA2Block + b) * kA2PageBytes;
+                    // one box: the page's 16 K rows, then its 16 V rows
+                    tma_load_4d(dst, &tmKV, full0 + 8 * rb, 0, 0, 0, page * p.nkv + g);
+                }
                 ++issued;
             }
-            if (s_flags[0]) {   // drain our copies before leaving
-                const int first = issued > kA2Stages ? issued - kA2Stages : 0;
-                for (int k = first; k < issued; ++k)
-                    bounded_wait(full0 + 8 * (k % kA2Stages), (uint32_t)((k / kA2Stages) & 1),
+        }
+        bad = __reduce_or_sync(0xffffffffu, bad);
+        if (lane == 0) {
+            if (bad) {
+                s_flags[1] = 1;
+                atomicOr(&g_status, QKVF_STATUS_BAD_REQUEST);
+            }
+            if (s_flags[0]) {   // drain our copies before the ring is reused or we leave
+                const int first = issued > kA2RingBlocks ? issued - kA2RingBlocks : 0;
+                for (int j = first; j < issued; ++j)
+                    bounded_wait(full0 + 8 * (j % kA2RingBlocks), (uint32_t)((j / kA2RingBlocks) & 1),
                                  s_flags, p.wait_limit_ns, false);
             }
         }
         __syncwarp();
+        a2_ring_done_sync();
     } else {
         // ---- compute: group grp = warp / 4 takes blocks grp, grp + G, ... ----
         const int tid = threadIdx.x;
@@ -210,7 +266,7 @@ __global__ void __launch_bounds__(kA2Threads, 1)
         }
         a2_compute_bar_sync();
         const int gq = lane >> 2, t = lane & 3;
-        uint32_t qa[4][4];
+        uint32_t qa[4][4];   // the warp's 16 Q rows as mma A fragments
         const uint32_t a_row = (uint32_t)(wig * 16 + (lane & 7) + ((lane >> 3) & 1) * 8);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
@@ -240,16 +296,15 @@ __global__ void __launch_bounds__(kA2Threads, 1)
         // reduction and one rescale of O per block, independent mma chains
         for (int k0 = grp * kA2Block; k0 < npages; k0 += kA2Groups * kA2Block) {
             const int nb = npages - k0 < kA2Block ? npages - k0 : kA2Block;   // same for every lane
-            bool landed = true;
+            const int jb = k0 / kA2Block, rb = jb % kA2RingBlocks;
+            const uint32_t ph = (uint32_t)((jb / kA2RingBlocks) & 1);
             bool inside = true;
             for (int b = 0; b < nb; ++b) {
-                const int k = k0 + b, s = k % kA2Stages;
-                const uint32_t ph = (uint32_t)((k / kA2Stages) & 1);
-                const int key0 = (first_mine + k * S) * kPageSlots;
+                const int key0 = (first_mine + (k0 + b) * S) * kPageSlots;
                 inside = inside && key0 >= edge_lo && key0 + kPageSlots - 1 <= edge_hi;
-                landed = landed && (mbar_try_wait(full0 + 8 * s, ph) ||
-                                    bounded_wait(full0 + 8 * s, ph, s_flags, p.wait_limit_ns, true));
             }
+            const bool landed = mbar_try_wait(full0 + 8 * rb, ph) ||
+                                bounded_wait(full0 + 8 * rb, ph, s_flags, p.wait_limit_ns, true);
             inside = inside && nb == kA2Block;
             if (__all_sync(0xffffffffu, landed)) {
                 float sc[2 * kA2Block][4];
@@ -270,20 +325,9 @@ __global__ void __launch_bounds__(kA2Threads, 1)
                         }
                     }
                 }
-                // scale into base 2 and (near the edges) mask: element e of tile
-                // nt = 2 b + h is key key0(b) + 8 h + 2 t + (e & 1), row a for e < 2
-                float mx_a = -INFINITY, mx_b = -INFINITY;
-                if (inside) {
-#pragma unroll
-                    for (int nt = 0; nt < 2 * kA2Block; ++nt)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float v = sc[nt][e] * p.scale_log2;
-                            sc[nt][e] = v;
-                            if (e >= 2) mx_b = fmaxf(mx_b, v);
-                            else mx_a = fmaxf(mx_a, v);
-                        }
-                } else {
+                // (near the edges) mask: element e of tile nt = 2 b + h is key
+                // key0(b) + 8 h + 2 t + (e & 1), row a for e < 2
+                if (!inside) {
 #pragma unroll
                     for (int b = 0; b < kA2Block; ++b) {
                         const int key0 = (first_mine + (k0 + b) * S) * kPageSlots;
@@ -292,16 +336,27 @@ __global__ void __launch_bounds__(kA2Threads, 1)
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
                                 const int key = key0 + 8 * h + 2 * t + (e & 1);
-                                const bool rb = e >= 2;
-                                const bool ok = b < nb &&
-                                                (rb ? (key >= lo_b && key <= pos_b) : (key >= lo_a && key <= pos_a));
-                                const float v = ok ? sc[2 * b + h][e] * p.scale_log2 : -INFINITY;
-                                sc[2 * b + h][e] = v;
-                                if (rb) mx_b = fmaxf(mx_b, v);
-                                else mx_a = fmaxf(mx_a, v);
+                                const bool ok = b < nb && (e >= 2 ? (key >= lo_b && key <= pos_b)
+                                                                  : (key >= lo_a && key <= pos_a));
+                                if (!ok) sc[2 * b + h][e] = -INFINITY;
                             }
                     }
                 }
+                // block maxima of the raw scores (the scale is positive), as trees
+                float tm[2 * kA2Block][2];
+#pragma unroll
+                for (int nt = 0; nt < 2 * kA2Block; ++nt) {
+                    tm[nt][0] = fmaxf(sc[nt][0], sc[nt][1]);
+                    tm[nt][1] = fmaxf(sc[nt][2], sc[nt][3]);
+                }
+#pragma unroll
+                for (int w = kA2Block; w >= 1; w >>= 1)
+#pragma unroll
+                    for (int nt = 0; nt < w; ++nt) {
+                        tm[nt][0] = fmaxf(tm[nt][0], tm[nt + w][0]);
+                        tm[nt][1] = fmaxf(tm[nt][1], tm[nt + w][1]);
+                    }
+                float mx_a = tm[0][0] * p.scale_log2, mx_b = tm[0][1] * p.scale_log2;
 #pragma unroll
                 for (int off = 1; off <= 2; off <<= 1) {
                     mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, off));
@@ -310,19 +365,26 @@ __global__ void __launch_bounds__(kA2Threads, 1)
                 const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
                 const float base_a = mn_a == -INFINITY ? 0.f : mn_a;
                 const float base_b = mn_b == -INFINITY ? 0.f : mn_b;
-                const float al_a = exp2f(m_a - base_a), al_b = exp2f(m_b - base_b);
-                float sum_a = 0.f, sum_b = 0.f;
+                const float al_a = a2_ex2(m_a - base_a), al_b = a2_ex2(m_b - base_b);
+                // weights 2^(scale s - base), one FMA and one ex2 each; sums as trees
+                float ts[2 * kA2Block][2];
 #pragma unroll
-                for (int nt = 0; nt < 2 * kA2Block; ++nt)
+                for (int nt = 0; nt < 2 * kA2Block; ++nt) {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float pe = exp2f(sc[nt][e] - (e >= 2 ? base_b : base_a));
-                        sc[nt][e] = pe;
-                        if (e >= 2) sum_b += pe;
-                        else sum_a += pe;
+                    for (int e = 0; e < 4; ++e)
+                        sc[nt][e] = a2_ex2(fmaf(sc[nt][e], p.scale_log2, e >= 2 ? -base_b : -base_a));
+                    ts[nt][0] = sc[nt][0] + sc[nt][1];
+                    ts[nt][1] = sc[nt][2] + sc[nt][3];
+                }
+#pragma unroll
+                for (int w = kA2Block; w >= 1; w >>= 1)
+#pragma unroll
+                    for (int nt = 0; nt < w; ++nt) {
+                        ts[nt][0] += ts[nt + w][0];
+                        ts[nt][1] += ts[nt + w][1];
                     }
-                l_a = l_a * al_a + sum_a;
-                l_b = l_b * al_b + sum_b;
+                l_a = l_a * al_a + ts[0][0];
+                l_b = l_b * al_b + ts[0][1];
                 m_a = mn_a;
                 m_b = mn_b;
 #pragma unroll
@@ -353,8 +415,9 @@ __global__ void __launch_bounds__(kA2Threads, 1)
             }
             __syncwarp();
             if (lane == 0)
-                for (int b = 0; b < nb; ++b) mbar_arrive(empty0 + 8 * ((k0 + b) % kA2Stages));
+                mbar_arrive(empty0 + 8 * rb);
         }
+        a2_ring_done_sync();   // every group is past the ring; the producer has drained
         // whole-row sums across the four threads of a row
 #pragma unroll
         for (int off = 1; off <= 2; off <<= 1) {
@@ -413,8 +476,20 @@ __global__ void __launch_bounds__(kA2Threads, 1)
     __syncthreads();
     if (S > 1) cluster_sync_all();
 
-    // ---- merge the ranks' partials, o-norm, gate, store (64 / S rows each) ----
+    // a request with an entry outside the cache on any rank is skipped by all
+    bool table_ok = true;
     if (req_ok) {
+        unsigned bad_rank = 0u;
+        if (S > 1) {
+            if (lane < S) bad_rank = ld_cluster_u32(map_to_rank(smem_u32(smem + LY.flags) + 4u, (uint32_t)lane));
+        } else if (lane == 0) {
+            bad_rank = (unsigned)s_flags[1];
+        }
+        table_ok = !__any_sync(0xffffffffu, bad_rank != 0u);
+    }
+
+    // ---- merge the ranks' partials, o-norm, gate, store (64 / S rows each) ----
+    if (req_ok && table_ok) {
         const int rows = 64 / S;
         const int q_heads = kQPerKv * p.nkv;
         const int gate_col = q_heads * kHeadDim + 2 * p.nkv * kHeadDim;
@@ -476,11 +551,14 @@ __global__ void __launch_bounds__(kA2Threads, 1)
 
 int encode_kv_map(const uint16_t *kv_cache, int64_t num_pages, int nkv, CUtensorMap *m)
 {
-    // [pages * nkv][16 slots][2 halves][64]: dim 0 = 64 elements of a half,
-    // dim 1 = K / V half, dim 2 = slot, dim 3 = (page, KV head)
-    const cuuint64_t dims[4] = {64, 2, (cuuint64_t)kPageSlots, (cuuint64_t)num_pages * nkv};
-    const cuuint64_t strides[3] = {128, 256, (cuuint64_t)kPageSlots * kSlotWidth * 2};
-    const cuuint32_t box[4] = {64, 1, (cuuint32_t)kPageSlots, 1};
+    // the cache [pages * nkv][16 slots][2 halves][64] seen with the half
+    // dimension outside the slot dimension: dim 0 = 64 elements of a half,
+    // dim 1 = slot (256 B apart), dim 2 = K / V half (128 B apart), dim 3 =
+    // (page, KV head).  One {64, 16, 2, 1} box is a page of one KV head with
+    // its 16 K rows first and its 16 V rows after, each 128 bytes, swizzled
+    const cuuint64_t dims[4] = {64, (cuuint64_t)kPageSlots, 2, (cuuint64_t)num_pages * nkv};
+    const cuuint64_t strides[3] = {256, 128, (cuuint64_t)kPageSlots * kSlotWidth * 2};
+    const cuuint32_t box[4] = {64, (cuuint32_t)kPageSlots, 2, 1};
     const cuuint32_t es[4] = {1, 1, 1, 1};
     return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, (void *)kv_cache, dims, strides, box, es,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -526,10 +604,21 @@ const char *check_attn2_args(const uint16_t *qkv, const uint16_t *kv_cache, int6
     return nullptr;
 }
 
-int attn2_splits_for(int num_reqs, int nkv, int max_blocks, int sms)
+// CTAs per (request, KV head): doubled while the grid stays within one CTA
+// per SM and every split keeps at least two pages, up to clusters of 8 (with
+// a CTA filling an SM's shared memory, fewer clusters of 16 than GPCs fit at
+// once).  The pages a request can need are its table's width, or with a
+// window W the at most W + 7 keys some row sees, over at most
+// ceil((W + 7) / 16) + 1 pages.
+int attn2_splits_for(int num_reqs, int nkv, int max_blocks, int window, int sms)
 {
+    int64_t pages = max_blocks;
+    if (window > 0) {
+        const int64_t wp = ((int64_t)window + 7 + kPageSlots - 1) / kPageSlots + 1;
+        if (wp < pages) pages = wp;
+    }
     int s = 1;
-    while (s < kA2MaxSplits && num_reqs * nkv * s * 2 <= sms && max_blocks >= 4 * s * 2) s *= 2;
+    while (s < kA2AutoSplits && (int64_t)num_reqs * nkv * s * 2 <= sms && pages >= 4 * (int64_t)s) s *= 2;
     return s;
 }
 
@@ -605,7 +694,7 @@ int attn2(const uint16_t *qkv, const uint16_t *kv_cache, int64_t num_pages,
     qkvf::DeviceState *d;
     const int rc = qkvf::probe_device(&d);
     if (rc != QKVF_OK) return rc;
-    const int splits = qkvf::attn2_splits_for(num_reqs, num_kv_heads, max_blocks, d->sms);
+    const int splits = qkvf::attn2_splits_for(num_reqs, num_kv_heads, max_blocks, window, d->sms);
     return qkvf::launch_attn2(qkv, kv_cache, num_pages, block_table, max_blocks, context_lens,
                               num_reqs, N, num_kv_heads, window, scale, eps, out, splits, stream);
 }
@@ -628,12 +717,12 @@ int attn2_launch_splits(const uint16_t *qkv, const uint16_t *kv_cache, int64_t n
                               num_reqs, N, num_kv_heads, window, scale, eps, out, splits, stream);
 }
 
-int attn2_splits(int num_reqs, int num_kv_heads, int max_blocks)
+int attn2_splits(int num_reqs, int num_kv_heads, int max_blocks, int window)
 {
-    if (num_reqs < 1 || num_kv_heads < 1 || max_blocks < 1) return 0;
+    if (num_reqs < 1 || num_kv_heads < 1 || max_blocks < 1 || window < 0) return 0;
     qkvf::DeviceState *d;
     if (qkvf::probe_device(&d) != QKVF_OK) return 0;
-    return qkvf::attn2_splits_for(num_reqs, num_kv_heads, max_blocks, d->sms);
+    return qkvf::attn2_splits_for(num_reqs, num_kv_heads, max_blocks, window, d->sms);
 }
 
 }  // extern "C"

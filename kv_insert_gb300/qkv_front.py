@@ -103,7 +103,7 @@ def load() -> ctypes.CDLL:
         lib.attn2.restype = i32
         lib.attn2_launch_splits.argtypes = a2 + [i32, vp]
         lib.attn2_launch_splits.restype = i32
-        lib.attn2_splits.argtypes = [i32, i32, i32]
+        lib.attn2_splits.argtypes = [i32, i32, i32, i32]
         lib.attn2_splits.restype = i32
         lib.qkv_front_set_pdl.argtypes = [i32]
         lib.qkv_front_set_pdl.restype = i32
@@ -427,8 +427,8 @@ def attn2(qkv, kv_cache, block_table, context_lens, out=None, window: int = 0,
     return out
 
 
-def attn2_splits(num_reqs: int, num_kv_heads: int, max_blocks: int) -> int:
-    return int(load().attn2_splits(num_reqs, num_kv_heads, max_blocks))
+def attn2_splits(num_reqs: int, num_kv_heads: int, max_blocks: int, window: int = 0) -> int:
+    return int(load().attn2_splits(num_reqs, num_kv_heads, max_blocks, window))
 
 
 def selftest_wait(timeout_ns: int, stream=None) -> None:

@@ -45,6 +45,20 @@ def test_attn2_workloads_match_oracle(name):
     assert_values(wl.bits(out.cpu()), ref, what=f"attn2 {name}")
 
 
+def test_attn2_default_splits():
+    """The split rule on this device: doubled while the grid fits one CTA per
+    SM and each split keeps two or more of the pages a row can see, up to 8."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert sms >= 128   # the cases below assume a full GB300
+    assert qf.attn2_splits(1, 8, 2048) == 8        # one 32K request: 8 x 8 CTAs
+    assert qf.attn2_splits(8, 8, 256) == 2         # 8 requests of 4K: 64 x 2 CTAs
+    assert qf.attn2_splits(2, 8, 64, 128) == 4     # window 128: at most 10 pages a row sees
+    assert qf.attn2_splits(1, 1, 3) == 1           # too few pages to split
+    assert qf.attn2_splits(1, 1, 8) == 4           # two pages per split
+    assert qf.attn2_splits(1, 1, 7) == 2
+    assert qf.attn2_splits(1, 8, 0) == 0           # bad input
+
+
 @pytest.mark.parametrize("splits", [1, 2, 4, 8, 16])
 def test_attn2_every_split(splits):
     w = wl.ATTN_WORKLOADS["attn_r2_window_nkv8"]
