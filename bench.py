@@ -42,9 +42,14 @@ METRIC = "µs/call and achieved HBM GB/s (fraction of GB300 peak) at M=1..16, 1 
 UNIT = "GB/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = [os.path.join(ROOT, "kv_insert_gb300", "csrc", f)
-                  for f in ("qkv_front.cu", "qknorm_rope_kv_insert.cuh", "layer_front.cuh",
-                            "attn2.cuh")]
+# the files that define each op's kernel (qkv_front.cu also holds the shared
+# device helpers); a traffic record counts only for the source it was taken on
+OP_SOURCES = {
+    "qkv_front": ("qkv_front.cu",),
+    "qknorm_rope_kv_insert": ("qkv_front.cu", "qknorm_rope_kv_insert.cuh"),
+    "layer_front": ("qkv_front.cu", "layer_front.cuh"),
+    "attn2": ("qkv_front.cu", "attn2.cuh"),
+}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 
 
@@ -137,9 +142,11 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def source_digest() -> str:
+def source_digest(op: str) -> str:
+    """sha256 over the op's kernel sources and the C header."""
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES + [os.path.join(ROOT, "include", "qkvfront.h")]:
+    files = [os.path.join(ROOT, "kv_insert_gb300", "csrc", f) for f in OP_SOURCES[op]]
+    for f in files + [os.path.join(ROOT, "include", "qkvfront.h")]:
         with open(f, "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
@@ -153,10 +160,10 @@ def recorded_traffic(op: str, workload: str):
             rec = json.load(fh)
     except (OSError, ValueError):
         return None
-    if rec.get("source_sha256") != source_digest():
-        return None
     per = rec.get("records", {}).get(f"{op}/{workload}")
-    return None if per is None else float(per["dram_bytes_per_launch"])
+    if per is None or per.get("source_sha256") != source_digest(op):
+        return None
+    return float(per["dram_bytes_per_launch"])
 
 
 class ClockSampler:
