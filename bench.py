@@ -49,6 +49,7 @@ OP_SOURCES = {
     "qknorm_rope_kv_insert": ("qkv_front.cu", "qknorm_rope_kv_insert.cuh"),
     "layer_front": ("qkv_front.cu", "layer_front.cuh"),
     "attn2": ("qkv_front.cu", "attn2.cuh"),
+    "attn2_split_kv": ("qkv_front.cu", "attn2.cuh"),
 }
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 
@@ -72,6 +73,9 @@ def parse_args(argv=None):
     ap.add_argument("--front-stages", type=int, default=0,
                     help="chain op: run the front at this ring depth (0: the library's choice)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--engine", choices=("cluster", "split_kv"), default="cluster",
+                    help="attn2 engine: clusters merging over DSMEM (the attn2 entry point, no "
+                         "workspace) or split-KV over the whole GPU with partials in a workspace")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seconds", type=float, default=90.0,
@@ -556,11 +560,20 @@ def run_attn2(args, w):
     torch.cuda.synchronize(dev)
     stream = torch.cuda.Stream(device=dev)
     per_graph = max(copies, (args.graph_calls // copies) * copies)
-    splits = qf.attn2_splits(w.R, w.num_kv_heads, w.max_blocks(), w.window)
+    if args.engine == "split_kv":
+        splits = qf.attn2_split_kv_splits(w.R, w.num_kv_heads, w.max_blocks(), w.window)
+        ws = torch.zeros(qf.attn2_split_kv_workspace_bytes(w.R, w.num_kv_heads, splits),
+                         dtype=torch.uint8, device=dev)
 
-    def call(i):
-        qf.attn2(g["qkv"], caches[i % copies], g["block_table"], g["context_lens"], out=out,
-                 window=w.window)
+        def call(i):
+            qf.attn2_split_kv(g["qkv"], caches[i % copies], g["block_table"], g["context_lens"], ws,
+                              out=out, window=w.window, splits=splits)
+    else:
+        splits = qf.attn2_splits(w.R, w.num_kv_heads, w.max_blocks(), w.window)
+
+        def call(i):
+            qf.attn2(g["qkv"], caches[i % copies], g["block_table"], g["context_lens"], out=out,
+                     window=w.window)
 
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
@@ -607,13 +620,14 @@ def run_attn2(args, w):
             "us_per_call": res["us_per_call"], "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": dict(w.describe(), **{
-                "splits": splits,
+                "engine": args.engine, "splits": splits,
                 "l2": f"inputs larger than L2: cache rotated over {copies} copies of "
                       f"{c_bytes / 1e6:.1f} MB (L2 {l2 / 1e6:.1f} MB)",
                 "graph_calls": per_graph, "parallelism": f"replicas x{world}"}),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": peak_kind,
-                         "traffic": recorded_traffic("attn2", w.name),
+                         "traffic": recorded_traffic(
+                             "attn2" if args.engine == "cluster" else "attn2_split_kv", w.name),
                          "bytes_per_launch": w.roofline_bytes()},
             "gpu_launches": args.steps, "clocks": clocks, "e2e": None}
 

@@ -55,6 +55,8 @@ constexpr int kA2OStride = 68;                            // floats per row of t
 constexpr int kA2MaxSplits = 16;
 constexpr int kA2AutoSplits = 8;   // the largest split chosen by default
 constexpr int kA2MaxRequests = 65535;   // grid z
+constexpr int kA2WsMaxSplits = 256;     // workspace engine: CTAs per (request, KV head)
+constexpr int kA2WsSlotFloats = 64 * 64 + 64 + 64 + 64;   // O [64][64], m, l, flags: 17152 bytes
 
 struct A2Layout {
     uint32_t q, ring, full, empty, o, m, l, flags, total;
@@ -89,6 +91,8 @@ __host__ __device__ inline A2Layout a2_layout()
 
 struct Attn2Params {
     const uint16_t *qkv;
+    float *ws;               // split-KV partials (workspace engine), else null
+    unsigned int *counters;  // one arrival counter per (request, KV head), workspace engine
     const int32_t *block_table;
     const int32_t *context_lens;
     uint16_t *out;
@@ -147,6 +151,37 @@ __device__ __forceinline__ uint32_t pack_f2bf(float lo, float hi)
     return pack_bf16x2(__float2bfloat16_rn(lo), __float2bfloat16_rn(hi));
 }
 
+// One output row of (request r, KV head g): o = (o0, o1) at dims 2 lane,
+// 2 lane + 1 and its softmax sum lt -> 1/lt, o-norm over the 64 dims (warp
+// butterfly), sigmoid gate of the row's gate head, bf16 store.
+__device__ __forceinline__ void a2_finish_row(const Attn2Params &p, int r, int g, int row, float o0,
+                                              float o1, float lt, int lane)
+{
+    const int q_heads = kQPerKv * p.nkv;
+    const int gate_col = q_heads * kHeadDim + 2 * p.nkv * kHeadDim;
+    const int out_cols = q_heads * kHeadDim;
+    const float inv = lt > 0.f ? 1.0f / lt : 0.f;
+    o0 *= inv;
+    o1 *= inv;
+    float ss = o0 * o0 + o1 * o1;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    const float rn = 1.0f / sqrtf(ss * (1.0f / kHeadDim) + p.eps);
+    const int tok = row >> 3, hj = 8 * g + (row & 7);
+    const size_t qrow = (size_t)r * 8 + tok;
+    const __nv_bfloat162 gt = *reinterpret_cast<const __nv_bfloat162 *>(
+        p.qkv + qrow * p.N + gate_col + (size_t)hj * kHeadDim + 2 * lane);
+    const float s0 = 1.0f / (1.0f + expf(-__low2float(gt)));
+    const float s1 = 1.0f / (1.0f + expf(-__high2float(gt)));
+    reinterpret_cast<uint32_t *>(p.out + qrow * out_cols + (size_t)hj * kHeadDim)[lane] =
+        pack_f2bf(o0 * rn * s0, o1 * rn * s1);
+}
+
+// kWorkspace = false: the S CTAs of (request, KV head) form a cluster and merge
+// over distributed shared memory.  true: no cluster; each CTA writes its
+// partial to a slot of the caller's workspace and the last of the S to arrive
+// (an atomic counter) merges the S slots in split order and resets the counter.
+template <bool kWorkspace>
 __global__ void __launch_bounds__(kA2Threads, 1)
     attn2_kernel(const __grid_constant__ CUtensorMap tmKV, const Attn2Params p)
 {
@@ -155,7 +190,7 @@ __global__ void __launch_bounds__(kA2Threads, 1)
     const A2Layout LY = a2_layout();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int S = p.splits;
-    const uint32_t z = S > 1 ? cluster_rank() : 0u;
+    const uint32_t z = kWorkspace ? blockIdx.x : (S > 1 ? cluster_rank() : 0u);
     const int g = blockIdx.y, r = blockIdx.z;
     const uint32_t sQ = smem_u32(smem + LY.q), sRing = smem_u32(smem + LY.ring);
     const uint32_t full0 = smem_u32(smem + LY.full), empty0 = smem_u32(smem + LY.empty);
@@ -474,79 +509,122 @@ __global__ void __launch_bounds__(kA2Threads, 1)
         }
     }
     __syncthreads();
-    if (S > 1) cluster_sync_all();
-
-    // a request with an entry outside the cache on any rank is skipped by all
-    bool table_ok = true;
-    if (req_ok) {
-        unsigned bad_rank = 0u;
-        if (S > 1) {
-            if (lane < S) bad_rank = ld_cluster_u32(map_to_rank(smem_u32(smem + LY.flags) + 4u, (uint32_t)lane));
-        } else if (lane == 0) {
-            bad_rank = (unsigned)s_flags[1];
+    if constexpr (kWorkspace) {
+        // ---- publish this CTA's partial; the last of the S merges them ----
+        __shared__ int s_last;
+        const int tid = threadIdx.x;
+        const size_t pair = (size_t)r * p.nkv + g;
+        float *slot = p.ws + (pair * S + z) * kA2WsSlotFloats;
+        for (int it = tid; it < 64 * 16; it += kA2Threads) {
+            const int row = it >> 4, c4 = it & 15;
+            __stcg(reinterpret_cast<float4 *>(slot + row * 64 + 4 * c4),
+                   *reinterpret_cast<const float4 *>(o_part + row * kA2OStride + 4 * c4));
         }
-        table_ok = !__any_sync(0xffffffffu, bad_rank != 0u);
-    }
-
-    // ---- merge the ranks' partials, o-norm, gate, store (64 / S rows each) ----
-    if (req_ok && table_ok) {
-        const int rows = 64 / S;
-        const int q_heads = kQPerKv * p.nkv;
-        const int gate_col = q_heads * kHeadDim + 2 * p.nkv * kHeadDim;
-        const int out_cols = q_heads * kHeadDim;
-        const uint32_t o_addr = smem_u32(o_part), m_addr = smem_u32(m_part), l_addr = smem_u32(l_part);
-        for (int i = warp; i < rows; i += kA2ComputeWarps + 1) {
-            const int row = (int)z * rows + i;
-            // the ranks' partials in rank order; all remote loads issued first
-            float mk[kA2MaxSplits], lk[kA2MaxSplits];
-            float2 ov[kA2MaxSplits];
+        if (tid < 64) {
+            __stcg(slot + 4096 + tid, m_part[tid]);
+            __stcg(slot + 4160 + tid, l_part[tid]);
+        }
+        if (tid == 0) __stcg(reinterpret_cast<int *>(slot + 4224), s_flags[1]);
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) s_last = atomicAdd(p.counters + pair, 1u) == (unsigned)(S - 1);
+        __syncthreads();
+        if (!s_last) return;
+        __threadfence();   // the other CTAs' slots, published before their arrivals
+        if (tid == 0) p.counters[pair] = 0u;   // every CTA of this launch has arrived
+        const float *slots = p.ws + pair * S * kA2WsSlotFloats;
+        unsigned bad = 0u;
+        for (int src = lane; src < S; src += 32)
+            bad |= (unsigned)__ldcg(reinterpret_cast<const int *>(slots + (size_t)src * kA2WsSlotFloats + 4224));
+        if (!req_ok || __any_sync(0xffffffffu, bad != 0u)) return;
+        for (int row = warp; row < 64; row += kA2ComputeWarps + 1) {
+            float M = -INFINITY;
+            for (int src = 0; src < S; ++src)
+                M = fmaxf(M, __ldcg(slots + (size_t)src * kA2WsSlotFloats + 4096 + row));
+            const float base = M == -INFINITY ? 0.f : M;
+            float lt = 0.f, o0 = 0.f, o1 = 0.f;
+            for (int s0 = 0; s0 < S; s0 += 8) {   // 8 slots' loads in flight, summed in split order
+                float mk[8], lk[8];
+                float2 ov[8];
 #pragma unroll
-            for (int src = 0; src < kA2MaxSplits; ++src) {
-                if (src < S) {
-                    if (S > 1) {
-                        mk[src] = ld_cluster_f32(map_to_rank(m_addr + 4u * row, (uint32_t)src));
-                        lk[src] = ld_cluster_f32(map_to_rank(l_addr + 4u * row, (uint32_t)src));
-                        ov[src] = ld_cluster_f2(map_to_rank(o_addr + 4u * (row * kA2OStride + 2 * lane), (uint32_t)src));
-                    } else {
-                        mk[src] = m_part[row];
-                        lk[src] = l_part[row];
-                        ov[src] = *reinterpret_cast<const float2 *>(o_part + row * kA2OStride + 2 * lane);
+                for (int j = 0; j < 8; ++j) {
+                    if (s0 + j < S) {
+                        const float *sl = slots + (size_t)(s0 + j) * kA2WsSlotFloats;
+                        mk[j] = __ldcg(sl + 4096 + row);
+                        lk[j] = __ldcg(sl + 4160 + row);
+                        ov[j] = __ldcg(reinterpret_cast<const float2 *>(sl + row * 64 + 2 * lane));
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if (s0 + j < S) {
+                        const float w = exp2f(mk[j] - base);
+                        lt = lt + lk[j] * w;
+                        o0 = o0 + ov[j].x * w;
+                        o1 = o1 + ov[j].y * w;
                     }
                 }
             }
-            float M = -INFINITY;
-#pragma unroll
-            for (int src = 0; src < kA2MaxSplits; ++src)
-                if (src < S) M = fmaxf(M, mk[src]);
-            const float base = M == -INFINITY ? 0.f : M;
-            float lt = 0.f, o0 = 0.f, o1 = 0.f;
-#pragma unroll
-            for (int src = 0; src < kA2MaxSplits; ++src) {
-                if (src < S) {
-                    const float w = exp2f(mk[src] - base);
-                    lt = lt + lk[src] * w;
-                    o0 = o0 + ov[src].x * w;
-                    o1 = o1 + ov[src].y * w;
-                }
-            }
-            const float inv = lt > 0.f ? 1.0f / lt : 0.f;
-            o0 *= inv;
-            o1 *= inv;
-            float ss = o0 * o0 + o1 * o1;
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-            const float rn = 1.0f / sqrtf(ss * (1.0f / kHeadDim) + p.eps);
-            const int tok = row >> 3, hj = 8 * g + (row & 7);
-            const size_t qrow = (size_t)r * 8 + tok;
-            const __nv_bfloat162 gt = *reinterpret_cast<const __nv_bfloat162 *>(
-                p.qkv + qrow * p.N + gate_col + (size_t)hj * kHeadDim + 2 * lane);
-            const float s0 = 1.0f / (1.0f + expf(-__low2float(gt)));
-            const float s1 = 1.0f / (1.0f + expf(-__high2float(gt)));
-            reinterpret_cast<uint32_t *>(p.out + qrow * out_cols + (size_t)hj * kHeadDim)[lane] =
-                pack_f2bf(o0 * rn * s0, o1 * rn * s1);
+            a2_finish_row(p, r, g, row, o0, o1, lt, lane);
         }
+    } else {
+        if (S > 1) cluster_sync_all();
+
+        // a request with an entry outside the cache on any rank is skipped by all
+        bool table_ok = true;
+        if (req_ok) {
+            unsigned bad_rank = 0u;
+            if (S > 1) {
+                if (lane < S) bad_rank = ld_cluster_u32(map_to_rank(smem_u32(smem + LY.flags) + 4u, (uint32_t)lane));
+            } else if (lane == 0) {
+                bad_rank = (unsigned)s_flags[1];
+            }
+            table_ok = !__any_sync(0xffffffffu, bad_rank != 0u);
+        }
+
+        // ---- merge the ranks' partials, o-norm, gate, store (64 / S rows each) ----
+        if (req_ok && table_ok) {
+            const int rows = 64 / S;
+            const uint32_t o_addr = smem_u32(o_part), m_addr = smem_u32(m_part), l_addr = smem_u32(l_part);
+            for (int i = warp; i < rows; i += kA2ComputeWarps + 1) {
+                const int row = (int)z * rows + i;
+                // the ranks' partials in rank order; all remote loads issued first
+                float mk[kA2MaxSplits], lk[kA2MaxSplits];
+                float2 ov[kA2MaxSplits];
+#pragma unroll
+                for (int src = 0; src < kA2MaxSplits; ++src) {
+                    if (src < S) {
+                        if (S > 1) {
+                            mk[src] = ld_cluster_f32(map_to_rank(m_addr + 4u * row, (uint32_t)src));
+                            lk[src] = ld_cluster_f32(map_to_rank(l_addr + 4u * row, (uint32_t)src));
+                            ov[src] = ld_cluster_f2(map_to_rank(o_addr + 4u * (row * kA2OStride + 2 * lane), (uint32_t)src));
+                        } else {
+                            mk[src] = m_part[row];
+                            lk[src] = l_part[row];
+                            ov[src] = *reinterpret_cast<const float2 *>(o_part + row * kA2OStride + 2 * lane);
+                        }
+                    }
+                }
+                float M = -INFINITY;
+#pragma unroll
+                for (int src = 0; src < kA2MaxSplits; ++src)
+                    if (src < S) M = fmaxf(M, mk[src]);
+                const float base = M == -INFINITY ? 0.f : M;
+                float lt = 0.f, o0 = 0.f, o1 = 0.f;
+#pragma unroll
+                for (int src = 0; src < kA2MaxSplits; ++src) {
+                    if (src < S) {
+                        const float w = exp2f(mk[src] - base);
+                        lt = lt + lk[src] * w;
+                        o0 = o0 + ov[src].x * w;
+                        o1 = o1 + ov[src].y * w;
+                    }
+                }
+                a2_finish_row(p, r, g, row, o0, o1, lt, lane);
+            }
+        }
+        if (S > 1) cluster_sync_all();   // no CTA leaves while its partials may still be read
     }
-    if (S > 1) cluster_sync_all();   // no CTA leaves while its partials may still be read
 }
 
 int encode_kv_map(const uint16_t *kv_cache, int64_t num_pages, int nkv, CUtensorMap *m)
@@ -622,24 +700,62 @@ int attn2_splits_for(int num_reqs, int nkv, int max_blocks, int window, int sms)
     return s;
 }
 
-bool prepare_attn2_kernel()
+// Split-KV engine: CTAs per (request, KV head) so that the grid covers the
+// SMs once (R * nkv * S <= SM count), each keeping two or more of the pages a
+// row can see.
+int attn2_split_kv_splits_for(int num_reqs, int nkv, int max_blocks, int window, int sms)
 {
-    return cudaFuncSetAttribute((const void *)attn2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)a2_layout().total) == cudaSuccess &&
-           cudaFuncSetAttribute((const void *)attn2_kernel,
-                                cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+    int64_t pages = max_blocks;
+    if (window > 0) {
+        const int64_t wp = ((int64_t)window + 7 + kPageSlots - 1) / kPageSlots + 1;
+        if (wp < pages) pages = wp;
+    }
+    int64_t s = sms / ((int64_t)num_reqs * nkv);
+    if (s > pages / 2) s = pages / 2;
+    if (s > kA2WsMaxSplits) s = kA2WsMaxSplits;
+    return s < 1 ? 1 : (int)s;
 }
 
+// Workspace of the split-KV engine: one 32-bit arrival counter per (request,
+// KV head), padded to 256 bytes, then R * nkv * S partial slots of 17152 bytes.
+size_t a2_counter_bytes(int num_reqs, int nkv)
+{
+    return ((size_t)num_reqs * nkv * 4 + 255) / 256 * 256;
+}
+
+size_t a2_workspace_bytes(int num_reqs, int nkv, int splits)
+{
+    return a2_counter_bytes(num_reqs, nkv) + (size_t)num_reqs * nkv * splits * kA2WsSlotFloats * 4;
+}
+
+bool prepare_attn2_kernel()
+{
+    const int smem = (int)a2_layout().total;
+    return cudaFuncSetAttribute((const void *)attn2_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                smem) == cudaSuccess &&
+           cudaFuncSetAttribute((const void *)attn2_kernel<false>,
+                                cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
+           cudaFuncSetAttribute((const void *)attn2_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                smem) == cudaSuccess;
+}
+
+// workspace == null: the cluster engine (splits 1..16, a power of two);
+// otherwise the split-KV engine over that workspace (splits 1..256)
 int launch_attn2(const uint16_t *qkv, const uint16_t *kv_cache, int64_t num_pages,
                  const int32_t *block_table, int max_blocks, const int32_t *context_lens, int num_reqs,
                  int N, int num_kv_heads, int window, float scale, float eps, uint16_t *out, int splits,
-                 void *stream)
+                 void *workspace, void *stream)
 {
     CUtensorMap m;
     int rc = encode_kv_map(kv_cache, num_pages, num_kv_heads, &m);
     if (rc != QKVF_OK) return rc;
+    const bool ws = workspace != nullptr;
     Attn2Params prm;
     prm.qkv = qkv;
+    prm.counters = ws ? static_cast<unsigned int *>(workspace) : nullptr;
+    prm.ws = ws ? reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
+                                            a2_counter_bytes(num_reqs, num_kv_heads))
+                : nullptr;
     prm.block_table = block_table;
     prm.context_lens = context_lens;
     prm.out = out;
@@ -659,7 +775,7 @@ int launch_attn2(const uint16_t *qkv, const uint16_t *kv_cache, int64_t num_page
     cfg.stream = (cudaStream_t)stream;
     cudaLaunchAttribute attrs[2];
     int na = 0;
-    if (splits > 1) {
+    if (!ws && splits > 1) {
         attrs[na].id = cudaLaunchAttributeClusterDimension;
         attrs[na].val.clusterDim.x = (unsigned)splits;
         attrs[na].val.clusterDim.y = 1;
@@ -671,7 +787,9 @@ int launch_attn2(const uint16_t *qkv, const uint16_t *kv_cache, int64_t num_page
     ++na;
     cfg.attrs = attrs;
     cfg.numAttrs = (unsigned)na;
-    if (cudaLaunchKernelEx(&cfg, attn2_kernel, m, prm) != cudaSuccess) {
+    const cudaError_t e = ws ? cudaLaunchKernelEx(&cfg, attn2_kernel<true>, m, prm)
+                             : cudaLaunchKernelEx(&cfg, attn2_kernel<false>, m, prm);
+    if (e != cudaSuccess) {
         (void)cudaGetLastError();
         return QKVF_ERR_CUDA;
     }
@@ -696,7 +814,7 @@ int attn2(const uint16_t *qkv, const uint16_t *kv_cache, int64_t num_pages,
     if (rc != QKVF_OK) return rc;
     const int splits = qkvf::attn2_splits_for(num_reqs, num_kv_heads, max_blocks, window, d->sms);
     return qkvf::launch_attn2(qkv, kv_cache, num_pages, block_table, max_blocks, context_lens,
-                              num_reqs, N, num_kv_heads, window, scale, eps, out, splits, stream);
+                              num_reqs, N, num_kv_heads, window, scale, eps, out, splits, nullptr, stream);
 }
 
 int attn2_launch_splits(const uint16_t *qkv, const uint16_t *kv_cache, int64_t num_pages,
@@ -714,7 +832,7 @@ int attn2_launch_splits(const uint16_t *qkv, const uint16_t *kv_cache, int64_t n
     const int rc = qkvf::probe_device(&d);
     if (rc != QKVF_OK) return rc;
     return qkvf::launch_attn2(qkv, kv_cache, num_pages, block_table, max_blocks, context_lens,
-                              num_reqs, N, num_kv_heads, window, scale, eps, out, splits, stream);
+                              num_reqs, N, num_kv_heads, window, scale, eps, out, splits, nullptr, stream);
 }
 
 int attn2_splits(int num_reqs, int num_kv_heads, int max_blocks, int window)
@@ -723,6 +841,59 @@ int attn2_splits(int num_reqs, int num_kv_heads, int max_blocks, int window)
     qkvf::DeviceState *d;
     if (qkvf::probe_device(&d) != QKVF_OK) return 0;
     return qkvf::attn2_splits_for(num_reqs, num_kv_heads, max_blocks, window, d->sms);
+}
+
+size_t attn2_split_kv_workspace_bytes(int num_reqs, int num_kv_heads, int splits)
+{
+    if (num_reqs < 1 || num_reqs > qkvf::kA2MaxRequests || num_kv_heads < 1 || num_kv_heads > 64 ||
+        splits < 1 || splits > qkvf::kA2WsMaxSplits)
+        return 0;
+    return qkvf::a2_workspace_bytes(num_reqs, num_kv_heads, splits);
+}
+
+int attn2_split_kv_splits(int num_reqs, int num_kv_heads, int max_blocks, int window)
+{
+    if (num_reqs < 1 || num_kv_heads < 1 || max_blocks < 1 || window < 0) return 0;
+    qkvf::DeviceState *d;
+    if (qkvf::probe_device(&d) != QKVF_OK) return 0;
+    return qkvf::attn2_split_kv_splits_for(num_reqs, num_kv_heads, max_blocks, window, d->sms);
+}
+
+int attn2_split_kv(const uint16_t *qkv, const uint16_t *kv_cache, int64_t num_pages,
+                   const int32_t *block_table, int max_blocks, const int32_t *context_lens, int num_reqs,
+                   int N, int num_kv_heads, int window, float scale, float eps, uint16_t *out, int splits,
+                   void *workspace, size_t workspace_bytes, void *stream)
+{
+    int code;
+    if (qkvf::check_attn2_args(qkv, kv_cache, num_pages, block_table, max_blocks, context_lens,
+                               num_reqs, N, num_kv_heads, window, scale, eps, out, &code))
+        return code;
+    if (splits < 0 || splits > qkvf::kA2WsMaxSplits) return QKVF_ERR_VARIANT;
+    if (num_reqs == 0) return QKVF_OK;
+    if (!workspace) return QKVF_ERR_NULL;
+    if (!qkvf::aligned(workspace, 256)) return QKVF_ERR_ALIGN;
+    qkvf::DeviceState *d = nullptr;
+    if (splits == 0) {   // the choice needs the device's SM count
+        const int rc = qkvf::probe_device(&d);
+        if (rc != QKVF_OK) return rc;
+        splits = qkvf::attn2_split_kv_splits_for(num_reqs, num_kv_heads, max_blocks, window, d->sms);
+    }
+    const size_t need = qkvf::a2_workspace_bytes(num_reqs, num_kv_heads, splits);
+    if (workspace_bytes < need) return QKVF_ERR_SIZES;
+    const size_t out_b = (size_t)num_reqs * 8 * qkvf::kQPerKv * num_kv_heads * qkvf::kHeadDim * 2;
+    const size_t qkv_b = (size_t)num_reqs * 8 * N * 2;
+    const size_t cache_b = (size_t)num_pages * num_kv_heads * qkvf::kPageSlots * qkvf::kSlotWidth * 2;
+    if (qkvf::overlap(workspace, need, out, out_b) || qkvf::overlap(workspace, need, qkv, qkv_b) ||
+        qkvf::overlap(workspace, need, kv_cache, cache_b) ||
+        qkvf::overlap(workspace, need, block_table, (size_t)num_reqs * max_blocks * 4) ||
+        qkvf::overlap(workspace, need, context_lens, (size_t)num_reqs * 4))
+        return QKVF_ERR_ARG;
+    if (!d) {
+        const int rc = qkvf::probe_device(&d);
+        if (rc != QKVF_OK) return rc;
+    }
+    return qkvf::launch_attn2(qkv, kv_cache, num_pages, block_table, max_blocks, context_lens,
+                              num_reqs, N, num_kv_heads, window, scale, eps, out, splits, workspace, stream);
 }
 
 }  // extern "C"

@@ -105,6 +105,12 @@ def load() -> ctypes.CDLL:
         lib.attn2_launch_splits.restype = i32
         lib.attn2_splits.argtypes = [i32, i32, i32, i32]
         lib.attn2_splits.restype = i32
+        lib.attn2_split_kv.argtypes = a2 + [i32, vp, ctypes.c_size_t, vp]
+        lib.attn2_split_kv.restype = i32
+        lib.attn2_split_kv_workspace_bytes.argtypes = [i32, i32, i32]
+        lib.attn2_split_kv_workspace_bytes.restype = ctypes.c_size_t
+        lib.attn2_split_kv_splits.argtypes = [i32, i32, i32, i32]
+        lib.attn2_split_kv_splits.restype = i32
         lib.qkv_front_set_pdl.argtypes = [i32]
         lib.qkv_front_set_pdl.restype = i32
         _lib = lib
@@ -394,11 +400,8 @@ def layer_front(x, stream_out, out, aux=None, weight=None, eps: float = 1e-6, st
     return out
 
 
-def attn2(qkv, kv_cache, block_table, context_lens, out=None, window: int = 0,
-          scale: float = 0.125, eps: float = 1e-6, splits=None, stream=None):
-    """Verify-step paged attention with o-norm and sigmoid gate (the o_proj
-    input).  qkv bf16 [8 R, N]; block_table int32 [R, max_blocks];
-    context_lens int32 [R]; returns out bf16 [8 R, 512 num_kv_heads]."""
+def _attn2_args(qkv, kv_cache, block_table, context_lens, out, window, scale, eps):
+    """Checks the torch arguments of attn2 and returns (out, C arguments)."""
     R = context_lens.shape[0]
     nkv = kv_cache.shape[1]
     N = qkv.shape[1]
@@ -419,6 +422,15 @@ def attn2(qkv, kv_cache, block_table, context_lens, out=None, window: int = 0,
     args = (qkv.data_ptr(), kv_cache.data_ptr(), kv_cache.shape[0], block_table.data_ptr(),
             block_table.shape[1], context_lens.data_ptr(), R, N, nkv, int(window), float(scale),
             float(eps), out.data_ptr())
+    return out, args
+
+
+def attn2(qkv, kv_cache, block_table, context_lens, out=None, window: int = 0,
+          scale: float = 0.125, eps: float = 1e-6, splits=None, stream=None):
+    """Verify-step paged attention with o-norm and sigmoid gate (the o_proj
+    input).  qkv bf16 [8 R, N]; block_table int32 [R, max_blocks];
+    context_lens int32 [R]; returns out bf16 [8 R, 512 num_kv_heads]."""
+    out, args = _attn2_args(qkv, kv_cache, block_table, context_lens, out, window, scale, eps)
     with torch.cuda.device(qkv.device):
         if splits is None:
             _check(load().attn2(*args, _stream(stream)))
@@ -429,6 +441,29 @@ def attn2(qkv, kv_cache, block_table, context_lens, out=None, window: int = 0,
 
 def attn2_splits(num_reqs: int, num_kv_heads: int, max_blocks: int, window: int = 0) -> int:
     return int(load().attn2_splits(num_reqs, num_kv_heads, max_blocks, window))
+
+
+def attn2_split_kv_workspace_bytes(num_reqs: int, num_kv_heads: int, splits: int) -> int:
+    return int(load().attn2_split_kv_workspace_bytes(num_reqs, num_kv_heads, splits))
+
+
+def attn2_split_kv_splits(num_reqs: int, num_kv_heads: int, max_blocks: int, window: int = 0) -> int:
+    return int(load().attn2_split_kv_splits(num_reqs, num_kv_heads, max_blocks, window))
+
+
+def attn2_split_kv(qkv, kv_cache, block_table, context_lens, workspace, out=None, window: int = 0,
+                   scale: float = 0.125, eps: float = 1e-6, splits: int = 0, stream=None):
+    """attn2 with the split-KV engine: partials in `workspace` (a uint8 CUDA
+    tensor of at least attn2_split_kv_workspace_bytes bytes, zero-filled
+    before its first use; every call leaves its counters zero)."""
+    out, args = _attn2_args(qkv, kv_cache, block_table, context_lens, out, window, scale, eps)
+    if (not workspace.is_cuda or workspace.dtype != torch.uint8 or not workspace.is_contiguous()
+            or workspace.device != qkv.device):
+        raise ValueError("workspace must be a contiguous uint8 CUDA tensor on qkv's device")
+    with torch.cuda.device(qkv.device):
+        _check(load().attn2_split_kv(*args, int(splits), workspace.data_ptr(), workspace.numel(),
+                                     _stream(stream)))
+    return out
 
 
 def selftest_wait(timeout_ns: int, stream=None) -> None:

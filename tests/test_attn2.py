@@ -146,3 +146,98 @@ def test_decode_layer_front_then_attn2():
     # and the whole layer against the all-oracle chain
     o_chain, _ = oracle.attn2(out_ref, cache_ref, table.numpy(), lens.numpy(), nkv)
     assert_values(wl.bits(o.cpu()), o_chain, what="front + attn2 vs the oracle chain")
+
+
+# ---- the split-KV engine: partials in a caller's workspace, last CTA merges ----
+
+def _workspace(R, nkv, splits):
+    n = qf.attn2_split_kv_workspace_bytes(R, nkv, splits)
+    assert n > 0
+    return torch.zeros(n, dtype=torch.uint8, device="cuda:0")
+
+
+def _counters_zero(ws, R, nkv):
+    return int(ws[:R * nkv * 4].view(torch.int32).abs().sum()) == 0
+
+
+@pytest.mark.parametrize("name", list(wl.ATTN_WORKLOADS))
+def test_attn2_split_kv_workloads_match_oracle(name):
+    w = wl.ATTN_WORKLOADS[name]
+    inp = wl.make_attn_inputs(w)
+    g = _dev(inp)
+    S = qf.attn2_split_kv_splits(w.R, w.num_kv_heads, w.max_blocks(), w.window)
+    assert S >= 1
+    ws = _workspace(w.R, w.num_kv_heads, S)
+    out = qf.attn2_split_kv(g["qkv"], g["kv_cache"], g["block_table"], g["context_lens"], ws,
+                            window=w.window)
+    torch.cuda.synchronize()
+    assert qf.status() == 0
+    assert _counters_zero(ws, w.R, w.num_kv_heads)
+    ref, err = _oracle(inp, w)
+    assert err == 0
+    assert_values(wl.bits(out.cpu()), ref, what=f"attn2 split-KV {name} S={S}")
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 5, 8, 19, 40])
+@pytest.mark.parametrize("name", ["attn_r3_mixed_nkv2", "attn_r2_window_nkv8"])
+def test_attn2_split_kv_every_split(name, splits):
+    """Any split, including more CTAs than pages (empty partials), matches the
+    oracle, repeats bitwise, and leaves the counters at zero."""
+    w = wl.ATTN_WORKLOADS[name]
+    inp = wl.make_attn_inputs(w)
+    g = _dev(inp)
+    ws = _workspace(w.R, w.num_kv_heads, splits)
+    outs = []
+    for _ in range(2):
+        outs.append(qf.attn2_split_kv(g["qkv"], g["kv_cache"], g["block_table"], g["context_lens"],
+                                      ws, window=w.window, splits=splits).clone())
+    torch.cuda.synchronize()
+    assert qf.status() == 0
+    assert _counters_zero(ws, w.R, w.num_kv_heads)
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    ref, _ = _oracle(inp, w)
+    assert_values(wl.bits(outs[0].cpu()), ref, what=f"attn2 split-KV {name} S={splits}")
+
+
+def test_attn2_split_kv_agrees_with_cluster_engine():
+    """Both engines at the same split: the same rows to the tolerance (their
+    merge orders differ only in the split partials' summation)."""
+    w = wl.ATTN_WORKLOADS["attn_r8_l4k_nkv8"]
+    inp = wl.make_attn_inputs(w)
+    g = _dev(inp)
+    a = qf.attn2(g["qkv"], g["kv_cache"], g["block_table"], g["context_lens"], splits=2)
+    ws = _workspace(w.R, w.num_kv_heads, 2)
+    b = qf.attn2_split_kv(g["qkv"], g["kv_cache"], g["block_table"], g["context_lens"], ws, splits=2)
+    torch.cuda.synchronize()
+    assert qf.status() == 0
+    ref, _ = _oracle(inp, w)
+    assert_values(wl.bits(a.cpu()), ref, what="cluster engine")
+    assert_values(wl.bits(b.cpu()), ref, what="split-KV engine")
+
+
+def test_attn2_split_kv_bad_requests_skipped_and_flagged():
+    w = wl.AttnWorkload("bad", R=3, num_kv_heads=1, context=(40, 40, 40), num_pages=16, seed=6200)
+    inp = wl.make_attn_inputs(w)
+    inp["context_lens"][0] = 5
+    inp["block_table"][1, 1] = 999
+    g = _dev(inp)
+    out = torch.full((24, 512), 7.0, dtype=torch.bfloat16, device="cuda:0")
+    ws = _workspace(w.R, 1, 3)
+    qf.attn2_split_kv(g["qkv"], g["kv_cache"], g["block_table"], g["context_lens"], ws, out=out,
+                      splits=3)
+    torch.cuda.synchronize()
+    assert qf.status() == qf.STATUS_BAD_REQUEST
+    assert _counters_zero(ws, w.R, 1)
+    got = wl.bits(out.cpu())
+    assert np.all(got[:16] == wl.bits(torch.tensor([7.0]).to(torch.bfloat16))[0])
+    ref, _ = _oracle(inp, w)
+    assert_values(got[16:], ref[16:], what="the good request")
+
+
+def test_attn2_split_kv_short_workspace_refused():
+    w = wl.ATTN_WORKLOADS["attn_r1_l8_nkv1"]
+    g = _dev(wl.make_attn_inputs(w))
+    ws = _workspace(w.R, 1, 4)
+    with pytest.raises(qf.QkvFrontError):
+        qf.attn2_split_kv(g["qkv"], g["kv_cache"], g["block_table"], g["context_lens"], ws[:-16],
+                          splits=4)

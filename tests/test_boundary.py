@@ -217,3 +217,32 @@ def test_attn2_refusals(lib):
     assert call() in (5, 6)
     assert lib.attn2_launch_splits(X, CACHE, 64, POS, 8, SL, 2, 2304, 2, 0, 0.125, 1e-6, OUT, 3,
                                    None) == 8
+
+
+def test_attn2_split_kv_refusals(lib):
+    """The workspace checks come before any device query: a missing,
+    misaligned, short or overlapping workspace and a bad split are refused."""
+    WS = 1 << 44
+    need = lib.attn2_split_kv_workspace_bytes(2, 2, 3)
+    assert need == 256 + 2 * 2 * 3 * 17152          # counters padded to 256 B, then the slots
+    assert lib.attn2_split_kv_workspace_bytes(1, 1, 1) == 256 + 17152
+    assert lib.attn2_split_kv_workspace_bytes(0, 2, 3) == 0
+    assert lib.attn2_split_kv_workspace_bytes(1, 1, 257) == 0
+    assert lib.attn2_split_kv_workspace_bytes(1, 65, 1) == 0
+    ok = dict(q=X, c=CACHE, pages=64, bt=POS, mb=8, cl=SL, R=2, N=2304, nkv=2, win=0, sc=0.125,
+              eps=1e-6, out=OUT, S=3, ws=WS, n=need)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return lib.attn2_split_kv(a["q"], a["c"], a["pages"], a["bt"], a["mb"], a["cl"], a["R"], a["N"],
+                                  a["nkv"], a["win"], a["sc"], a["eps"], a["out"], a["S"], a["ws"],
+                                  a["n"], None)
+    assert call(R=-1) == 1 and call(N=1152) == 2 and call(q=0) == 3
+    assert call(S=-1) == 8 and call(S=257) == 8
+    assert call(ws=0) == 3
+    assert call(ws=WS + 16) == 4
+    assert call(n=need - 1) == 7
+    assert call(ws=OUT) == 9                         # workspace on top of out
+    assert call(ws=CACHE) == 9                       # workspace inside the cache
+    assert call(R=0, ws=0) == 0
+    assert call() in (5, 6)                          # valid: reaches the device query
