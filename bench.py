@@ -73,7 +73,7 @@ def parse_args(argv=None):
     ap.add_argument("--front-stages", type=int, default=0,
                     help="chain op: run the front at this ring depth (0: the library's choice)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--engine", choices=("cluster", "split_kv"), default="cluster",
+    ap.add_argument("--engine", choices=("cluster", "split_kv"), default="split_kv",
                     help="attn2 engine: clusters merging over DSMEM (the attn2 entry point, no "
                          "workspace) or split-KV over the whole GPU with partials in a workspace")
     ap.add_argument("--no-e2e", action="store_true")
@@ -629,7 +629,8 @@ def run_attn2(args, w):
                          "traffic": recorded_traffic(
                              "attn2" if args.engine == "cluster" else "attn2_split_kv", w.name),
                          "bytes_per_launch": w.roofline_bytes()},
-            "gpu_launches": args.steps, "clocks": clocks, "e2e": None}
+            "gpu_launches": args.steps * (2 if args.engine == "split_kv" else 1), "clocks": clocks,
+            "e2e": None}
 
 
 CHAIN_METRIC = "µs per first-layer front step: layer_front then qkv_front, PDL-linked, 1 GPU"

@@ -271,30 +271,27 @@ int attn2_splits(int num_reqs, int num_kv_heads, int max_blocks, int window);
  * attn2, split-KV engine: the same result as attn2 (same arguments, readings
  * and bad-request rule) with the pages a row sees split over `splits` CTAs
  * per (request, KV head) without clusters, so that few requests can still
- * cover every SM.  Each CTA writes its partial (row maxima, sums and
- * unnormalised O, FP32) to its slot of the caller's workspace; the last CTA
- * of a (request, KV head) to arrive, counted by an atomic counter, merges the
- * slots in split order (so a fixed `splits` gives the same bits every time),
- * finishes the rows and resets the counter.  Nothing waits on another CTA.
+ * cover every SM.  Two grids, PDL-linked on the stream: the first writes each
+ * CTA's partial (row maxima, sums and unnormalised O, FP32) to its slot of
+ * the caller's workspace; the second merges a row's slots in split order (a
+ * fixed `splits` gives the same bits every time) and finishes the rows.
  *   splits          1 .. 256, or 0 for attn2_split_kv_splits' choice;
  *                   otherwise QKVF_ERR_VARIANT.
  *   workspace       device memory, 256-byte aligned, at least
  *                   attn2_split_kv_workspace_bytes(num_reqs, num_kv_heads,
  *                   splits) bytes, owned by the caller, overlapping no other
- *                   argument.  Its counters (the first bytes) must be zero
- *                   before the first call (zero-fill it once); every call
- *                   leaves them zero.  One workspace serves one stream at a
- *                   time.
+ *                   argument, no initial contents needed; one workspace serves
+ *                   one stream at a time.
  * Returns QKVF_ERR_NULL / _ALIGN / _SIZES / _ARG for a missing, misaligned,
- * short or overlapping workspace, else as attn2.  Launched with PDL.
+ * short or overlapping workspace, else as attn2.
  */
 int attn2_split_kv(const uint16_t *qkv, const uint16_t *kv_cache, int64_t num_pages,
                    const int32_t *block_table, int max_blocks, const int32_t *context_lens, int num_reqs,
                    int N, int num_kv_heads, int window, float scale, float eps, uint16_t *out, int splits,
                    void *workspace, size_t workspace_bytes, void *stream);
 
-/* Workspace bytes attn2_split_kv needs (0 on bad input): the counters, then
- * num_reqs * num_kv_heads * splits slots of 17152 bytes. */
+/* Workspace bytes attn2_split_kv needs (0 on bad input): num_reqs *
+ * num_kv_heads * splits slots of 17152 bytes. */
 size_t attn2_split_kv_workspace_bytes(int num_reqs, int num_kv_heads, int splits);
 
 /* The split attn2_split_kv picks for splits == 0 on the current device: the

@@ -92,7 +92,6 @@ __host__ __device__ inline A2Layout a2_layout()
 struct Attn2Params {
     const uint16_t *qkv;
     float *ws;               // split-KV partials (workspace engine), else null
-    unsigned int *counters;  // one arrival counter per (request, KV head), workspace engine
     const int32_t *block_table;
     const int32_t *context_lens;
     uint16_t *out;
@@ -179,8 +178,8 @@ __device__ __forceinline__ void a2_finish_row(const Attn2Params &p, int r, int g
 
 // kWorkspace = false: the S CTAs of (request, KV head) form a cluster and merge
 // over distributed shared memory.  true: no cluster; each CTA writes its
-// partial to a slot of the caller's workspace and the last of the S to arrive
-// (an atomic counter) merges the S slots in split order and resets the counter.
+// partial to its slot of the caller's workspace and attn2_merge_kernel, the
+// next grid on the stream, merges the S slots.
 template <bool kWorkspace>
 __global__ void __launch_bounds__(kA2Threads, 1)
     attn2_kernel(const __grid_constant__ CUtensorMap tmKV, const Attn2Params p)
@@ -510,11 +509,9 @@ __global__ void __launch_bounds__(kA2Threads, 1)
     }
     __syncthreads();
     if constexpr (kWorkspace) {
-        // ---- publish this CTA's partial; the last of the S merges them ----
-        __shared__ int s_last;
+        // ---- publish this CTA's partial: O [64][64], m, l, the bad-entry flag ----
         const int tid = threadIdx.x;
-        const size_t pair = (size_t)r * p.nkv + g;
-        float *slot = p.ws + (pair * S + z) * kA2WsSlotFloats;
+        float *slot = p.ws + (((size_t)r * p.nkv + g) * S + z) * kA2WsSlotFloats;
         for (int it = tid; it < 64 * 16; it += kA2Threads) {
             const int row = it >> 4, c4 = it & 15;
             __stcg(reinterpret_cast<float4 *>(slot + row * 64 + 4 * c4),
@@ -525,48 +522,6 @@ __global__ void __launch_bounds__(kA2Threads, 1)
             __stcg(slot + 4160 + tid, l_part[tid]);
         }
         if (tid == 0) __stcg(reinterpret_cast<int *>(slot + 4224), s_flags[1]);
-        __threadfence();
-        __syncthreads();
-        if (tid == 0) s_last = atomicAdd(p.counters + pair, 1u) == (unsigned)(S - 1);
-        __syncthreads();
-        if (!s_last) return;
-        __threadfence();   // the other CTAs' slots, published before their arrivals
-        if (tid == 0) p.counters[pair] = 0u;   // every CTA of this launch has arrived
-        const float *slots = p.ws + pair * S * kA2WsSlotFloats;
-        unsigned bad = 0u;
-        for (int src = lane; src < S; src += 32)
-            bad |= (unsigned)__ldcg(reinterpret_cast<const int *>(slots + (size_t)src * kA2WsSlotFloats + 4224));
-        if (!req_ok || __any_sync(0xffffffffu, bad != 0u)) return;
-        for (int row = warp; row < 64; row += kA2ComputeWarps + 1) {
-            float M = -INFINITY;
-            for (int src = 0; src < S; ++src)
-                M = fmaxf(M, __ldcg(slots + (size_t)src * kA2WsSlotFloats + 4096 + row));
-            const float base = M == -INFINITY ? 0.f : M;
-            float lt = 0.f, o0 = 0.f, o1 = 0.f;
-            for (int s0 = 0; s0 < S; s0 += 8) {   // 8 slots' loads in flight, summed in split order
-                float mk[8], lk[8];
-                float2 ov[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    if (s0 + j < S) {
-                        const float *sl = slots + (size_t)(s0 + j) * kA2WsSlotFloats;
-                        mk[j] = __ldcg(sl + 4096 + row);
-                        lk[j] = __ldcg(sl + 4160 + row);
-                        ov[j] = __ldcg(reinterpret_cast<const float2 *>(sl + row * 64 + 2 * lane));
-                    }
-                }
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    if (s0 + j < S) {
-                        const float w = exp2f(mk[j] - base);
-                        lt = lt + lk[j] * w;
-                        o0 = o0 + ov[j].x * w;
-                        o1 = o1 + ov[j].y * w;
-                    }
-                }
-            }
-            a2_finish_row(p, r, g, row, o0, o1, lt, lane);
-        }
     } else {
         if (S > 1) cluster_sync_all();
 
@@ -625,6 +580,79 @@ __global__ void __launch_bounds__(kA2Threads, 1)
         }
         if (S > 1) cluster_sync_all();   // no CTA leaves while its partials may still be read
     }
+}
+
+// Merge of the split-KV engine, the grid after attn2_kernel<true> on the
+// stream: one warp per output row of (request, KV head).  Lane l holds the
+// maxima and sums of splits l, l + 32, ...; the row's maximum and sum are warp
+// reductions in a fixed order; O is summed over the splits in split order,
+// 32 splits' loads in flight per batch; then o-norm, gate, store.
+constexpr int kA2MergeWarps = 8;
+
+__global__ void __launch_bounds__(32 * kA2MergeWarps) attn2_merge_kernel(const Attn2Params p)
+{
+    __shared__ float w_sh[kA2MergeWarps][kA2WsMaxSplits];
+    if (threadIdx.x == 0) griddep_launch_dependents();
+    griddep_wait();   // the partials (and, transitively, q and the gate) are written
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row = blockIdx.x * kA2MergeWarps + warp, g = blockIdx.y, r = blockIdx.z;
+    const int S = p.splits;
+    const int L = p.context_lens[r];
+    if (L < 8 || (L + kPageSlots - 1) / kPageSlots > p.max_blocks) return;
+    const float *slots = p.ws + ((size_t)r * p.nkv + g) * S * kA2WsSlotFloats;
+    constexpr int kPer = kA2WsMaxSplits / 32;
+    float ml[kPer], ll[kPer];
+    unsigned bad = 0u;
+    float M = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        const int src = lane + 32 * j;
+        ml[j] = -INFINITY;
+        ll[j] = 0.f;
+        if (src < S) {
+            const float *sl = slots + (size_t)src * kA2WsSlotFloats;
+            ml[j] = __ldcg(sl + 4096 + row);
+            ll[j] = __ldcg(sl + 4160 + row);
+            bad |= (unsigned)__ldcg(reinterpret_cast<const int *>(sl + 4224));
+        }
+    }
+    if (__any_sync(0xffffffffu, bad != 0u)) return;   // a page outside the cache: rows skipped
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) M = fmaxf(M, ml[j]);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    const float base = M == -INFINITY ? 0.f : M;
+    float lt = 0.f;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        const int src = lane + 32 * j;
+        if (src < S) {
+            const float w = exp2f(ml[j] - base);
+            w_sh[warp][src] = w;
+            lt = lt + ll[j] * w;
+        }
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) lt += __shfl_xor_sync(0xffffffffu, lt, off);
+    __syncwarp();
+    float o0 = 0.f, o1 = 0.f;
+    for (int s0 = 0; s0 < S; s0 += 32) {
+        float2 v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (s0 + j < S)
+                v[j] = __ldcg(reinterpret_cast<const float2 *>(slots + (size_t)(s0 + j) * kA2WsSlotFloats +
+                                                               row * 64 + 2 * lane));
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            if (s0 + j < S) {
+                const float w = w_sh[warp][s0 + j];
+                o0 = o0 + v[j].x * w;
+                o1 = o1 + v[j].y * w;
+            }
+        }
+    }
+    a2_finish_row(p, r, g, row, o0, o1, lt, lane);
 }
 
 int encode_kv_map(const uint16_t *kv_cache, int64_t num_pages, int nkv, CUtensorMap *m)
@@ -716,16 +744,11 @@ int attn2_split_kv_splits_for(int num_reqs, int nkv, int max_blocks, int window,
     return s < 1 ? 1 : (int)s;
 }
 
-// Workspace of the split-KV engine: one 32-bit arrival counter per (request,
-// KV head), padded to 256 bytes, then R * nkv * S partial slots of 17152 bytes.
-size_t a2_counter_bytes(int num_reqs, int nkv)
-{
-    return ((size_t)num_reqs * nkv * 4 + 255) / 256 * 256;
-}
-
+// Workspace of the split-KV engine: R * nkv * S partial slots of 17152 bytes
+// (O [64][64], the 64 row maxima and sums, the bad-entry flag; FP32).
 size_t a2_workspace_bytes(int num_reqs, int nkv, int splits)
 {
-    return a2_counter_bytes(num_reqs, nkv) + (size_t)num_reqs * nkv * splits * kA2WsSlotFloats * 4;
+    return (size_t)num_reqs * nkv * splits * kA2WsSlotFloats * 4;
 }
 
 bool prepare_attn2_kernel()
@@ -752,10 +775,7 @@ int launch_attn2(const uint16_t *qkv, const uint16_t *kv_cache, int64_t num_page
     const bool ws = workspace != nullptr;
     Attn2Params prm;
     prm.qkv = qkv;
-    prm.counters = ws ? static_cast<unsigned int *>(workspace) : nullptr;
-    prm.ws = ws ? reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
-                                            a2_counter_bytes(num_reqs, num_kv_heads))
-                : nullptr;
+    prm.ws = static_cast<float *>(workspace);
     prm.block_table = block_table;
     prm.context_lens = context_lens;
     prm.out = out;
@@ -787,8 +807,20 @@ int launch_attn2(const uint16_t *qkv, const uint16_t *kv_cache, int64_t num_page
     ++na;
     cfg.attrs = attrs;
     cfg.numAttrs = (unsigned)na;
-    const cudaError_t e = ws ? cudaLaunchKernelEx(&cfg, attn2_kernel<true>, m, prm)
-                             : cudaLaunchKernelEx(&cfg, attn2_kernel<false>, m, prm);
+    cudaError_t e = ws ? cudaLaunchKernelEx(&cfg, attn2_kernel<true>, m, prm)
+                       : cudaLaunchKernelEx(&cfg, attn2_kernel<false>, m, prm);
+    if (e == cudaSuccess && ws) {   // the merge, PDL-linked behind the partials
+        cudaLaunchConfig_t mc = {};
+        mc.gridDim = dim3(64 / kA2MergeWarps, (unsigned)num_kv_heads, (unsigned)num_reqs);
+        mc.blockDim = dim3(32 * kA2MergeWarps, 1, 1);
+        mc.stream = (cudaStream_t)stream;
+        cudaLaunchAttribute ma;
+        ma.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        ma.val.programmaticStreamSerializationAllowed = g_pdl ? 1 : 0;
+        mc.attrs = &ma;
+        mc.numAttrs = 1;
+        e = cudaLaunchKernelEx(&mc, attn2_merge_kernel, prm);
+    }
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         return QKVF_ERR_CUDA;

@@ -454,8 +454,8 @@ def attn2_split_kv_splits(num_reqs: int, num_kv_heads: int, max_blocks: int, win
 def attn2_split_kv(qkv, kv_cache, block_table, context_lens, workspace, out=None, window: int = 0,
                    scale: float = 0.125, eps: float = 1e-6, splits: int = 0, stream=None):
     """attn2 with the split-KV engine: partials in `workspace` (a uint8 CUDA
-    tensor of at least attn2_split_kv_workspace_bytes bytes, zero-filled
-    before its first use; every call leaves its counters zero)."""
+    tensor of at least attn2_split_kv_workspace_bytes bytes), merged by a
+    second grid."""
     out, args = _attn2_args(qkv, kv_cache, block_table, context_lens, out, window, scale, eps)
     if (not workspace.is_cuda or workspace.dtype != torch.uint8 or not workspace.is_contiguous()
             or workspace.device != qkv.device):

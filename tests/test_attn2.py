@@ -148,16 +148,14 @@ def test_decode_layer_front_then_attn2():
     assert_values(wl.bits(o.cpu()), o_chain, what="front + attn2 vs the oracle chain")
 
 
-# ---- the split-KV engine: partials in a caller's workspace, last CTA merges ----
+# ---- the split-KV engine: partials in a caller's workspace, a second grid merges ----
 
 def _workspace(R, nkv, splits):
+    """A workspace of the size asked for, filled with NaN bytes: the engine
+    needs no initial contents."""
     n = qf.attn2_split_kv_workspace_bytes(R, nkv, splits)
     assert n > 0
-    return torch.zeros(n, dtype=torch.uint8, device="cuda:0")
-
-
-def _counters_zero(ws, R, nkv):
-    return int(ws[:R * nkv * 4].view(torch.int32).abs().sum()) == 0
+    return torch.full((n,), 0xFF, dtype=torch.uint8, device="cuda:0")
 
 
 @pytest.mark.parametrize("name", list(wl.ATTN_WORKLOADS))
@@ -172,7 +170,6 @@ def test_attn2_split_kv_workloads_match_oracle(name):
                             window=w.window)
     torch.cuda.synchronize()
     assert qf.status() == 0
-    assert _counters_zero(ws, w.R, w.num_kv_heads)
     ref, err = _oracle(inp, w)
     assert err == 0
     assert_values(wl.bits(out.cpu()), ref, what=f"attn2 split-KV {name} S={S}")
@@ -182,7 +179,7 @@ def test_attn2_split_kv_workloads_match_oracle(name):
 @pytest.mark.parametrize("name", ["attn_r3_mixed_nkv2", "attn_r2_window_nkv8"])
 def test_attn2_split_kv_every_split(name, splits):
     """Any split, including more CTAs than pages (empty partials), matches the
-    oracle, repeats bitwise, and leaves the counters at zero."""
+    oracle and repeats bitwise."""
     w = wl.ATTN_WORKLOADS[name]
     inp = wl.make_attn_inputs(w)
     g = _dev(inp)
@@ -193,7 +190,6 @@ def test_attn2_split_kv_every_split(name, splits):
                                       ws, window=w.window, splits=splits).clone())
     torch.cuda.synchronize()
     assert qf.status() == 0
-    assert _counters_zero(ws, w.R, w.num_kv_heads)
     assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
     ref, _ = _oracle(inp, w)
     assert_values(wl.bits(outs[0].cpu()), ref, what=f"attn2 split-KV {name} S={splits}")
@@ -227,7 +223,6 @@ def test_attn2_split_kv_bad_requests_skipped_and_flagged():
                       splits=3)
     torch.cuda.synchronize()
     assert qf.status() == qf.STATUS_BAD_REQUEST
-    assert _counters_zero(ws, w.R, 1)
     got = wl.bits(out.cpu())
     assert np.all(got[:16] == wl.bits(torch.tensor([7.0]).to(torch.bfloat16))[0])
     ref, _ = _oracle(inp, w)

@@ -224,8 +224,8 @@ def test_attn2_split_kv_refusals(lib):
     misaligned, short or overlapping workspace and a bad split are refused."""
     WS = 1 << 44
     need = lib.attn2_split_kv_workspace_bytes(2, 2, 3)
-    assert need == 256 + 2 * 2 * 3 * 17152          # counters padded to 256 B, then the slots
-    assert lib.attn2_split_kv_workspace_bytes(1, 1, 1) == 256 + 17152
+    assert need == 2 * 2 * 3 * 17152                # one slot per (request, KV head, split)
+    assert lib.attn2_split_kv_workspace_bytes(1, 1, 1) == 17152
     assert lib.attn2_split_kv_workspace_bytes(0, 2, 3) == 0
     assert lib.attn2_split_kv_workspace_bytes(1, 1, 257) == 0
     assert lib.attn2_split_kv_workspace_bytes(1, 65, 1) == 0
