@@ -150,15 +150,23 @@ __device__ __forceinline__ uint32_t pack_f2bf(float lo, float hi)
     return pack_bf16x2(__float2bfloat16_rn(lo), __float2bfloat16_rn(hi));
 }
 
+// The gate values at dims 2 lane, 2 lane + 1 of output row `row` of
+// (request r, KV head g): gate head 8 g + row % 8 of token row / 8.
+__device__ __forceinline__ __nv_bfloat162 a2_gate(const Attn2Params &p, int r, int g, int row, int lane)
+{
+    const int gate_col = kQPerKv * p.nkv * kHeadDim + 2 * p.nkv * kHeadDim;
+    const size_t qrow = (size_t)r * 8 + (row >> 3);
+    return *reinterpret_cast<const __nv_bfloat162 *>(p.qkv + qrow * p.N + gate_col +
+                                                    (size_t)(8 * g + (row & 7)) * kHeadDim + 2 * lane);
+}
+
 // One output row of (request r, KV head g): o = (o0, o1) at dims 2 lane,
 // 2 lane + 1 and its softmax sum lt -> 1/lt, o-norm over the 64 dims (warp
-// butterfly), sigmoid gate of the row's gate head, bf16 store.
+// butterfly), sigmoid gate gt of the row's gate head, bf16 store.
 __device__ __forceinline__ void a2_finish_row(const Attn2Params &p, int r, int g, int row, float o0,
-                                              float o1, float lt, int lane)
+                                              float o1, float lt, int lane, __nv_bfloat162 gt)
 {
-    const int q_heads = kQPerKv * p.nkv;
-    const int gate_col = q_heads * kHeadDim + 2 * p.nkv * kHeadDim;
-    const int out_cols = q_heads * kHeadDim;
+    const int out_cols = kQPerKv * p.nkv * kHeadDim;
     const float inv = lt > 0.f ? 1.0f / lt : 0.f;
     o0 *= inv;
     o1 *= inv;
@@ -168,8 +176,6 @@ __device__ __forceinline__ void a2_finish_row(const Attn2Params &p, int r, int g
     const float rn = 1.0f / sqrtf(ss * (1.0f / kHeadDim) + p.eps);
     const int tok = row >> 3, hj = 8 * g + (row & 7);
     const size_t qrow = (size_t)r * 8 + tok;
-    const __nv_bfloat162 gt = *reinterpret_cast<const __nv_bfloat162 *>(
-        p.qkv + qrow * p.N + gate_col + (size_t)hj * kHeadDim + 2 * lane);
     const float s0 = 1.0f / (1.0f + expf(-__low2float(gt)));
     const float s1 = 1.0f / (1.0f + expf(-__high2float(gt)));
     reinterpret_cast<uint32_t *>(p.out + qrow * out_cols + (size_t)hj * kHeadDim)[lane] =
@@ -543,6 +549,7 @@ __global__ void __launch_bounds__(kA2Threads, 1)
             const uint32_t o_addr = smem_u32(o_part), m_addr = smem_u32(m_part), l_addr = smem_u32(l_part);
             for (int i = warp; i < rows; i += kA2ComputeWarps + 1) {
                 const int row = (int)z * rows + i;
+                const __nv_bfloat162 gt = a2_gate(p, r, g, row, lane);
                 // the ranks' partials in rank order; all remote loads issued first
                 float mk[kA2MaxSplits], lk[kA2MaxSplits];
                 float2 ov[kA2MaxSplits];
@@ -575,7 +582,7 @@ __global__ void __launch_bounds__(kA2Threads, 1)
                         o1 = o1 + ov[src].y * w;
                     }
                 }
-                a2_finish_row(p, r, g, row, o0, o1, lt, lane);
+                a2_finish_row(p, r, g, row, o0, o1, lt, lane, gt);
             }
         }
         if (S > 1) cluster_sync_all();   // no CTA leaves while its partials may still be read
@@ -597,13 +604,14 @@ __global__ void __launch_bounds__(32 * kA2MergeWarps) attn2_merge_kernel(const A
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int row = blockIdx.x * kA2MergeWarps + warp, g = blockIdx.y, r = blockIdx.z;
     const int S = p.splits;
-    const int L = p.context_lens[r];
-    if (L < 8 || (L + kPageSlots - 1) / kPageSlots > p.max_blocks) return;
     const float *slots = p.ws + ((size_t)r * p.nkv + g) * S * kA2WsSlotFloats;
+    // every load of the row first: the length, the gate, the splits' maxima,
+    // sums and flags, and the first 32 splits' O
+    const int L = p.context_lens[r];
+    const __nv_bfloat162 gt = a2_gate(p, r, g, row, lane);
     constexpr int kPer = kA2WsMaxSplits / 32;
     float ml[kPer], ll[kPer];
     unsigned bad = 0u;
-    float M = -INFINITY;
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
         const int src = lane + 32 * j;
@@ -616,7 +624,14 @@ __global__ void __launch_bounds__(32 * kA2MergeWarps) attn2_merge_kernel(const A
             bad |= (unsigned)__ldcg(reinterpret_cast<const int *>(sl + 4224));
         }
     }
-    if (__any_sync(0xffffffffu, bad != 0u)) return;   // a page outside the cache: rows skipped
+    float2 v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+        if (j < S)
+            v[j] = __ldcg(reinterpret_cast<const float2 *>(slots + (size_t)j * kA2WsSlotFloats + row * 64 + 2 * lane));
+    if (L < 8 || (L + kPageSlots - 1) / kPageSlots > p.max_blocks) return;   // a bad request: rows skipped
+    if (__any_sync(0xffffffffu, bad != 0u)) return;                          // a page outside the cache
+    float M = -INFINITY;
 #pragma unroll
     for (int j = 0; j < kPer; ++j) M = fmaxf(M, ml[j]);
 #pragma unroll
@@ -637,12 +652,13 @@ __global__ void __launch_bounds__(32 * kA2MergeWarps) attn2_merge_kernel(const A
     __syncwarp();
     float o0 = 0.f, o1 = 0.f;
     for (int s0 = 0; s0 < S; s0 += 32) {
-        float2 v[32];
+        if (s0 > 0) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-            if (s0 + j < S)
-                v[j] = __ldcg(reinterpret_cast<const float2 *>(slots + (size_t)(s0 + j) * kA2WsSlotFloats +
-                                                               row * 64 + 2 * lane));
+            for (int j = 0; j < 32; ++j)
+                if (s0 + j < S)
+                    v[j] = __ldcg(reinterpret_cast<const float2 *>(slots + (size_t)(s0 + j) * kA2WsSlotFloats +
+                                                                   row * 64 + 2 * lane));
+        }
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
             if (s0 + j < S) {
@@ -652,7 +668,7 @@ __global__ void __launch_bounds__(32 * kA2MergeWarps) attn2_merge_kernel(const A
             }
         }
     }
-    a2_finish_row(p, r, g, row, o0, o1, lt, lane);
+    a2_finish_row(p, r, g, row, o0, o1, lt, lane, gt);
 }
 
 int encode_kv_map(const uint16_t *kv_cache, int64_t num_pages, int nkv, CUtensorMap *m)
