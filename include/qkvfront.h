@@ -299,6 +299,29 @@ size_t attn2_split_kv_workspace_bytes(int num_reqs, int num_kv_heads, int splits
  * each split keeps two or more of the pages a row can see; 0 on bad input. */
 int attn2_split_kv_splits(int num_reqs, int num_kv_heads, int max_blocks, int window);
 
+/*
+ * attn2_split_kv for callers that cannot allocate device memory: a plugin
+ * whose host process owns every device allocation through its own pool, or
+ * a decode step that must not risk cudaMalloc's implicit synchronisation or
+ * a failed allocation mid-step.  The paper has no counterpart of this entry
+ * point.  Same arguments and result as attn2_split_kv without the workspace:
+ * the partials go to a file-scope device array of the library, 256 slots of
+ * 17152 bytes (4,390,912 bytes), which every GPU that loads the library holds
+ * until the process exits.  The call allocates nothing.
+ *   num_reqs * num_kv_heads * splits (after splits == 0 is resolved as
+ *   attn2_split_kv_splits does) must be <= 256, else QKVF_ERR_SIZES.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  The array needs no clearing: a call reads only slots it wrote.
+ * Every call shares it, so calls that overlap on the GPU (other streams,
+ * other host threads) race; run them one after another.
+ */
+int attn2_split_kv_noalloc(const uint16_t *qkv, const uint16_t *kv_cache, int64_t num_pages,
+                           const int32_t *block_table, int max_blocks, const int32_t *context_lens,
+                           int num_reqs, int N, int num_kv_heads, int window, float scale, float eps,
+                           uint16_t *out, int splits, void *stream);
+
+
 /* Static text of a QKVF_* return code. */
 const char *qkv_front_strerror(int code);
 

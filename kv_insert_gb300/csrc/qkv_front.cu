@@ -1271,3 +1271,79 @@ int qkv_front_set_wait_limit(int64_t ns)
 }
 
 }  // extern "C"
+
+// ---- attn2 split-KV without a caller's workspace ---------------------------
+//
+// For callers that cannot allocate device memory themselves: a plugin whose
+// host process owns every device allocation through its own pool, or a
+// decode step that must not risk cudaMalloc's implicit synchronisation or a
+// failed allocation halfway through.  Their split-KV partials go to one
+// file-scope array that every GPU loading this library holds until exit
+// (256 slots of 17152 bytes, 4.39 MB).  The engine reads no slot it has not
+// written in the same call, so the array needs no clearing between calls;
+// calls that overlap on the GPU share it and race.
+
+namespace qkvf {
+
+constexpr int kNoAllocSlots = 256;
+constexpr size_t kNoAllocBytes = (size_t)kNoAllocSlots * kA2WsSlotFloats * 4;
+static __device__ __align__(256) float g_a2_noalloc_scratch[(size_t)kNoAllocSlots * kA2WsSlotFloats];
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void *g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+// The array's device address on the current device (host code only sees a
+// stand-in under its name), looked up once per device.
+int noalloc_scratch(void **ptr)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) {
+        (void)cudaGetLastError();
+        return QKVF_ERR_DEVICE;
+    }
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_a2_noalloc_scratch) != cudaSuccess || !p) {
+            (void)cudaGetLastError();
+            return QKVF_ERR_CUDA;
+        }
+        g_noalloc_ptr[dev] = p;
+    }
+    *ptr = g_noalloc_ptr[dev];
+    return QKVF_OK;
+}
+
+}  // namespace qkvf
+
+extern "C" {
+
+int attn2_split_kv_noalloc(const uint16_t *qkv, const uint16_t *kv_cache, int64_t num_pages,
+                           const int32_t *block_table, int max_blocks, const int32_t *context_lens,
+                           int num_reqs, int N, int num_kv_heads, int window, float scale, float eps,
+                           uint16_t *out, int splits, void *stream)
+{
+    int code;
+    if (qkvf::check_attn2_args(qkv, kv_cache, num_pages, block_table, max_blocks, context_lens,
+                               num_reqs, N, num_kv_heads, window, scale, eps, out, &code))
+        return code;
+    if (splits < 0 || splits > qkvf::kA2WsMaxSplits) return QKVF_ERR_VARIANT;
+    if (num_reqs == 0) return QKVF_OK;
+    if (splits > 0 && (int64_t)num_reqs * num_kv_heads * splits > qkvf::kNoAllocSlots)
+        return QKVF_ERR_SIZES;   // more partial slots than the array holds
+    qkvf::DeviceState *d;
+    int rc = qkvf::probe_device(&d);
+    if (rc != QKVF_OK) return rc;
+    if (splits == 0)
+        splits = qkvf::attn2_split_kv_splits_for(num_reqs, num_kv_heads, max_blocks, window, d->sms);
+    if ((int64_t)num_reqs * num_kv_heads * splits > qkvf::kNoAllocSlots) return QKVF_ERR_SIZES;
+    void *scratch = nullptr;
+    rc = qkvf::noalloc_scratch(&scratch);
+    if (rc != QKVF_OK) return rc;
+    return attn2_split_kv(qkv, kv_cache, num_pages, block_table, max_blocks, context_lens, num_reqs, N,
+                          num_kv_heads, window, scale, eps, out, splits, scratch, qkvf::kNoAllocBytes,
+                          stream);
+}
+
+}  // extern "C"

@@ -111,6 +111,8 @@ def load() -> ctypes.CDLL:
         lib.attn2_split_kv_workspace_bytes.restype = ctypes.c_size_t
         lib.attn2_split_kv_splits.argtypes = [i32, i32, i32, i32]
         lib.attn2_split_kv_splits.restype = i32
+        lib.attn2_split_kv_noalloc.argtypes = a2 + [i32, vp]
+        lib.attn2_split_kv_noalloc.restype = i32
         lib.qkv_front_set_pdl.argtypes = [i32]
         lib.qkv_front_set_pdl.restype = i32
         _lib = lib
@@ -449,6 +451,18 @@ def attn2_split_kv_workspace_bytes(num_reqs: int, num_kv_heads: int, splits: int
 
 def attn2_split_kv_splits(num_reqs: int, num_kv_heads: int, max_blocks: int, window: int = 0) -> int:
     return int(load().attn2_split_kv_splits(num_reqs, num_kv_heads, max_blocks, window))
+
+
+def attn2_split_kv_noalloc(qkv, kv_cache, block_table, context_lens, out=None, window: int = 0,
+                           scale: float = 0.125, eps: float = 1e-6, splits: int = 0, stream=None):
+    """attn2_split_kv for callers that cannot allocate device memory: the
+    partials go to the library's own device array (256 slots; more raises
+    QkvFrontError with QKVF_ERR_SIZES).  Pass `out` to keep the call free of
+    allocations: with out=None this wrapper allocates the output with torch."""
+    out, args = _attn2_args(qkv, kv_cache, block_table, context_lens, out, window, scale, eps)
+    with torch.cuda.device(qkv.device):
+        _check(load().attn2_split_kv_noalloc(*args, int(splits), _stream(stream)))
+    return out
 
 
 def attn2_split_kv(qkv, kv_cache, block_table, context_lens, workspace, out=None, window: int = 0,

@@ -1,0 +1,61 @@
+"""attn2_split_kv_noalloc: split-KV attention for callers that cannot
+allocate device memory themselves — a plugin whose host process owns every
+device allocation through its own pool, or a decode step that must not risk
+cudaMalloc's implicit synchronisation or a failed allocation mid-step.  Its
+partials live in the library's own device array instead of a caller's
+workspace.  Checked through the C ABI against attn2_split_kv with a caller's
+workspace, on two calls in a row.  This file is collected last, so a run that
+stops at its first failure has already run every other test."""
+import pytest
+import torch
+
+from kv_insert_gb300 import qkv_front as qf
+from kv_insert_gb300 import workloads as wl
+
+from _parity import assert_values
+
+SLOTS = 256   # partial slots in the library's array: num_reqs * num_kv_heads * splits
+
+
+@pytest.fixture(scope="module")
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+    return qf.load()
+
+
+def test_noalloc_refuses_more_slots_than_its_array(built):
+    """Sizes beyond the array are refused on the host, before any launch
+    (explicit splits need no device query)."""
+    lib = built
+    X, CACHE, POS, SL, OUT = ((i + 1) << 36 for i in range(5))
+    # 2 requests x 2 KV heads x 65 splits = 260 slots > 256
+    assert lib.attn2_split_kv_noalloc(X, CACHE, 64, POS, 8, SL, 2, 2304, 2, 0, 0.125, 1e-6, OUT, 65,
+                                      None) == 7
+    assert lib.attn2_split_kv_noalloc(X, CACHE, 64, POS, 8, SL, 2, 2304, 2, 0, 0.125, 1e-6, OUT, 257,
+                                      None) == 8
+    assert lib.attn2_split_kv_noalloc(0, CACHE, 64, POS, 8, SL, 2, 2304, 2, 0, 0.125, 1e-6, OUT, 1,
+                                      None) == 3
+
+
+@pytest.mark.gpu
+def test_noalloc_matches_the_workspace_engine_two_calls_in_a_row(built):
+    """Call 1: one 32K request, 8 KV heads, the library's split (152 slots).
+    Call 2: three mixed requests at 5 splits, on other inputs, over whatever
+    call 1 left in the array.  Each against attn2_split_kv at the same split
+    with a caller's workspace, within the parity tolerance of the other tests."""
+    for name, splits in (("attn_r1_l32k_nkv8", 0), ("attn_r3_mixed_nkv2", 5)):
+        w = wl.ATTN_WORKLOADS[name]
+        g = {k: v.to("cuda:0") for k, v in wl.make_attn_inputs(w).items()}
+        S = splits or qf.attn2_split_kv_splits(w.R, w.num_kv_heads, w.max_blocks(), w.window)
+        assert 1 <= w.R * w.num_kv_heads * S <= SLOTS
+        out = torch.empty(8 * w.R, 512 * w.num_kv_heads, dtype=torch.bfloat16, device="cuda:0")
+        qf.attn2_split_kv_noalloc(g["qkv"], g["kv_cache"], g["block_table"], g["context_lens"],
+                                  out=out, window=w.window, splits=splits)
+        ws = torch.zeros(qf.attn2_split_kv_workspace_bytes(w.R, w.num_kv_heads, S), dtype=torch.uint8,
+                         device="cuda:0")
+        ref = qf.attn2_split_kv(g["qkv"], g["kv_cache"], g["block_table"], g["context_lens"], ws,
+                                window=w.window, splits=S)
+        torch.cuda.synchronize()
+        assert qf.status() == 0
+        assert_values(wl.bits(out.cpu()), wl.bits(ref.cpu()), what=f"no-alloc attn2 {name} S={S}")
