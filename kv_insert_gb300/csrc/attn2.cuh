@@ -15,18 +15,22 @@
 // with o = softmax(scale q K^T) V.
 //
 // Design: a CTA per (request r, KV head g, split z).  A producer warp streams
-// the CTA's pages (p0 + z, p0 + z + S, ...) into a ring, one TMA box per page
-// (16 K rows then 16 V rows of 64, 128-byte swizzle), blocks of 4 pages
+// the CTA's pages (p0 + z, p0 + z + S, ...) into a ring of blocks of 4 pages
+// (the block's 64 K rows, then its 64 V rows, 128-byte swizzled TMA boxes)
 // sharing one full / empty barrier pair.  Groups of four compute warps
-// (16 of the 64 query rows each — 8 tokens x 8 heads, row 8 i + j — held in
-// registers as mma.sync A fragments) take blocks of 4 pages in turn and run
-// QK^T, the online softmax (base 2; masks only near the causal / window
-// edges) and PV with mma.sync, P going from the S accumulators straight into
-// the A fragments.  Each group keeps its own (max, sum, O), folded into one
-// per CTA in group order; the S CTAs of a (request, KV head) form a cluster
-// and merge their partials through distributed shared memory in rank order —
-// no global workspace, deterministic for a launch shape — then each rank
-// finishes 64 / S rows: o-norm, gate, BF16 store.
+// (16 of the 64 query rows each — 8 tokens x 8 heads, row 8 i + j) take
+// blocks of 4 pages in turn: one thread of the group issues Q K^T for the
+// block's 64 keys as four tcgen05.mma (M = 64 rows, N = 64 keys, K = 16)
+// into the group's 64 tensor-memory columns, the warps read the scores back
+// with tcgen05.ld in the mma.sync accumulator layout, run the online softmax
+// (base 2; masks only near the causal / window edges) and P V with mma.sync,
+// P going from the score registers straight into the A fragments.  Each
+// group keeps its own (max, sum, O), folded into one per CTA in group order.
+// Cluster engine: the S CTAs of a (request, KV head) form a cluster and merge
+// their partials through distributed shared memory in rank order — no global
+// workspace, deterministic for a launch shape — then each rank finishes 64 / S
+// rows: o-norm, gate, BF16 store.  Split-KV engine: no cluster; the partials
+// go to a caller's workspace and a second grid merges them.
 
 #ifndef A2_GROUPS
 #define A2_GROUPS 3
@@ -37,6 +41,9 @@
 #ifndef A2_BLOCK
 #define A2_BLOCK 4
 #endif
+#ifndef A2_TC_QK
+#define A2_TC_QK 1   // 0: Q K^T with mma.sync + ldmatrix of K (2 - 3 % slower on GB300)
+#endif
 
 namespace qkvf {
 
@@ -44,12 +51,15 @@ constexpr int kA2Groups = A2_GROUPS;                      // groups of 4 compute
 constexpr int kA2ComputeWarps = 4 * kA2Groups;
 constexpr int kA2Threads = 32 * (kA2ComputeWarps + 1);   // the last warp produces
 constexpr int kA2Block = A2_BLOCK;                        // pages per softmax step (16 per page)
+constexpr bool kA2TcQK = A2_TC_QK != 0;                   // Q K^T on tcgen05 (else mma.sync)
+constexpr int kA2TmemCols = 256;                          // one 64-column S tile per group
 constexpr int kA2RingBlocks = A2_RING_BLOCKS;
 constexpr int kA2Stages = kA2RingBlocks * kA2Block;       // pages in flight per CTA
 // ring slot k % stages always serves group (k / block) % groups: each group
 // waits on its own slots in order, so a full barrier's parity never aliases
 static_assert(kA2RingBlocks % kA2Groups == 0, "ring blocks must be a multiple of the groups");
 static_assert(32 % kA2Block == 0, "a block's table entries lie in one 32-entry chunk");
+static_assert(!kA2TcQK || (kA2Block == 4 && kA2Groups * 64 <= kA2TmemCols), "tcgen05 Q K^T: 64-key blocks");
 constexpr uint32_t kA2PageBytes = 4096;                   // K box + V box
 constexpr int kA2OStride = 68;                            // floats per row of the O partial
 constexpr int kA2MaxSplits = 16;
@@ -59,7 +69,7 @@ constexpr int kA2WsMaxSplits = 256;     // workspace engine: CTAs per (request, 
 constexpr int kA2WsSlotFloats = 64 * 64 + 64 + 64 + 64;   // O [64][64], m, l, flags: 17152 bytes
 
 struct A2Layout {
-    uint32_t q, ring, full, empty, o, m, l, flags, total;
+    uint32_t q, ring, full, empty, sbar, tslot, o, m, l, flags, total;
 };
 
 // the groups' O partials overlay the ring: written only once every page has
@@ -79,6 +89,10 @@ __host__ __device__ inline A2Layout a2_layout()
     off += kA2RingBlocks * 8;
     L.empty = off;
     off += kA2RingBlocks * 8;
+    L.sbar = off;   // per group: its Q K^T (tcgen05) is done
+    off += kA2Groups * 8;
+    L.tslot = off;  // tensor-memory base address
+    off += 8;
     L.m = off;
     off += kA2Groups * 64 * 4;
     L.l = off;
@@ -134,6 +148,43 @@ __device__ __forceinline__ void a2_compute_bar_sync()
 __device__ __forceinline__ void a2_ring_done_sync()
 {
     asm volatile("bar.sync 3, %0;" ::"n"(kA2Threads) : "memory");
+}
+
+// named barrier 4 + grp over the 4 warps of compute group grp
+__device__ __forceinline__ void a2_group_bar_sync(int grp)
+{
+    asm volatile("bar.sync %0, 128;" ::"r"(4 + grp) : "memory");
+}
+
+__device__ __forceinline__ void a2_tmem_alloc(uint32_t slot_saddr)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_saddr),
+                 "n"(kA2TmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void a2_tmem_dealloc(uint32_t taddr)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "n"(kA2TmemCols)
+                 : "memory");
+}
+
+// 16 lanes x 64 consecutive 32-bit columns of tensor memory in the layout of
+// mma.sync accumulators: register 4 i + e of thread (gq = lane / 4, t = lane % 4)
+// holds lane taddr.lane + gq (+ 8 for e >= 2), column taddr.col + 8 i + 2 t + (e & 1).
+__device__ __forceinline__ void a2_tmem_ld_16x256b_x8(uint32_t taddr, uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+        "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+        "%30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+          "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+          "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
 }
 
 // 2^x for x <= 0 (softmax weights): the hardware approximation, subnormal
@@ -210,12 +261,18 @@ __global__ void __launch_bounds__(kA2Threads, 1)
             mbar_init(full0 + 8 * s, 1);
             mbar_init(empty0 + 8 * s, 4);   // the 4 warps of the group that owns the block
         }
+        if constexpr (kA2TcQK)
+            for (int q = 0; q < kA2Groups; ++q) mbar_init(smem_u32(smem + LY.sbar) + 8 * q, 1);
         s_flags[0] = 0;
         s_flags[1] = 0;
         fence_barrier_init();
         griddep_launch_dependents();
     }
+    if constexpr (kA2TcQK)
+        if (warp == 0) a2_tmem_alloc(smem_u32(smem + LY.tslot));
+    if constexpr (kA2TcQK) tc_fence_before();
     __syncthreads();
+    if constexpr (kA2TcQK) tc_fence_after();
     griddep_wait();   // q, the cache, the table and the lengths come from earlier kernels
 
     // ---- the request: length and visible pages ----------------------------
@@ -268,9 +325,12 @@ __global__ void __launch_bounds__(kA2Threads, 1)
                 }
                 const int b = c + lane - k0;   // this lane's page within the block
                 if (b >= 0 && b < nb) {
-                    const uint32_t dst = sRing + (uint32_t)(rb * kA2Block + b) * kA2PageBytes;
-                    // one box: the page's 16 K rows, then its 16 V rows
-                    tma_load_4d(dst, &tmKV, full0 + 8 * rb, 0, 0, 0, page * p.nkv + g);
+                    // the block's K rows together, then its V rows: 64 keys of
+                    // 128 bytes each, one operand for Q K^T
+                    const uint32_t blk = sRing + (uint32_t)rb * (kA2Block * kA2PageBytes);
+                    tma_load_4d(blk + (uint32_t)b * 2048, &tmKV, full0 + 8 * rb, 0, 0, 0, page * p.nkv + g);
+                    tma_load_4d(blk + (uint32_t)(kA2Block + b) * 2048, &tmKV, full0 + 8 * rb, 0, 0, 1,
+                                page * p.nkv + g);
                 }
                 ++issued;
             }
@@ -303,15 +363,26 @@ __global__ void __launch_bounds__(kA2Threads, 1)
                     p.qkv + ((size_t)r * 8 + (row >> 3)) * p.N + (size_t)(8 * g + (row & 7)) * kHeadDim + 8 * cc);
                 *reinterpret_cast<uint4 *>(smem + LY.q + row * 128 + ((cc ^ (row & 7)) << 4)) = v;
             }
+            if constexpr (kA2TcQK)   // the tensor cores read Q through the async proxy
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         }
         a2_compute_bar_sync();
         const int gq = lane >> 2, t = lane & 3;
-        uint32_t qa[4][4];   // the warp's 16 Q rows as mma A fragments
-        const uint32_t a_row = (uint32_t)(wig * 16 + (lane & 7) + ((lane >> 3) & 1) * 8);
+        uint32_t qa[4][4];   // the warp's 16 Q rows as mma A fragments (mma.sync Q K^T)
+        if constexpr (!kA2TcQK) {
+            const uint32_t a_row = (uint32_t)(wig * 16 + (lane & 7) + ((lane >> 3) & 1) * 8);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-            ldsm_x4(sQ + a_row * 128u + ((((uint32_t)(2 * kk) + (uint32_t)(lane >> 4)) ^ (uint32_t)(lane & 7)) << 4),
-                    qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+            for (int kk = 0; kk < 4; ++kk)
+                ldsm_x4(sQ + a_row * 128u + ((((uint32_t)(2 * kk) + (uint32_t)(lane >> 4)) ^ (uint32_t)(lane & 7)) << 4),
+                        qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+        }
+        // tcgen05 Q K^T: the group's S tile [64 rows x 64 keys] in tensor memory
+        // columns 64 grp.., rows 16 w .. 16 w + 15 in lanes 32 w .. 32 w + 15
+        const uint32_t sbar = smem_u32(smem + LY.sbar) + 8 * grp;
+        const uint32_t tS = kA2TcQK ? *reinterpret_cast<volatile uint32_t *>(smem + LY.tslot) + 64u * grp : 0u;
+        const bool issuer = wig == 0 && lane == 0;
+        uint32_t sph = 0;            // phase of sbar this block waits for
+        int committed = 0, observed = 0;   // the issuer's commits, and those it saw complete
 
         // this thread's rows: 16 wig + gq (token 2 wig) and 16 wig + gq + 8 (token 2 wig + 1)
         const int pos_a = L - 8 + 2 * wig, pos_b = pos_a + 1;
@@ -343,25 +414,56 @@ __global__ void __launch_bounds__(kA2Threads, 1)
                 const int key0 = (first_mine + (k0 + b) * S) * kPageSlots;
                 inside = inside && key0 >= edge_lo && key0 + kPageSlots - 1 <= edge_hi;
             }
-            const bool landed = mbar_try_wait(full0 + 8 * rb, ph) ||
-                                bounded_wait(full0 + 8 * rb, ph, s_flags, p.wait_limit_ns, true);
+            bool landed = mbar_try_wait(full0 + 8 * rb, ph) ||
+                          bounded_wait(full0 + 8 * rb, ph, s_flags, p.wait_limit_ns, true);
             inside = inside && nb == kA2Block;
+            const uint32_t kreg = sRing + (uint32_t)rb * (kA2Block * kA2PageBytes);   // the block's K rows
+            const uint32_t vreg = kreg + kA2Block * 2048;                            // then its V rows
+            if constexpr (kA2TcQK) {
+                // every warp of the group is past the previous block's tcgen05.ld
+                tc_fence_before();
+                a2_group_bar_sync(grp);
+                if (issuer && landed) {
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)   // K = 16 dims per instruction: 32 bytes along the rows
+                        umma_bf16(tS, umma_desc_sw128(sQ + 32u * kk), umma_desc_sw128(kreg + 32u * kk),
+                                  umma_idesc_bf16(64, 64), kk != 0 ? 1u : 0u);
+                    umma_commit(sbar);
+                    ++committed;
+                }
+                const bool s_ok = mbar_try_wait(sbar, sph) || bounded_wait(sbar, sph, s_flags, p.wait_limit_ns, true);
+                sph ^= 1u;
+                if (issuer && s_ok) observed = committed;
+                landed = landed && s_ok;
+            }
             if (__all_sync(0xffffffffu, landed)) {
                 float sc[2 * kA2Block][4];
+                if constexpr (kA2TcQK) {
+                    tc_fence_after();
+                    uint32_t rr[32];
+                    a2_tmem_ld_16x256b_x8(tS + ((uint32_t)(32 * wig) << 16), rr);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int nt = 0; nt < 2 * kA2Block; ++nt)
+                    for (int nt = 0; nt < 2 * kA2Block; ++nt)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) sc[nt][e] = 0.f;
+                        for (int e = 0; e < 4; ++e) sc[nt][e] = __uint_as_float(rr[4 * nt + e]);
+                } else {
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
+                    for (int nt = 0; nt < 2 * kA2Block; ++nt)
 #pragma unroll
-                    for (int b = 0; b < kA2Block; ++b) {
-                        if (b < nb) {
-                            const uint32_t kbox = sRing + (uint32_t)((k0 + b) % kA2Stages) * kA2PageBytes;
-                            uint32_t b0, b1, b2, b3;
-                            ldsm_x4(kbox + k_key * 128u + ((((uint32_t)(2 * kk) + k_hi) ^ sw) << 4), b0, b1, b2, b3);
-                            mma_bf16_16816(sc[2 * b], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
-                            mma_bf16_16816(sc[2 * b + 1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
+                        for (int e = 0; e < 4; ++e) sc[nt][e] = 0.f;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+                        for (int b = 0; b < kA2Block; ++b) {
+                            if (b < nb) {
+                                const uint32_t kbox = kreg + (uint32_t)b * 2048;
+                                uint32_t b0, b1, b2, b3;
+                                ldsm_x4(kbox + k_key * 128u + ((((uint32_t)(2 * kk) + k_hi) ^ sw) << 4), b0, b1, b2, b3);
+                                mma_bf16_16816(sc[2 * b], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
+                                mma_bf16_16816(sc[2 * b + 1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
+                            }
                         }
                     }
                 }
@@ -437,7 +539,7 @@ __global__ void __launch_bounds__(kA2Threads, 1)
 #pragma unroll
                 for (int b = 0; b < kA2Block; ++b) {
                     if (b < nb) {
-                        const uint32_t vbox = sRing + (uint32_t)((k0 + b) % kA2Stages) * kA2PageBytes + 2048;
+                        const uint32_t vbox = vreg + (uint32_t)b * 2048;
                         // P (rows a / b x the page's 16 keys) as the A fragment of PV
                         const uint32_t pa0 = pack_f2bf(sc[2 * b][0], sc[2 * b][1]);
                         const uint32_t pa1 = pack_f2bf(sc[2 * b][2], sc[2 * b][3]);
@@ -457,7 +559,16 @@ __global__ void __launch_bounds__(kA2Threads, 1)
             if (lane == 0)
                 mbar_arrive(empty0 + 8 * rb);
         }
+        if constexpr (kA2TcQK) {
+            if (issuer && committed != observed)   // an abandoned wait: let the MMAs finish first
+                bounded_wait(sbar, (uint32_t)((committed - 1) & 1), s_flags, p.wait_limit_ns, false);
+            tc_fence_before();
+        }
         a2_ring_done_sync();   // every group is past the ring; the producer has drained
+        if constexpr (kA2TcQK) {
+            tc_fence_after();
+            if (warp == 0) a2_tmem_dealloc(*reinterpret_cast<volatile uint32_t *>(smem + LY.tslot));
+        }
         // whole-row sums across the four threads of a row
 #pragma unroll
         for (int off = 1; off <= 2; off <<= 1) {
@@ -676,11 +787,11 @@ int encode_kv_map(const uint16_t *kv_cache, int64_t num_pages, int nkv, CUtensor
     // the cache [pages * nkv][16 slots][2 halves][64] seen with the half
     // dimension outside the slot dimension: dim 0 = 64 elements of a half,
     // dim 1 = slot (256 B apart), dim 2 = K / V half (128 B apart), dim 3 =
-    // (page, KV head).  One {64, 16, 2, 1} box is a page of one KV head with
-    // its 16 K rows first and its 16 V rows after, each 128 bytes, swizzled
+    // (page, KV head).  A {64, 16, 1, 1} box is the 16 K (or V) rows of a
+    // page of one KV head, 128 bytes each, swizzled
     const cuuint64_t dims[4] = {64, (cuuint64_t)kPageSlots, 2, (cuuint64_t)num_pages * nkv};
     const cuuint64_t strides[3] = {256, 128, (cuuint64_t)kPageSlots * kSlotWidth * 2};
-    const cuuint32_t box[4] = {64, (cuuint32_t)kPageSlots, 2, 1};
+    const cuuint32_t box[4] = {64, (cuuint32_t)kPageSlots, 1, 1};
     const cuuint32_t es[4] = {1, 1, 1, 1};
     return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, (void *)kv_cache, dims, strides, box, es,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
