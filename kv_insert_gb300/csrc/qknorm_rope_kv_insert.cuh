@@ -39,7 +39,11 @@ struct EpiParams {
 constexpr int kEpiConsumerWarps = 8;
 constexpr int kEpiThreads = 32 * (kEpiConsumerWarps + 1);   // warp 0 produces
 constexpr int kEpiMaxTokens = 1 << 24;
-constexpr int kEpiRingBudget = 100 * 1024;   // two CTAs per SM
+#ifndef EPI_CTAS_PER_SM
+#define EPI_CTAS_PER_SM 2
+#endif
+constexpr int kEpiCtasPerSm = EPI_CTAS_PER_SM;
+constexpr int kEpiRingBudget = (kEpiCtasPerSm >= 3 ? 64 : 100) * 1024;   // per CTA
 constexpr int kEpiMaxSlots = 16;
 
 // bytes of one token's ring slot: its q | k | v heads, its cos|sin row, and a
@@ -62,21 +66,73 @@ __host__ __device__ inline uint32_t epi_smem_bytes(int nkv)
     return (uint32_t)epi_slots(nkv) * epi_slot_bytes(nkv) + 2 * kEpiMaxSlots * 8 + 16 + 128;
 }
 
+// Packed FP32 pairs (Blackwell's f32x2 arithmetic): two IEEE round-to-nearest
+// operations in one instruction, each lane's result the same bits as the
+// scalar __fmul_rn / __fadd_rn / __fsub_rn.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi)
+{
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+    return d;
+}
+
+__device__ __forceinline__ void f2_unpack(uint64_t v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// Eight BF16 values (16 bytes: four rotation pairs 2j, 2j + 1) widened to
+// FP32 and regrouped for packed arithmetic over pairs j and j + 1:
+// ev[k] = (element 4k, element 4k + 2), od[k] = (element 4k + 1, element 4k + 3).
+__device__ __forceinline__ void unpack8_pairs(const uint4 &v, uint64_t (&ev)[2], uint64_t (&od)[2])
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        ev[k] = f2_pack(__uint_as_float(w[2 * k] << 16), __uint_as_float(w[2 * k + 1] << 16));
+        od[k] = f2_pack(__uint_as_float(w[2 * k] & 0xFFFF0000u), __uint_as_float(w[2 * k + 1] & 0xFFFF0000u));
+    }
+}
+
 // Sum of squares of one head held by 4 lanes, in exactly the association of
 // the fused front's warp butterfly (qk_norm_rope_pair), so both kernels give
 // the same bits.  In the front, lane l holds pair l (columns 2l, 2l+1) and the
 // butterfly adds across lane bits 4, 3, 2, 1, 0 in that order.  Here lane c of
-// the 4-lane group holds pairs 4c..4c+3 (lo[]) and 16+4c..16+4c+3 (hi[]): the
+// the 4-lane group holds pairs 4c..4c+3 (lo) and 16+4c..16+4c+3 (hi): the
 // front's lane bit 4 is lo/hi (added in registers), bits 3, 2 are this group's
 // lane bits 1, 0 (two shuffle levels), and bits 1, 0 index the four pairs.
-__device__ __forceinline__ float head_sum_sq_front_order(const float (&lo)[8], const float (&hi)[8])
+// Pair j's (x_2j^2 + x_2j+1^2) of lo and of hi, and their sum, are formed two
+// pairs at a time.
+__device__ __forceinline__ float head_sum_sq_front_order(const uint64_t (&lo_ev)[2], const uint64_t (&lo_od)[2],
+                                                         const uint64_t (&hi_ev)[2], const uint64_t (&hi_od)[2])
 {
     float a[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const float sl = __fadd_rn(__fmul_rn(lo[2 * j], lo[2 * j]), __fmul_rn(lo[2 * j + 1], lo[2 * j + 1]));
-        const float sh = __fadd_rn(__fmul_rn(hi[2 * j], hi[2 * j]), __fmul_rn(hi[2 * j + 1], hi[2 * j + 1]));
-        a[j] = __fadd_rn(sl, sh);
+    for (int k = 0; k < 2; ++k) {
+        const uint64_t sl = f2_add(f2_mul(lo_ev[k], lo_ev[k]), f2_mul(lo_od[k], lo_od[k]));
+        const uint64_t sh = f2_add(f2_mul(hi_ev[k], hi_ev[k]), f2_mul(hi_od[k], hi_od[k]));
+        f2_unpack(f2_add(sl, sh), a[2 * k], a[2 * k + 1]);
     }
 #pragma unroll
     for (int off = 2; off >= 1; off >>= 1)
@@ -85,28 +141,25 @@ __device__ __forceinline__ float head_sum_sq_front_order(const float (&lo)[8], c
     return __fadd_rn(__fadd_rn(a[0], a[2]), __fadd_rn(a[1], a[3]));
 }
 
-__device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8])
+// Scale four rotation pairs by r and rotate them by (c, s), two pairs per
+// packed operation: (a, b) = r (x_2j, x_2j+1); (a c - b s, b c + a s); BF16.
+// cs points at cos[j0], sn at sin[j0] of the first pair (8-byte aligned).
+__device__ __forceinline__ uint4 rope4_pairs(const uint64_t (&ev)[2], const uint64_t (&od)[2], uint64_t rr,
+                                             const float *cs, const float *sn)
 {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const __nv_bfloat162 pr = *reinterpret_cast<const __nv_bfloat162 *>(&w[j]);
-        f[2 * j] = __low2float(pr);
-        f[2 * j + 1] = __high2float(pr);
-    }
-}
-
-// rotate four pairs by (c, s) after scaling by r; pack to BF16
-__device__ __forceinline__ uint4 rope4(const float (&f)[8], float r, const float4 c, const float4 s)
-{
-    const float cc[4] = {c.x, c.y, c.z, c.w}, sn[4] = {s.x, s.y, s.z, s.w};
     uint32_t o[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const float a = __fmul_rn(f[2 * j], r), b = __fmul_rn(f[2 * j + 1], r);
-        const float y0 = __fsub_rn(__fmul_rn(a, cc[j]), __fmul_rn(b, sn[j]));
-        const float y1 = __fadd_rn(__fmul_rn(b, cc[j]), __fmul_rn(a, sn[j]));
-        o[j] = pack_bf16x2(__float2bfloat16_rn(y0), __float2bfloat16_rn(y1));
+    for (int k = 0; k < 2; ++k) {
+        const uint64_t c = *reinterpret_cast<const uint64_t *>(cs + 2 * k);
+        const uint64_t s = *reinterpret_cast<const uint64_t *>(sn + 2 * k);
+        const uint64_t a = f2_mul(ev[k], rr), b = f2_mul(od[k], rr);
+        const uint64_t y0 = f2_sub(f2_mul(a, c), f2_mul(b, s));
+        const uint64_t y1 = f2_add(f2_mul(b, c), f2_mul(a, s));
+        float y00, y01, y10, y11;
+        f2_unpack(y0, y00, y01);
+        f2_unpack(y1, y10, y11);
+        o[2 * k] = pack_bf16x2(__float2bfloat16_rn(y00), __float2bfloat16_rn(y10));
+        o[2 * k + 1] = pack_bf16x2(__float2bfloat16_rn(y01), __float2bfloat16_rn(y11));
     }
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
@@ -127,7 +180,7 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
 // with c = l % 4), norm and
 // rotate q / k heads in place in global memory and write k / v heads into the
 // cache slot.
-__global__ void __launch_bounds__(kEpiThreads, 2) qknorm_rope_kv_insert_kernel(const EpiParams p)
+__global__ void __launch_bounds__(kEpiThreads, kEpiCtasPerSm) qknorm_rope_kv_insert_kernel(const EpiParams p)
 {
     extern __shared__ uint8_t epi_smem_dyn[];
     uint8_t *smem = epi_smem_dyn + ((128u - (smem_u32(epi_smem_dyn) & 127u)) & 127u);
@@ -250,16 +303,15 @@ __global__ void __launch_bounds__(kEpiThreads, 2) qknorm_rope_kv_insert_kernel(c
                         v1 = *reinterpret_cast<const uint4 *>(src + 64);
                     }
                     if (grp * 8 < qk_heads && pos_ok) {   // the whole warp: shuffles inside
-                        float lo[8], hi[8];
-                        unpack8(v0, lo);
-                        unpack8(v1, hi);
-                        const float ss = head_sum_sq_front_order(lo, hi);
+                        uint64_t lo_ev[2], lo_od[2], hi_ev[2], hi_od[2];
+                        unpack8_pairs(v0, lo_ev, lo_od);
+                        unpack8_pairs(v1, hi_ev, hi_od);
+                        const float ss = head_sum_sq_front_order(lo_ev, lo_od, hi_ev, hi_od);
                         const float ms = __fmul_rn(ss, 1.0f / (float)kHeadDim);   // exact: a power of two
                         const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, kEps)));
-                        const uint4 o0 = rope4(lo, r, *reinterpret_cast<const float4 *>(row + 4 * part),
-                                               *reinterpret_cast<const float4 *>(row + 32 + 4 * part));
-                        const uint4 o1 = rope4(hi, r, *reinterpret_cast<const float4 *>(row + 16 + 4 * part),
-                                               *reinterpret_cast<const float4 *>(row + 48 + 4 * part));
+                        const uint64_t rr = f2_pack(r, r);
+                        const uint4 o0 = rope4_pairs(lo_ev, lo_od, rr, row + 4 * part, row + 32 + 4 * part);
+                        const uint4 o1 = rope4_pairs(hi_ev, hi_od, rr, row + 16 + 4 * part, row + 48 + 4 * part);
                         if (h < qk_heads) {
                             v0 = o0;
                             v1 = o1;
@@ -345,7 +397,7 @@ int launch_epi(uint16_t *qkv, const int64_t *positions, const int64_t *slots, co
     prm.N = N;
     prm.nkv = num_kv_heads;
     prm.wait_limit_ns = g_wait_limit_ns;
-    int64_t blocks = (int64_t)sms * 2;   // two CTAs per SM, each walking its tokens
+    int64_t blocks = (int64_t)sms * kEpiCtasPerSm;   // CTAs per SM, each walking its tokens
     if (blocks > T) blocks = T;
     if (blocks < 1) blocks = 1;
     cudaLaunchConfig_t cfg = {};
