@@ -154,11 +154,14 @@ int qkv_front_status(unsigned int *bits);
 
 /*
  * qkv_front_from_host: the whole call for a caller whose tokens live in host
- * memory.  On `stream`, asynchronously: copies x [M, 8192], positions [M] and
- * slots [M] from host memory into the caller's device `staging` buffer, runs
- * qkv_front on them, and copies out [M, N] back to `out_host`.  Host buffers
- * should be pinned (page-locked) for the copies to be asynchronous, and must
- * stay valid until the stream passes the call.  W, cos_sin and kv_cache are
+ * memory.  On `stream`, asynchronously: x [M, 8192], positions [M] and slots
+ * [M] go from host memory into the caller's device `staging` buffer, qkv_front
+ * runs on them, and out [M, N] goes back to `out_host`.  Pinned (page-locked,
+ * device-mapped) host buffers are read by a staging kernel over the host link,
+ * PDL-linked to the front so that its weight stream starts while x arrives,
+ * and a pinned out_host is written by the front directly; pageable buffers go
+ * through copies on the stream instead.  Host buffers must stay valid and
+ * unchanged until the stream passes the call.  W, cos_sin and kv_cache are
  * device pointers as for qkv_front.
  *   staging        device buffer, 256-byte aligned, at least
  *                  qkv_front_staging_bytes(M, N) bytes; owned by the caller;

@@ -1183,6 +1183,47 @@ int qkv_front_status(unsigned int *bits)
     return QKVF_OK;
 }
 
+// Copies a call's host inputs into the staging buffer from the GPU itself,
+// for pinned (device-mapped) host memory: x as 16-byte loads, positions and
+// slots by the first M threads.  The host reads are issued before the wait
+// for the kernel before (whose front may still read the staging buffer);
+// the stores after it.  Launched with PDL, and it lets the front launch at
+// once, so the front's weight stream starts while x is still arriving.
+constexpr int kStageThreads = 256;
+
+__global__ void __launch_bounds__(kStageThreads) stage_from_host_kernel(
+    const uint4 *x_host, const int64_t *pos_host, const int64_t *slot_host, uint4 *x, int64_t *pos,
+    int64_t *slot, int n16, int M)
+{
+    if (threadIdx.x == 0) griddep_launch_dependents();
+    const int i = blockIdx.x * kStageThreads + threadIdx.x;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (i < n16) v = __ldcv(x_host + i);   // not cached: the host rewrites it between calls
+    int64_t pv = 0, sv = 0;
+    if (i < M) {
+        pv = __ldcv(reinterpret_cast<const long long *>(pos_host) + i);
+        sv = __ldcv(reinterpret_cast<const long long *>(slot_host) + i);
+    }
+    griddep_wait();
+    if (i < n16) x[i] = v;
+    if (i < M) {
+        pos[i] = pv;
+        slot[i] = sv;
+    }
+}
+
+// The device address of a pinned (page-locked, device-mapped) host buffer,
+// or null when the GPU cannot reach it (pageable memory: copy it instead).
+static void *mapped_host(const void *p)
+{
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
 // staging layout of qkv_front_from_host: x | positions | slots | out, each
 // starting on a 256-byte boundary
 struct Staging {
@@ -1229,17 +1270,46 @@ int qkv_front_from_host(const uint16_t *x_host, const int64_t *positions_host,
                    num_kv_heads, &code))
         return code;
     const cudaStream_t s = (cudaStream_t)stream;
-    if (cudaMemcpyAsync((void *)x, x_host, (size_t)M * kHidden * 2, cudaMemcpyHostToDevice, s) !=
-            cudaSuccess ||
-        cudaMemcpyAsync((void *)pos, positions_host, (size_t)M * 8, cudaMemcpyHostToDevice, s) !=
-            cudaSuccess ||
-        cudaMemcpyAsync((void *)slots, slots_host, (size_t)M * 8, cudaMemcpyHostToDevice, s) !=
-            cudaSuccess)
-        return QKVF_ERR_CUDA;
-    const int rc = qkv_front_launch(x, W, pos, slots, cos_sin, cos_sin_rows, out, kv_cache,
-                                    num_pages, M, N, num_kv_heads, stream);
+    DeviceState *d;
+    int rc = probe_device(&d);
     if (rc != QKVF_OK) return rc;
-    if (cudaMemcpyAsync(out_host, out, (size_t)M * N * 2, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    // pinned host buffers are read and written by the kernels over the
+    // host link; pageable ones go through copies on the stream
+    const void *xm = mapped_host(x_host), *pm = mapped_host(positions_host), *sm = mapped_host(slots_host);
+    void *om = mapped_host(out_host);
+    if (xm && pm && sm && (uintptr_t)xm % 16 == 0) {
+        const int n16 = M * kHidden * 2 / 16;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)((n16 + kStageThreads - 1) / kStageThreads), 1, 1);
+        cfg.blockDim = dim3(kStageThreads, 1, 1);
+        cfg.stream = s;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr.val.programmaticStreamSerializationAllowed = g_pdl ? 1 : 0;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, stage_from_host_kernel, static_cast<const uint4 *>(xm),
+                               static_cast<const int64_t *>(pm), static_cast<const int64_t *>(sm),
+                               reinterpret_cast<uint4 *>(const_cast<uint16_t *>(x)), const_cast<int64_t *>(pos),
+                               const_cast<int64_t *>(slots), n16, M) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return QKVF_ERR_CUDA;
+        }
+    } else if (cudaMemcpyAsync((void *)x, x_host, (size_t)M * kHidden * 2, cudaMemcpyHostToDevice, s) !=
+                   cudaSuccess ||
+               cudaMemcpyAsync((void *)pos, positions_host, (size_t)M * 8, cudaMemcpyHostToDevice, s) !=
+                   cudaSuccess ||
+               cudaMemcpyAsync((void *)slots, slots_host, (size_t)M * 8, cudaMemcpyHostToDevice, s) !=
+                   cudaSuccess) {
+        return QKVF_ERR_CUDA;
+    }
+    const bool out_direct = om && (uintptr_t)om % 16 == 0;
+    rc = qkv_front_launch(x, W, pos, slots, cos_sin, cos_sin_rows,
+                          out_direct ? static_cast<uint16_t *>(om) : out, kv_cache, num_pages, M, N,
+                          num_kv_heads, stream);
+    if (rc != QKVF_OK) return rc;
+    if (!out_direct &&
+        cudaMemcpyAsync(out_host, out, (size_t)M * N * 2, cudaMemcpyDeviceToHost, s) != cudaSuccess)
         return QKVF_ERR_CUDA;
     return QKVF_OK;
 }

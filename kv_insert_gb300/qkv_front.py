@@ -303,10 +303,10 @@ def staging_bytes(m: int, n: int) -> int:
 
 def qkv_front_from_host(x_host, positions_host, slots_host, out_host, weight, cos_sin, kv_cache,
                         staging, stream=None):
-    """The whole call from host buffers: x / positions / slots copied in,
-    the front run, out copied back, all on one stream in one library call.
-    Host tensors should be pinned; `staging` is a device uint8 tensor of at
-    least staging_bytes(M, N) bytes."""
+    """The whole call from host buffers: x / positions / slots in, the front
+    run, out back, all on one stream in one library call.  Pinned host tensors
+    are read and written by the kernels directly, pageable ones are copied;
+    `staging` is a device uint8 tensor of at least staging_bytes(M, N) bytes."""
     for name, t in (("x_host", x_host), ("positions_host", positions_host),
                     ("slots_host", slots_host), ("out_host", out_host)):
         if t.is_cuda or not t.is_contiguous():

@@ -168,3 +168,27 @@ def test_from_host_entry_matches_device_call(name):
         assert qf.status() == 0
         assert torch.equal(oh.view(torch.int16), out_dev.cpu().view(torch.int16))
         assert torch.equal(g2["kv_cache"].view(torch.int16), cache_dev.view(torch.int16))
+
+
+@pytest.mark.parametrize("pinned_in,pinned_out", [(False, False), (True, False), (False, True)])
+def test_from_host_pageable_buffers_take_the_copy_path(pinned_in, pinned_out):
+    """Pinned host buffers are read and written by the kernels directly;
+    pageable ones are copied on the stream.  Every mix gives the device
+    call's bits."""
+    w = wl.WORKLOADS["m8_nkv8_n9216"]
+    inp = wl.make_inputs(w)
+    g = device_inputs(inp)
+    out_dev = run_device(g)
+    cache_dev = g["kv_cache"].clone()
+    g2 = device_inputs(inp)
+    pin = (lambda t: t.pin_memory()) if pinned_in else (lambda t: t.clone())
+    xh, ph, sh = pin(inp["x"]), pin(inp["positions"]), pin(inp["slots"])
+    oh = torch.zeros(w.M, w.N, dtype=torch.bfloat16)
+    if pinned_out:
+        oh = oh.pin_memory()
+    staging = torch.empty(qf.staging_bytes(w.M, w.N), dtype=torch.uint8, device="cuda:0")
+    qf.qkv_front_from_host(xh, ph, sh, oh, g2["W"], g2["cos_sin"], g2["kv_cache"], staging)
+    torch.cuda.synchronize()
+    assert qf.status() == 0
+    assert torch.equal(oh.view(torch.int16), out_dev.cpu().view(torch.int16))
+    assert torch.equal(g2["kv_cache"].view(torch.int16), cache_dev.view(torch.int16))
