@@ -23,6 +23,7 @@ import hashlib
 import json
 import math
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -258,6 +259,23 @@ def time_oracle_units(inp, w, units: int):
     return time.perf_counter() - t0
 
 
+def cpu_model() -> str:
+    """The host CPU's name as /proc/cpuinfo gives it (x86 model name, or the
+    Arm implementer / part numbers), else the machine type."""
+    try:
+        fields = {}
+        for line in open("/proc/cpuinfo"):
+            k, _, v = line.partition(":")
+            fields.setdefault(k.strip(), v.strip())
+        if "model name" in fields:
+            return fields["model name"]
+        if "CPU part" in fields:
+            return f"{platform.machine()} CPU implementer {fields.get('CPU implementer', '?')} part {fields['CPU part']}"
+    except OSError:
+        pass
+    return platform.machine()
+
+
 def cpu_baseline(inp, w, seconds: float) -> dict:
     """The oracle, as it stands, on host cores: whole calls of the workload
     until `seconds` of CPU work (at least one)."""
@@ -277,7 +295,8 @@ def cpu_baseline(inp, w, seconds: float) -> dict:
             break
     return {"value": w.roofline_bytes() * calls / el / 1e9, "unit": UNIT, "cores": 1,
             "kind": "oracle",
-            "sample": f"{calls} whole calls of {w.name} (single-threaded C oracle), {el:.1f} s"}
+            "sample": f"{calls} whole calls of {w.name} (single-threaded C oracle), {el:.1f} s, "
+                      f"on {cpu_model()} ({os.cpu_count()} cores visible)"}
 
 
 def run_reference(args, w: wl.Workload):
@@ -293,7 +312,7 @@ def run_reference(args, w: wl.Workload):
     el = time_oracle_units(inp, w, units_per_step * args.steps)
     value = unit_bytes * units_per_step * args.steps / el / 1e9
     sample = (f"each step: {units_per_step} of the {n_units} (token, KV-head group) units of "
-              f"{w.name} through the single-threaded C oracle")
+              f"{w.name} through the single-threaded C oracle, on {cpu_model()}")
     cfg = w.describe()
     cfg.update({"l2": "n/a (host)", "units_per_step": units_per_step})
     return {"metric": METRIC, "value": value, "unit": UNIT, "impl": "reference",
@@ -383,6 +402,25 @@ def run_ours(args, w: wl.Workload):
     el_max = max_over_ranks(el, dev)
     res = aggregate(w.roofline_bytes(), args.steps, world, el_max)
 
+    # the same calls on one W copy (the warm case: whatever of W the L2 keeps
+    # between calls is not re-read), outside the timed region, labelled
+    warm_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(warm_graph, stream=stream):
+        for _ in range(per_graph):
+            qf.launch(g["x"], Ws[0], g["positions"], g["slots"], g["cos_sin"], g["kv_cache"], out)
+    with torch.cuda.stream(stream):
+        warm_graph.replay()
+    stream.synchronize()
+    w_start, w_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    warm_reps = max(1, min(20, args.steps // per_graph))
+    with torch.cuda.stream(stream):
+        w_start.record(stream)
+        for _ in range(warm_reps):
+            warm_graph.replay()
+        w_end.record(stream)
+    torch.cuda.synchronize(dev)
+    warm_us = w_start.elapsed_time(w_end) * 1e3 / (warm_reps * per_graph)
+
     # end to end through the public API: pinned host inputs -> device, the call,
     # device -> pinned host result, every step
     e2e = None
@@ -443,6 +481,9 @@ def run_ours(args, w: wl.Workload):
         "gpu_launches": args.steps,
         "clocks": clocks,
         "e2e": e2e,
+        "warm_same_w": {"us_per_call": warm_us, "calls": warm_reps * per_graph,
+                        "note": "one W copy for every call, timed after and apart from the "
+                                "headline; not the headline"},
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(inp, w, args.cpu_seconds)
