@@ -43,6 +43,13 @@ constexpr int kEpiMaxTokens = 1 << 24;
 #define EPI_CTAS_PER_SM 2
 #endif
 constexpr int kEpiCtasPerSm = EPI_CTAS_PER_SM;
+#ifndef EPI_CPASYNC
+#define EPI_CPASYNC 1
+#endif
+// token regions by 16-byte cp.async from the producer warp's 32 lanes (a
+// bulk copy costs the SM's TMA unit ~0.2 us whatever its size, which set
+// this kernel's pace at two copies per token), else by bulk copies
+constexpr bool kEpiCpAsync = EPI_CPASYNC != 0;
 constexpr int kEpiRingBudget = (kEpiCtasPerSm >= 3 ? 64 : 100) * 1024;   // per CTA
 constexpr int kEpiMaxSlots = 16;
 
@@ -198,7 +205,8 @@ __global__ void __launch_bounds__(kEpiThreads, kEpiCtasPerSm) qknorm_rope_kv_ins
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < nslots; ++s) {
-            mbar_init(full0 + 8 * s, 1);
+            // cp.async: the 32 lanes' copies land (32) and lane 0's header (1)
+            mbar_init(full0 + 8 * s, kEpiCpAsync ? 33 : 1);
             mbar_init(empty0 + 8 * s, (heads + 7) >> 3);   // one arrival per 8-head group
         }
         *s_abort = 0;
@@ -228,33 +236,47 @@ __global__ void __launch_bounds__(kEpiThreads, kEpiCtasPerSm) qknorm_rope_kv_ins
                 if (t >= p.T) break;   // the same for every lane
                 const int64_t pos = __shfl_sync(0xffffffffu, pos_l, j);
                 const int64_t sl = __shfl_sync(0xffffffffu, slot_l, j);
-                if (lane == 0) {
-                    const int s = i % nslots, use = i / nslots;
-                    if (use > 0 && !bounded_wait(empty0 + 8 * s, (uint32_t)((use - 1) & 1), s_abort,
-                                                 p.wait_limit_ns, true)) {
-                        stop = true;
-                    } else {
-                        uint8_t *base = smem + (size_t)s * slot_bytes;
-                        const bool pos_ok = pos >= 0 && pos < p.cos_rows;
-                        const bool ins = sl >= 0 && sl < slot_end && pos_ok;
-                        int64_t *hdr = reinterpret_cast<int64_t *>(base + region + kHeadDim * 4);
-                        hdr[0] = pos;
-                        hdr[1] = sl;
-                        hdr[2] = (pos_ok ? 1 : 0) | (ins ? 2 : 0);
-                        const uint32_t bar = full0 + 8 * s;
-                        mbar_expect_tx(bar, region + (pos_ok ? kHeadDim * 4 : 0));
-                        bulk_load(smem_u32(base), p.qkv + (size_t)t * p.N, region, bar);
-                        if (pos_ok)
-                            bulk_load(smem_u32(base + region), p.cos_sin + pos * kHeadDim, kHeadDim * 4,
-                                      bar);
-                        ++issued;
-                    }
+                const int s = i % nslots, use = i / nslots;
+                int ok = 1;
+                if (lane == 0 && use > 0)
+                    ok = bounded_wait(empty0 + 8 * s, (uint32_t)((use - 1) & 1), s_abort, p.wait_limit_ns, true);
+                if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                    stop = true;
+                    break;
                 }
-                stop = __shfl_sync(0xffffffffu, stop ? 1 : 0, 0) != 0;
-                if (stop) break;
+                uint8_t *base = smem + (size_t)s * slot_bytes;
+                const bool pos_ok = pos >= 0 && pos < p.cos_rows;
+                const bool ins = sl >= 0 && sl < slot_end && pos_ok;
+                const uint32_t bar = full0 + 8 * s;
+                if (lane == 0) {
+                    int64_t *hdr = reinterpret_cast<int64_t *>(base + region + kHeadDim * 4);
+                    hdr[0] = pos;
+                    hdr[1] = sl;
+                    hdr[2] = (pos_ok ? 1 : 0) | (ins ? 2 : 0);
+                }
+                if constexpr (kEpiCpAsync) {
+                    const uint8_t *src = reinterpret_cast<const uint8_t *>(p.qkv + (size_t)t * p.N);
+                    for (uint32_t c = (uint32_t)lane; c < region / 16; c += 32)
+                        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(base) + 16 * c),
+                                     "l"(src + 16 * c)
+                                     : "memory");
+                    if (pos_ok && lane < kHeadDim * 4 / 16)
+                        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(base + region) + 16 * lane),
+                                     "l"(reinterpret_cast<const uint8_t *>(p.cos_sin + pos * kHeadDim) + 16 * lane)
+                                     : "memory");
+                    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+                    if (lane == 0) mbar_arrive(bar);   // the header
+                } else if (lane == 0) {
+                    mbar_expect_tx(bar, region + (pos_ok ? kHeadDim * 4 : 0));
+                    bulk_load(smem_u32(base), p.qkv + (size_t)t * p.N, region, bar);
+                    if (pos_ok)
+                        bulk_load(smem_u32(base + region), p.cos_sin + pos * kHeadDim, kHeadDim * 4, bar);
+                }
+                ++issued;
             }
         }
-        if (lane == 0 && *s_abort) {   // drain our copies before leaving
+        if constexpr (kEpiCpAsync) asm volatile("cp.async.wait_all;" ::: "memory");   // nothing left in flight
+        if (!kEpiCpAsync && lane == 0 && *s_abort) {   // drain our copies before leaving
             const int first = issued > nslots ? issued - nslots : 0;
             for (int k = first; k < issued; ++k)
                 bounded_wait(full0 + 8 * (k % nslots), (uint32_t)((k / nslots) & 1), s_abort,
