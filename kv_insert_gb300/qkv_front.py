@@ -284,9 +284,60 @@ def variant_full(n: int, m: int) -> dict:
     return out
 
 
+def k_split(n: int) -> int:
+    """CTAs per head splitting the 8192-long K (a power of two <= 16 with
+    heads x splits within the SM count): 1 at N = 9216, 8 at N = 1152."""
+    return variant_full(n, 1)["splits"]
+
+
+def ring_stages(n: int, m: int) -> int:
+    """Ring slots of the W / x stream for n columns and m tokens."""
+    return variant_full(n, m)["stages"]
+
+
 def prepare(n: int, num_kv_heads: int) -> None:
     """Set the kernel attributes the variants of n columns need (before graph capture)."""
     _check(load().qkv_front_prepare(n, num_kv_heads))
+
+
+def compile_qkv_front(n: int, num_kv_heads: int) -> None:
+    """The kernels are compiled ahead of time for sm_103a (build()); what is
+    left to do before the first call or a graph capture is prepare()."""
+    prepare(n, num_kv_heads)
+
+
+def sm100_family(device=None) -> bool:
+    """Whether the device is a compute capability 10.x part.  This library is
+    built for 10.3 (GB300) only; other 10.x parts are refused at the first call."""
+    if not torch.cuda.is_available():
+        return False
+    return torch.cuda.get_device_capability(device)[0] == 10
+
+
+def unsupported_projection(weight, bias=None, is_neox_style: bool = False, cos_sin=None,
+                           gather_output: bool = False, quantized: bool = False):
+    """Why a QKV projection layer cannot use the fused front, or None: the
+    front takes unquantized BF16 weights [N, 8192] with no bias, interleaved
+    RoPE (pairs 2i, 2i + 1) from an FP32 [positions, 64] cos | sin table, and
+    keeps its column shard (no gathered output)."""
+    if quantized:
+        return "quantized weights (the front streams BF16 weights)"
+    if weight.dtype != torch.bfloat16:
+        return f"{weight.dtype} weights (the front streams BF16 weights)"
+    if weight.dim() != 2 or weight.shape[1] != HIDDEN:
+        return f"weight shape {tuple(weight.shape)} (the front takes [N, {HIDDEN}])"
+    if bias is not None:
+        return "a bias on the projection"
+    if is_neox_style:
+        return "neox-style RoPE (the front rotates interleaved pairs 2i, 2i + 1)"
+    if cos_sin is not None and (cos_sin.dtype != torch.float32 or cos_sin.dim() != 2
+                                or cos_sin.shape[1] != HEAD_DIM):
+        return f"a cos | sin table other than FP32 [positions, {HEAD_DIM}]"
+    if gather_output:
+        return "a gathered output (the front keeps each rank's column shard)"
+    if weight.shape[0] % (2 * (Q_PER_KV + 1) * HEAD_DIM) != 0:
+        return f"N = {weight.shape[0]} (the front takes 1152 columns per KV head)"
+    return None
 
 
 def status() -> int:

@@ -246,3 +246,19 @@ def test_attn2_split_kv_refusals(lib):
     assert call(ws=CACHE) == 9                       # workspace inside the cache
     assert call(R=0, ws=0) == 0
     assert call() in (5, 6)                          # valid: reaches the device query
+
+
+def test_unsupported_projection_reasons():
+    """The host-side refusals of a projection layer the front cannot take
+    (no device needed)."""
+    w = torch.zeros(2304, 8192, dtype=torch.bfloat16)
+    assert qf.unsupported_projection(w) is None
+    assert "quantized" in qf.unsupported_projection(w, quantized=True)
+    assert "float16" in qf.unsupported_projection(w.to(torch.float16))
+    assert "bias" in qf.unsupported_projection(w, bias=torch.zeros(2304))
+    assert "neox" in qf.unsupported_projection(w, is_neox_style=True)
+    assert "gathered" in qf.unsupported_projection(w, gather_output=True)
+    assert "cos" in qf.unsupported_projection(w, cos_sin=torch.zeros(16, 64, dtype=torch.float16))
+    assert qf.unsupported_projection(w, cos_sin=torch.zeros(16, 64)) is None
+    assert "1152" in qf.unsupported_projection(torch.zeros(2000, 8192, dtype=torch.bfloat16))
+    assert "shape" in qf.unsupported_projection(torch.zeros(2304, 4096, dtype=torch.bfloat16))

@@ -192,3 +192,12 @@ def test_from_host_pageable_buffers_take_the_copy_path(pinned_in, pinned_out):
     assert qf.status() == 0
     assert torch.equal(oh.view(torch.int16), out_dev.cpu().view(torch.int16))
     assert torch.equal(g2["kv_cache"].view(torch.int16), cache_dev.view(torch.int16))
+
+
+def test_page_helper_names():
+    """The pages' helper names on this device: k_split, ring_stages,
+    sm100_family, compile_qkv_front."""
+    assert qf.sm100_family()
+    assert qf.k_split(9216) == 1 and qf.k_split(1152) == 8
+    assert qf.ring_stages(9216, 8) == qf.variant_full(9216, 8)["stages"] >= 2
+    qf.compile_qkv_front(9216, 8)
