@@ -41,12 +41,6 @@
 #ifndef A2_BLOCK
 #define A2_BLOCK 4
 #endif
-#ifndef A2_TC_PV
-#define A2_TC_PV 0   // 1: P V on tcgen05 too, O in tensor memory, lazily rescaled
-#endif
-#ifndef A2_CPASYNC
-#define A2_CPASYNC 0   // 1: pages by 16-byte cp.async from the producer warp instead of TMA
-#endif
 #ifndef A2_TC_QK
 #define A2_TC_QK 1   // 0: Q K^T with mma.sync + ldmatrix of K (2 - 3 % slower on GB300)
 #endif
@@ -58,13 +52,7 @@ constexpr int kA2ComputeWarps = 4 * kA2Groups;
 constexpr int kA2Threads = 32 * (kA2ComputeWarps + 1);   // the last warp produces
 constexpr int kA2Block = A2_BLOCK;                        // pages per softmax step (16 per page)
 constexpr bool kA2TcQK = A2_TC_QK != 0;                   // Q K^T on tcgen05 (else mma.sync)
-constexpr bool kA2TcPV = A2_TC_PV != 0;
-// cp.async producer: the swizzled layout TMA would give; each block is
-// signalled kA2CpLag blocks later, once its copies are known complete and
-// fenced for the tensor cores
-constexpr bool kA2CpAsync = A2_CPASYNC != 0;
-constexpr int kA2CpLag = 8;
-constexpr int kA2TmemCols = kA2TcPV ? 512 : 256;           // per group an S tile (and an O tile)
+constexpr int kA2TmemCols = 256;                          // one 64-column S tile per group
 constexpr int kA2RingBlocks = A2_RING_BLOCKS;
 constexpr int kA2Stages = kA2RingBlocks * kA2Block;       // pages in flight per CTA
 // ring slot k % stages always serves group (k / block) % groups: each group
@@ -72,7 +60,6 @@ constexpr int kA2Stages = kA2RingBlocks * kA2Block;       // pages in flight per
 static_assert(kA2RingBlocks % kA2Groups == 0, "ring blocks must be a multiple of the groups");
 static_assert(32 % kA2Block == 0, "a block's table entries lie in one 32-entry chunk");
 static_assert(!kA2TcQK || (kA2Block == 4 && kA2Groups * 64 <= kA2TmemCols), "tcgen05 Q K^T: 64-key blocks");
-static_assert(!kA2TcPV || (kA2TcQK && kA2Groups * 128 <= kA2TmemCols), "tcgen05 P V needs tcgen05 Q K^T");
 constexpr uint32_t kA2PageBytes = 4096;                   // K box + V box
 constexpr int kA2OStride = 68;                            // floats per row of the O partial
 constexpr int kA2MaxSplits = 16;
@@ -82,7 +69,7 @@ constexpr int kA2WsMaxSplits = 256;     // workspace engine: CTAs per (request, 
 constexpr int kA2WsSlotFloats = 64 * 64 + 64 + 64 + 64;   // O [64][64], m, l, flags: 17152 bytes
 
 struct A2Layout {
-    uint32_t q, p, ring, full, empty, sbar, obar, tslot, o, m, l, flags, total;
+    uint32_t q, ring, full, empty, sbar, tslot, o, m, l, flags, total;
 };
 
 // the groups' O partials overlay the ring: written only once every page has
@@ -95,8 +82,6 @@ __host__ __device__ inline A2Layout a2_layout()
     uint32_t off = 0;
     L.q = off;
     off += 64 * 128;
-    L.p = off;   // per group: P of the block in flight, bf16 [64 rows][64 keys] swizzled (tcgen05 P V)
-    if (kA2TcPV) off += kA2Groups * 64 * 128;
     L.ring = off;
     L.o = off;
     off += kA2Stages * kA2PageBytes;
@@ -105,8 +90,6 @@ __host__ __device__ inline A2Layout a2_layout()
     L.empty = off;
     off += kA2RingBlocks * 8;
     L.sbar = off;   // per group: its Q K^T (tcgen05) is done
-    off += kA2Groups * 8;
-    L.obar = off;   // per group: its P V (tcgen05) is done
     off += kA2Groups * 8;
     L.tslot = off;  // tensor-memory base address
     off += 8;
@@ -122,7 +105,6 @@ __host__ __device__ inline A2Layout a2_layout()
 
 struct Attn2Params {
     const uint16_t *qkv;
-    const uint16_t *kv;      // the cache (the cp.async producer reads it directly)
     float *ws;               // split-KV partials (workspace engine), else null
     const int32_t *block_table;
     const int32_t *context_lens;
@@ -205,35 +187,6 @@ __device__ __forceinline__ void a2_tmem_ld_16x256b_x8(uint32_t taddr, uint32_t (
         : "r"(taddr));
 }
 
-__device__ __forceinline__ void a2_tmem_st_16x256b_x8(uint32_t taddr, const uint32_t (&r)[32])
-{
-    asm volatile(
-        "tcgen05.st.sync.aligned.16x256b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
-        "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
-        "%30, %31, %32};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
-        "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
-        "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-        : "memory");
-}
-
-__device__ __forceinline__ void a2_tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-// Shared-memory descriptor of an MN-major operand (V as the B of P V: keys
-// down 128-byte rows of 64 dims, 128-byte swizzle), 8-key groups 1024 bytes
-// apart.  With N = 64 the operand is one swizzle atom wide, so the stride
-// between atoms along N is never used; both stride fields hold 1024.
-__device__ __forceinline__ uint64_t a2_desc_sw128_mn(uint32_t saddr)
-{
-    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
-    d |= (uint64_t)(1024u >> 4) << 16;
-    d |= (uint64_t)(1024u >> 4) << 32;
-    d |= (uint64_t)1 << 46;
-    d |= (uint64_t)2 << 61;
-    return d;
-}
-
 // 2^x for x <= 0 (softmax weights): the hardware approximation, subnormal
 // results flushed to zero — weights below 2^-126 of the row maximum
 __device__ __forceinline__ float a2_ex2(float x)
@@ -305,14 +258,11 @@ __global__ void __launch_bounds__(kA2Threads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kA2RingBlocks; ++s) {   // one full / empty pair per block of pages
-            mbar_init(full0 + 8 * s, kA2CpAsync ? 32 : 1);   // cp.async: each producer lane
-            mbar_init(empty0 + 8 * s, kA2TcPV ? 1 : 4);   // the owning group's 4 warps, or its P V commit
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 4);   // the 4 warps of the group that owns the block
         }
         if constexpr (kA2TcQK)
-            for (int q = 0; q < kA2Groups; ++q) {
-                mbar_init(smem_u32(smem + LY.sbar) + 8 * q, 1);
-                mbar_init(smem_u32(smem + LY.obar) + 8 * q, 1);
-            }
+            for (int q = 0; q < kA2Groups; ++q) mbar_init(smem_u32(smem + LY.sbar) + 8 * q, 1);
         s_flags[0] = 0;
         s_flags[1] = 0;
         fence_barrier_init();
@@ -367,37 +317,11 @@ __global__ void __launch_bounds__(kA2Threads, 1)
                 if (lane == 0) {
                     ok = use == 0 || bounded_wait(empty0 + 8 * rb, (uint32_t)((use - 1) & 1),
                                                   s_flags, p.wait_limit_ns, true);
-                    if (ok && !kA2CpAsync) mbar_expect_tx(full0 + 8 * rb, (uint32_t)nb * kA2PageBytes);
+                    if (ok) mbar_expect_tx(full0 + 8 * rb, (uint32_t)nb * kA2PageBytes);
                 }
                 if (!__shfl_sync(0xffffffffu, ok, 0)) {
                     stop = true;
                     break;
-                }
-                if constexpr (kA2CpAsync) {
-                    // 256 chunks of 16 bytes per page: lane l takes chunks l, l + 32, ...
-                    // (slot q / 16, half (q / 8) % 2, chunk q % 8 of the 128-byte half row)
-                    const uint32_t blk = sRing + (uint32_t)rb * (kA2Block * kA2PageBytes);
-                    for (int b = 0; b < nb; ++b) {
-                        const int pg = __shfl_sync(0xffffffffu, page, (k0 - c + b) & 31);
-                        const uint8_t *src = reinterpret_cast<const uint8_t *>(p.kv) +
-                                             ((size_t)pg * p.nkv + g) * kA2PageBytes;
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const int q = lane + 32 * i, sl = q >> 4, half = (q >> 3) & 1, cc = q & 7;
-                            const uint32_t dst = blk + (uint32_t)half * (kA2Block * 2048) +
-                                                 (uint32_t)(b * 16 + sl) * 128 + ((uint32_t)(cc ^ (sl & 7)) << 4);
-                            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src + 16 * q)
-                                         : "memory");
-                        }
-                    }
-                    asm volatile("cp.async.commit_group;" ::: "memory");
-                    if (issued >= kA2CpLag) {   // the block issued kA2CpLag blocks ago has landed
-                        asm volatile("cp.async.wait_group %0;" ::"n"(kA2CpLag) : "memory");
-                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                        mbar_arrive(full0 + 8 * ((issued - kA2CpLag) % kA2RingBlocks));
-                    }
-                    ++issued;
-                    continue;
                 }
                 const int b = c + lane - k0;   // this lane's page within the block
                 if (b >= 0 && b < nb) {
@@ -411,19 +335,13 @@ __global__ void __launch_bounds__(kA2Threads, 1)
                 ++issued;
             }
         }
-        if constexpr (kA2CpAsync) {   // the last blocks: all copies landed, fenced, signalled
-            asm volatile("cp.async.wait_all;" ::: "memory");
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            for (int j = issued > kA2CpLag ? issued - kA2CpLag : 0; j < issued; ++j)
-                mbar_arrive(full0 + 8 * (j % kA2RingBlocks));
-        }
         bad = __reduce_or_sync(0xffffffffu, bad);
         if (lane == 0) {
             if (bad) {
                 s_flags[1] = 1;
                 atomicOr(&g_status, QKVF_STATUS_BAD_REQUEST);
             }
-            if (!kA2CpAsync && s_flags[0]) {   // drain our copies before the ring is reused or we leave
+            if (s_flags[0]) {   // drain our copies before the ring is reused or we leave
                 const int first = issued > kA2RingBlocks ? issued - kA2RingBlocks : 0;
                 for (int j = first; j < issued; ++j)
                     bounded_wait(full0 + 8 * (j % kA2RingBlocks), (uint32_t)((j / kA2RingBlocks) & 1),
@@ -461,7 +379,7 @@ __global__ void __launch_bounds__(kA2Threads, 1)
         // tcgen05 Q K^T: the group's S tile [64 rows x 64 keys] in tensor memory
         // columns 64 grp.., rows 16 w .. 16 w + 15 in lanes 32 w .. 32 w + 15
         const uint32_t sbar = smem_u32(smem + LY.sbar) + 8 * grp;
-        const uint32_t tS = kA2TcQK ? *reinterpret_cast<volatile uint32_t *>(smem + LY.tslot) + (kA2TcPV ? 128u : 64u) * grp : 0u;
+        const uint32_t tS = kA2TcQK ? *reinterpret_cast<volatile uint32_t *>(smem + LY.tslot) + 64u * grp : 0u;
         const bool issuer = wig == 0 && lane == 0;
         uint32_t sph = 0;            // phase of sbar this block waits for
         int committed = 0, observed = 0;   // the issuer's commits, and those it saw complete
@@ -485,186 +403,6 @@ __global__ void __launch_bounds__(kA2Threads, 1)
         const uint32_t v_hi = (uint32_t)(lane >> 4);
         const uint32_t sw = (uint32_t)(lane & 7);
 
-        if constexpr (kA2TcPV) {
-        // ---- both products on tcgen05: S and O tiles in tensor memory -----
-        // Per block: the issuer starts Q K^T into S; the warps read S, run the
-        // softmax against a reference maximum that moves only when a row's
-        // maximum grows by more than 2^8 (then O is rescaled in tensor memory),
-        // write P as bf16 into the group's swizzled P buffer, and the issuer
-        // accumulates P V into O, whose commit also frees the ring block.
-        const uint32_t tO = tS + 64u, lane_off = (uint32_t)(32 * wig) << 16;
-        const uint32_t obar = smem_u32(smem + LY.obar) + 8 * grp;
-        const uint32_t pbuf = smem_u32(smem + LY.p) + 8192u * grp;
-        int li = 0, pv_issued = 0;
-        for (int k0 = grp * kA2Block; k0 < npages; k0 += kA2Groups * kA2Block) {
-            const int nb = npages - k0 < kA2Block ? npages - k0 : kA2Block;   // same for every lane
-            const int jb = k0 / kA2Block, rb = jb % kA2RingBlocks;
-            const uint32_t ph = (uint32_t)((jb / kA2RingBlocks) & 1);
-            bool inside = true;
-            for (int b = 0; b < nb; ++b) {
-                const int key0 = (first_mine + (k0 + b) * S) * kPageSlots;
-                inside = inside && key0 >= edge_lo && key0 + kPageSlots - 1 <= edge_hi;
-            }
-            inside = inside && nb == kA2Block;
-            bool ok = mbar_try_wait(full0 + 8 * rb, ph) ||
-                      bounded_wait(full0 + 8 * rb, ph, s_flags, p.wait_limit_ns, true);
-            const uint32_t kreg = sRing + (uint32_t)rb * (kA2Block * kA2PageBytes);
-            const uint32_t vreg = kreg + kA2Block * 2048;
-            // S is free: every warp read the last one before the last group barrier
-            if (issuer && ok) {
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    umma_bf16(tS, umma_desc_sw128(sQ + 32u * kk), umma_desc_sw128(kreg + 32u * kk),
-                              umma_idesc_bf16(64, 64), kk != 0 ? 1u : 0u);
-                umma_commit(sbar);
-                ++committed;
-            }
-            const uint32_t sp = (uint32_t)(li & 1);
-            ok = ok && (mbar_try_wait(sbar, sp) || bounded_wait(sbar, sp, s_flags, p.wait_limit_ns, true));
-            if (issuer && ok) observed = committed;
-            if (li > 0) {   // the last P V is done: P and O may be touched
-                const uint32_t op = (uint32_t)((li - 1) & 1);
-                ok = ok && (mbar_try_wait(obar, op) || bounded_wait(obar, op, s_flags, p.wait_limit_ns, true));
-            }
-            const bool go = __all_sync(0xffffffffu, ok);
-            if (go) {
-                tc_fence_after();
-                float sc[2 * kA2Block][4];
-                {
-                    uint32_t rr[32];
-                    a2_tmem_ld_16x256b_x8(tS + lane_off, rr);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int nt = 0; nt < 2 * kA2Block; ++nt)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) sc[nt][e] = __uint_as_float(rr[4 * nt + e]);
-                }
-                if (!inside) {
-#pragma unroll
-                    for (int b = 0; b < kA2Block; ++b) {
-                        const int key0 = (first_mine + (k0 + b) * S) * kPageSlots;
-#pragma unroll
-                        for (int h = 0; h < 2; ++h)
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const int key = key0 + 8 * h + 2 * t + (e & 1);
-                                const bool kok = b < nb && (e >= 2 ? (key >= lo_b && key <= pos_b)
-                                                                   : (key >= lo_a && key <= pos_a));
-                                if (!kok) sc[2 * b + h][e] = -INFINITY;
-                            }
-                    }
-                }
-                float tm[2 * kA2Block][2];
-#pragma unroll
-                for (int nt = 0; nt < 2 * kA2Block; ++nt) {
-                    tm[nt][0] = fmaxf(sc[nt][0], sc[nt][1]);
-                    tm[nt][1] = fmaxf(sc[nt][2], sc[nt][3]);
-                }
-#pragma unroll
-                for (int w = kA2Block; w >= 1; w >>= 1)
-#pragma unroll
-                    for (int nt = 0; nt < w; ++nt) {
-                        tm[nt][0] = fmaxf(tm[nt][0], tm[nt + w][0]);
-                        tm[nt][1] = fmaxf(tm[nt][1], tm[nt + w][1]);
-                    }
-                float mx_a = tm[0][0] * p.scale_log2, mx_b = tm[0][1] * p.scale_log2;
-#pragma unroll
-                for (int off = 1; off <= 2; off <<= 1) {
-                    mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, off));
-                    mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, off));
-                }
-                // the reference maximum moves only past 2^8 of growth
-                const bool mv_a = mx_a > m_a + 8.f, mv_b = mx_b > m_b + 8.f;
-                const float nr_a = mv_a ? mx_a : m_a, nr_b = mv_b ? mx_b : m_b;
-                const float base_a = nr_a == -INFINITY ? 0.f : nr_a;
-                const float base_b = nr_b == -INFINITY ? 0.f : nr_b;
-                const float al_a = a2_ex2(m_a - base_a), al_b = a2_ex2(m_b - base_b);
-                float ts[2 * kA2Block][2];
-#pragma unroll
-                for (int nt = 0; nt < 2 * kA2Block; ++nt) {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        sc[nt][e] = a2_ex2(fmaf(sc[nt][e], p.scale_log2, e >= 2 ? -base_b : -base_a));
-                    ts[nt][0] = sc[nt][0] + sc[nt][1];
-                    ts[nt][1] = sc[nt][2] + sc[nt][3];
-                }
-#pragma unroll
-                for (int w = kA2Block; w >= 1; w >>= 1)
-#pragma unroll
-                    for (int nt = 0; nt < w; ++nt) {
-                        ts[nt][0] += ts[nt + w][0];
-                        ts[nt][1] += ts[nt + w][1];
-                    }
-                l_a = l_a * al_a + ts[0][0];
-                l_b = l_b * al_b + ts[0][1];
-                if (li > 0 && __any_sync(0xffffffffu, mv_a || mv_b)) {   // this warp's O rows, rescaled
-                    uint32_t oo[32];
-                    a2_tmem_ld_16x256b_x8(tO + lane_off, oo);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int nd = 0; nd < 8; ++nd) {
-                        oo[4 * nd + 0] = __float_as_uint(__uint_as_float(oo[4 * nd + 0]) * al_a);
-                        oo[4 * nd + 1] = __float_as_uint(__uint_as_float(oo[4 * nd + 1]) * al_a);
-                        oo[4 * nd + 2] = __float_as_uint(__uint_as_float(oo[4 * nd + 2]) * al_b);
-                        oo[4 * nd + 3] = __float_as_uint(__uint_as_float(oo[4 * nd + 3]) * al_b);
-                    }
-                    a2_tmem_st_16x256b_x8(tO + lane_off, oo);
-                    a2_tmem_st_wait();
-                }
-                m_a = nr_a;
-                m_b = nr_b;
-                // P into the P buffer: row r at r * 128, its 16-byte chunk nt XORed by r % 8
-                const uint32_t ra = (uint32_t)(16 * wig + gq), rsw = ra & 7u;
-#pragma unroll
-                for (int nt = 0; nt < 2 * kA2Block; ++nt) {
-                    const uint32_t col = (((uint32_t)nt ^ rsw) << 4) + 4u * t;
-                    asm volatile("st.shared.b32 [%0], %1;" ::"r"(pbuf + ra * 128u + col),
-                                 "r"(pack_f2bf(sc[nt][0], sc[nt][1])) : "memory");
-                    asm volatile("st.shared.b32 [%0], %1;" ::"r"(pbuf + (ra + 8u) * 128u + col),
-                                 "r"(pack_f2bf(sc[nt][2], sc[nt][3])) : "memory");
-                }
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // P for the tensor cores
-            }
-            tc_fence_before();
-            a2_group_bar_sync(grp);
-            if (issuer && go) {
-                tc_fence_after();
-                // one page (16 keys) per instruction, loaded pages only: the rows of
-                // a short block's missing pages hold stale bytes (0 x NaN is NaN)
-                for (int kk = 0; kk < nb; ++kk)
-                    umma_bf16(tO, umma_desc_sw128(pbuf + 32u * kk), a2_desc_sw128_mn(vreg + 2048u * kk),
-                              umma_idesc_bf16(64, 64) | (1u << 16), (li > 0 || kk > 0) ? 1u : 0u);
-                umma_commit(obar);
-                umma_commit(empty0 + 8 * rb);   // the ring block is free once P V has read it
-                ++pv_issued;
-            }
-            ++li;
-        }
-        // the last P V, then O into registers in the accumulator layout
-        bool o_ok = li > 0;
-        if (li > 0) {
-            const uint32_t op = (uint32_t)((li - 1) & 1);
-            o_ok = mbar_try_wait(obar, op) || bounded_wait(obar, op, s_flags, p.wait_limit_ns, true);
-        }
-        if (issuer) {   // an abandoned wait: let this group's MMAs finish before tensor memory is freed
-            if (committed != observed)
-                bounded_wait(sbar, (uint32_t)((committed - 1) & 1), s_flags, p.wait_limit_ns, false);
-            if (pv_issued > 0)
-                bounded_wait(obar, (uint32_t)((pv_issued - 1) & 1), s_flags, p.wait_limit_ns, false);
-        }
-        if (__all_sync(0xffffffffu, o_ok)) {
-            tc_fence_after();
-            uint32_t oo[32];
-            a2_tmem_ld_16x256b_x8(tO + lane_off, oo);
-            tmem_ld_wait();
-#pragma unroll
-            for (int nd = 0; nd < 8; ++nd)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) o[nd][e] = __uint_as_float(oo[4 * nd + e]);
-        }
-        committed = observed;   // drained above
-        } else {
         // blocks of up to kA2Block pages (16 kA2Block keys): one softmax
         // reduction and one rescale of O per block, independent mma chains
         for (int k0 = grp * kA2Block; k0 < npages; k0 += kA2Groups * kA2Block) {
@@ -820,7 +558,6 @@ __global__ void __launch_bounds__(kA2Threads, 1)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(empty0 + 8 * rb);
-        }
         }
         if constexpr (kA2TcQK) {
             if (issuer && committed != observed)   // an abandoned wait: let the MMAs finish first
@@ -1166,7 +903,6 @@ int launch_attn2(const uint16_t *qkv, const uint16_t *kv_cache, int64_t num_page
     Attn2Params prm;
     prm.qkv = qkv;
     prm.ws = static_cast<float *>(workspace);
-    prm.kv = kv_cache;
     prm.block_table = block_table;
     prm.context_lens = context_lens;
     prm.out = out;
