@@ -670,7 +670,7 @@ def run_attn2(args, w):
                          "traffic": recorded_traffic(
                              "attn2" if args.engine == "cluster" else "attn2_split_kv", w.name),
                          "bytes_per_launch": w.roofline_bytes()},
-            "gpu_launches": args.steps * (2 if args.engine == "split_kv" else 1), "clocks": clocks,
+            "gpu_launches": args.steps * (2 if args.engine == "split_kv" and splits > 1 else 1), "clocks": clocks,
             "e2e": None}
 
 

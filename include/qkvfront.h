@@ -285,6 +285,8 @@ int attn2_splits(int num_reqs, int num_kv_heads, int max_blocks, int window);
  *                   splits) bytes, owned by the caller, overlapping no other
  *                   argument, no initial contents needed; one workspace serves
  *                   one stream at a time.
+ * With splits == 1 the call runs one grid (each CTA finishes its own rows)
+ * and leaves the workspace untouched.
  * Returns QKVF_ERR_NULL / _ALIGN / _SIZES / _ARG for a missing, misaligned,
  * short or overlapping workspace, else as attn2.
  */

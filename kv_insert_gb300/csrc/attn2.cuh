@@ -69,7 +69,7 @@ constexpr int kA2WsMaxSplits = 256;     // workspace engine: CTAs per (request, 
 constexpr int kA2WsSlotFloats = 64 * 64 + 64 + 64 + 64;   // O [64][64], m, l, flags: 17152 bytes
 
 struct A2Layout {
-    uint32_t q, ring, full, empty, sbar, tslot, o, m, l, flags, total;
+    uint32_t q, gate, ring, full, empty, sbar, tslot, o, m, l, flags, total;
 };
 
 // the groups' O partials overlay the ring: written only once every page has
@@ -81,6 +81,8 @@ __host__ __device__ inline A2Layout a2_layout()
     A2Layout L;
     uint32_t off = 0;
     L.q = off;
+    off += 64 * 128;
+    L.gate = off;   // the rows' gate heads, bf16 [64 rows][64], loaded with Q
     off += 64 * 128;
     L.ring = off;
     L.o = off;
@@ -362,6 +364,13 @@ __global__ void __launch_bounds__(kA2Threads, 1)
                 const uint4 v = *reinterpret_cast<const uint4 *>(
                     p.qkv + ((size_t)r * 8 + (row >> 3)) * p.N + (size_t)(8 * g + (row & 7)) * kHeadDim + 8 * cc);
                 *reinterpret_cast<uint4 *>(smem + LY.q + row * 128 + ((cc ^ (row & 7)) << 4)) = v;
+            }
+            // the same rows' gate heads, for the finish (no global load at the tail)
+            const int gate_col = kQPerKv * p.nkv * kHeadDim + 2 * p.nkv * kHeadDim;
+            for (int c = tid; c < 512; c += 32 * kA2ComputeWarps) {
+                const int row = c >> 3, cc = c & 7;
+                *reinterpret_cast<uint4 *>(smem + LY.gate + row * 128 + 16 * cc) = *reinterpret_cast<const uint4 *>(
+                    p.qkv + ((size_t)r * 8 + (row >> 3)) * p.N + gate_col + (size_t)(8 * g + (row & 7)) * kHeadDim + 8 * cc);
             }
             if constexpr (kA2TcQK)   // the tensor cores read Q through the async proxy
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -660,37 +669,33 @@ __global__ void __launch_bounds__(kA2Threads, 1)
             const uint32_t o_addr = smem_u32(o_part), m_addr = smem_u32(m_part), l_addr = smem_u32(l_part);
             for (int i = warp; i < rows; i += kA2ComputeWarps + 1) {
                 const int row = (int)z * rows + i;
-                const __nv_bfloat162 gt = a2_gate(p, r, g, row, lane);
-                // the ranks' partials in rank order; all remote loads issued first
-                float mk[kA2MaxSplits], lk[kA2MaxSplits];
-                float2 ov[kA2MaxSplits];
-#pragma unroll
-                for (int src = 0; src < kA2MaxSplits; ++src) {
-                    if (src < S) {
-                        if (S > 1) {
-                            mk[src] = ld_cluster_f32(map_to_rank(m_addr + 4u * row, (uint32_t)src));
-                            lk[src] = ld_cluster_f32(map_to_rank(l_addr + 4u * row, (uint32_t)src));
-                            ov[src] = ld_cluster_f2(map_to_rank(o_addr + 4u * (row * kA2OStride + 2 * lane), (uint32_t)src));
-                        } else {
-                            mk[src] = m_part[row];
-                            lk[src] = l_part[row];
-                            ov[src] = *reinterpret_cast<const float2 *>(o_part + row * kA2OStride + 2 * lane);
-                        }
-                    }
-                }
-                float M = -INFINITY;
-#pragma unroll
-                for (int src = 0; src < kA2MaxSplits; ++src)
-                    if (src < S) M = fmaxf(M, mk[src]);
-                const float base = M == -INFINITY ? 0.f : M;
-                float lt = 0.f, o0 = 0.f, o1 = 0.f;
-#pragma unroll
-                for (int src = 0; src < kA2MaxSplits; ++src) {
-                    if (src < S) {
-                        const float w = exp2f(mk[src] - base);
-                        lt = lt + lk[src] * w;
-                        o0 = o0 + ov[src].x * w;
-                        o1 = o1 + ov[src].y * w;
+                const __nv_bfloat162 gt = *reinterpret_cast<const __nv_bfloat162 *>(smem + LY.gate + row * 128 + 4 * lane);
+                // the ranks' partials in rank order (short loops: a fully unrolled
+                // merge over every possible rank cost ~3000 cycles a row)
+                float lt, o0, o1;
+                if (S == 1) {
+                    const float2 v = *reinterpret_cast<const float2 *>(o_part + row * kA2OStride + 2 * lane);
+                    o0 = v.x;
+                    o1 = v.y;
+                    lt = l_part[row];
+                } else {
+                    float M = -INFINITY;
+#pragma unroll 4
+                    for (int src = 0; src < S; ++src)
+                        M = fmaxf(M, ld_cluster_f32(map_to_rank(m_addr + 4u * row, (uint32_t)src)));
+                    const float base = M == -INFINITY ? 0.f : M;
+                    lt = 0.f;
+                    o0 = 0.f;
+                    o1 = 0.f;
+#pragma unroll 4
+                    for (int src = 0; src < S; ++src) {
+                        const float w = exp2f(ld_cluster_f32(map_to_rank(m_addr + 4u * row, (uint32_t)src)) - base);
+                        const float lk = ld_cluster_f32(map_to_rank(l_addr + 4u * row, (uint32_t)src));
+                        const float2 ov =
+                            ld_cluster_f2(map_to_rank(o_addr + 4u * (row * kA2OStride + 2 * lane), (uint32_t)src));
+                        lt = lt + lk * w;
+                        o0 = o0 + ov.x * w;
+                        o1 = o1 + ov.y * w;
                     }
                 }
                 a2_finish_row(p, r, g, row, o0, o1, lt, lane, gt);
@@ -1051,6 +1056,9 @@ int attn2_split_kv(const uint16_t *qkv, const uint16_t *kv_cache, int64_t num_pa
         const int rc = qkvf::probe_device(&d);
         if (rc != QKVF_OK) return rc;
     }
+    if (splits == 1)   // one CTA per (request, KV head) finishes its own rows: no partials to merge
+        return qkvf::launch_attn2(qkv, kv_cache, num_pages, block_table, max_blocks, context_lens, num_reqs,
+                                  N, num_kv_heads, window, scale, eps, out, 1, nullptr, stream);
     return qkvf::launch_attn2(qkv, kv_cache, num_pages, block_table, max_blocks, context_lens,
                               num_reqs, N, num_kv_heads, window, scale, eps, out, splits, workspace, stream);
 }

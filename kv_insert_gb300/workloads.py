@@ -287,7 +287,9 @@ for _a in (AttnWorkload("attn_r1_l8_nkv1", R=1, num_kv_heads=1, context=(8,), nu
            AttnWorkload("attn_r1_l32k_nkv8", R=1, num_kv_heads=8, context=(32768,), num_pages=4096,
                         seed=5004),
            AttnWorkload("attn_r8_l4k_nkv8", R=8, num_kv_heads=8, context=(4096,) * 8,
-                        num_pages=4096, seed=5005)):
+                        num_pages=4096, seed=5005),
+           AttnWorkload("attn_r32_l1k_nkv8", R=32, num_kv_heads=8, context=(1024,) * 32,
+                        num_pages=4096, seed=5006)):
     ATTN_WORKLOADS[_a.name] = _a
 
 ATTN_BENCH_WORKLOAD = "attn_r1_l32k_nkv8"
