@@ -148,11 +148,11 @@ def hbm_peak():
 
 
 def source_digest(op: str) -> str:
-    """sha256 over the op's kernel sources and the C header."""
+    """sha256 over the op's kernel sources (the .cu / .cuh files that make its
+    kernels; the C header only declares them)."""
     h = hashlib.sha256()
-    files = [os.path.join(ROOT, "kv_insert_gb300", "csrc", f) for f in OP_SOURCES[op]]
-    for f in files + [os.path.join(ROOT, "include", "qkvfront.h")]:
-        with open(f, "rb") as fh:
+    for f in OP_SOURCES[op]:
+        with open(os.path.join(ROOT, "kv_insert_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
 
