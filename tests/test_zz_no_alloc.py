@@ -59,3 +59,19 @@ def test_noalloc_matches_the_workspace_engine_two_calls_in_a_row(built):
         torch.cuda.synchronize()
         assert qf.status() == 0
         assert_values(wl.bits(out.cpu()), wl.bits(ref.cpu()), what=f"no-alloc attn2 {name} S={S}")
+
+
+@pytest.mark.gpu
+def test_noalloc_refuses_a_library_split_beyond_its_array(built):
+    """With the split left to the library, a shape whose partial slots exceed
+    the array (40 requests x 8 KV heads = 320 > 256 at one split) is refused
+    with QKVF_ERR_SIZES and launches nothing."""
+    w = wl.AttnWorkload("noalloc_big", R=40, num_kv_heads=8, context=(64,) * 40, num_pages=256, seed=7100)
+    g = {k: v.to("cuda:0") for k, v in wl.make_attn_inputs(w).items()}
+    out = torch.full((8 * w.R, 512 * w.num_kv_heads), 3.0, dtype=torch.bfloat16, device="cuda:0")
+    assert qf.attn2_split_kv_splits(w.R, w.num_kv_heads, w.max_blocks()) >= 1
+    with pytest.raises(qf.QkvFrontError) as e:
+        qf.attn2_split_kv_noalloc(g["qkv"], g["kv_cache"], g["block_table"], g["context_lens"], out=out)
+    assert e.value.code == 7
+    torch.cuda.synchronize()
+    assert torch.all(out == 3.0)
