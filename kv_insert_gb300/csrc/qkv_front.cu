@@ -111,14 +111,15 @@ __host__ __device__ inline Layout layout_of(int mt, int kb, int stages)
     L.tmem_slot = off;
     off += 8;
     off = (off + 15u) & ~15u;
+    // per-token arrays for the tile's mt tokens (M <= mt)
     L.pos = off;
-    off += kMaxTokens * 8;
+    off += (uint32_t)mt * 8;
     L.slot = off;
-    off += kMaxTokens * 8;
+    off += (uint32_t)mt * 8;
     L.cs = off;
-    off += kMaxTokens * kHeadDim * 4;
+    off += (uint32_t)mt * kHeadDim * 4;
     L.flag = off;
-    off += kMaxTokens * 4;
+    off += (uint32_t)mt * 4;
     L.abort_flag = off;
     off += 16;
     L.total = off;
@@ -747,12 +748,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (S == 1) {
             v = reinterpret_cast<const float2 *>(part + u * kPartStride)[lane];
         } else {
+            // every rank's partial is requested before the first add (one
+            // round trip, not S); the adds keep rank order 0..S-1
             const uint32_t a = part_addr + (uint32_t)(u * kPartStride + 2 * lane) * 4u;
-            v = ld_cluster_f2(map_to_rank(a, 0));
-            for (int src = 1; src < S; ++src) {
-                const float2 r = ld_cluster_f2(map_to_rank(a, (uint32_t)src));
-                v.x = __fadd_rn(v.x, r.x);
-                v.y = __fadd_rn(v.y, r.y);
+            float2 r[16];
+#pragma unroll
+            for (int src = 0; src < 16; ++src)
+                if (src < S) r[src] = ld_cluster_f2(map_to_rank(a, (uint32_t)src));
+            v = r[0];
+#pragma unroll
+            for (int src = 1; src < 16; ++src) {
+                if (src < S) {
+                    v.x = __fadd_rn(v.x, r[src].x);
+                    v.y = __fadd_rn(v.y, r[src].y);
+                }
             }
         }
         const int flag = s_flag[u];
