@@ -229,15 +229,19 @@ class ClockSampler:
 
 # ---- the CPU oracle (baseline and reference arm) ---------------------------
 
-def oracle_unit_inputs(inp: dict, w: wl.Workload, t: int, g: int):
-    """One token and one KV-head group of the workload: the rows of W that KV
-    head g owns ([q heads 8g..8g+7 | k head g | v head g | gate heads
-    8g..8g+7]), i.e. one tensor-parallel shard, and token t."""
-    nkv = w.num_kv_heads
+def shard_rows(nkv: int, g: int) -> np.ndarray:
+    """The rows of W that KV head g owns ([q heads 8g..8g+7 | k head g | v
+    head g | gate heads 8g..8g+7]): one tensor-parallel shard, itself a front
+    with one KV head."""
     heads = (list(range(8 * g, 8 * g + 8)) + [8 * nkv + g, 9 * nkv + g]
              + list(range(10 * nkv + 8 * g, 10 * nkv + 8 * g + 8)))
-    rows = np.concatenate([np.arange(h * 64, h * 64 + 64) for h in heads])
-    Wb = wl.bits(inp["W"])[rows]
+    return np.concatenate([np.arange(h * 64, h * 64 + 64) for h in heads])
+
+
+def oracle_unit_inputs(inp: dict, w: wl.Workload, t: int, g: int):
+    """One token and one KV-head group of the workload: KV head g's shard of
+    W and token t."""
+    Wb = wl.bits(inp["W"])[shard_rows(w.num_kv_heads, g)]
     return (wl.bits(inp["x"])[t: t + 1], np.ascontiguousarray(Wb),
             inp["positions"].numpy()[t: t + 1], np.array([0], np.int64))
 
@@ -297,6 +301,52 @@ def cpu_baseline(inp, w, seconds: float) -> dict:
             "kind": "oracle",
             "sample": f"{calls} whole calls of {w.name} (single-threaded C oracle), {el:.1f} s, "
                       f"on {cpu_model()} ({os.cpu_count()} cores visible)"}
+
+
+def oracle_shard_call(xb, w_shard, pos, cs, cache):
+    """One KV head's shard of a call through the oracle, tokens t -> slots t
+    of a one-page cache (M <= 16): the same arithmetic, per column, as the
+    whole call."""
+    import oracle
+    slots = np.arange(xb.shape[0], dtype=np.int64)
+    out, err = oracle.qkv_front(xb, w_shard, pos, slots, cs, cache, 1)
+    if err:
+        raise RuntimeError(f"oracle error {err}")
+    return out
+
+
+def cpu_baseline_all_cores(inp, w, seconds: float) -> dict:
+    """The same oracle on every host core: each whole call split into its
+    KV-head shards, the shards of several calls run side by side in threads
+    (the oracle's C call releases the GIL). Each output column is computed
+    exactly as in the whole call."""
+    from concurrent.futures import ThreadPoolExecutor
+    threads = os.cpu_count() or 1
+    nkv = w.num_kv_heads
+    cs = inp["cos_sin"].numpy()
+    xb, pos = wl.bits(inp["x"]), inp["positions"].numpy()
+    Wall = wl.bits(inp["W"])
+    shards = [np.ascontiguousarray(Wall[shard_rows(nkv, g)]) for g in range(nkv)]
+    per_wave = max(1, -(-threads // nkv))   # whole calls in flight together
+    tasks = per_wave * nkv
+    caches = [np.zeros((1, 1, 16, 128), np.uint16) for _ in range(tasks)]
+
+    def task(i):
+        oracle_shard_call(xb, shards[i % nkv], pos, cs, caches[i])
+
+    calls = 0
+    with ThreadPoolExecutor(min(threads, tasks)) as ex:
+        t0 = time.perf_counter()
+        while True:
+            list(ex.map(task, range(tasks)))
+            calls += per_wave
+            el = time.perf_counter() - t0
+            if el >= seconds:
+                break
+    return {"value": w.roofline_bytes() * calls / el / 1e9, "unit": UNIT,
+            "cores": min(threads, tasks), "kind": "oracle",
+            "sample": f"{calls} whole calls of {w.name} as {nkv} KV-head shards each, "
+                      f"{min(threads, tasks)} threads, {el:.1f} s, on {cpu_model()}"}
 
 
 def run_reference(args, w: wl.Workload):
@@ -487,6 +537,7 @@ def run_ours(args, w: wl.Workload):
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(inp, w, args.cpu_seconds)
+        line["cpu_baseline_all_cores"] = cpu_baseline_all_cores(inp, w, args.cpu_seconds)
     return line
 
 

@@ -72,3 +72,28 @@ def test_roofline_bytes_formula():
     assert w.roofline_bytes() == 151_289_856
     assert wl.WORKLOADS["m1_nkv1_n1152"].roofline_bytes() == 18_893_312
     assert wl.WORKLOADS["m8_nkv16_n18432"].roofline_bytes() == 302_448_640
+
+
+def test_all_cores_baseline_shards_reproduce_the_whole_call():
+    """The all-cores CPU baseline runs each call as KV-head shards; the
+    shards' columns and cache rows must be bit-identical to the whole call."""
+    import numpy as np
+    import bench
+    import oracle
+    from kv_insert_gb300 import workloads as wl
+    w = wl.Workload("shard_check_m3_nkv2", M=3, num_kv_heads=2, max_pos=64, num_pages=4, seed=77)
+    inp = wl.make_inputs(w)
+    xb, Wb = wl.bits(inp["x"]), wl.bits(inp["W"])
+    pos, cs = inp["positions"].numpy(), inp["cos_sin"].numpy()
+    cache = wl.bits(inp["kv_cache"]).copy()
+    slots = inp["slots"].numpy()
+    whole, err = oracle.qkv_front(xb, Wb, pos, slots, cs, cache, w.num_kv_heads)
+    assert err == 0
+    for g in range(w.num_kv_heads):
+        rows = bench.shard_rows(w.num_kv_heads, g)
+        shard_cache = np.zeros((1, 1, 16, 128), np.uint16)
+        part = bench.oracle_shard_call(xb, np.ascontiguousarray(Wb[rows]), pos, cs, shard_cache)
+        assert np.array_equal(part, whole[:, rows]), g
+        for t, slot in enumerate(slots):
+            page, off = divmod(int(slot), 16)
+            assert np.array_equal(shard_cache[0, 0, t], cache[page, g, off]), (g, t)
