@@ -235,6 +235,40 @@ __device__ __forceinline__ void a2_finish_row(const Attn2Params &p, int r, int g
         pack_f2bf(o0 * rn * s0, o1 * rn * s1);
 }
 
+// The same finish with 8 lanes per row: lane j of the row's group of 8 holds
+// dims 8 j .. 8 j + 7 (o = oa | ob, their gate values in gw), so a warp
+// finishes 4 rows at once; the o-norm's sum is a 3-level butterfly inside the
+// group.  `store` is false for a padding row past the tile.
+__device__ __forceinline__ void a2_finish_row8(const Attn2Params &p, int r, int g, int row, float4 oa,
+                                               float4 ob, float lt, int j, uint4 gw, bool store)
+{
+    const int out_cols = kQPerKv * p.nkv * kHeadDim;
+    const float inv = lt > 0.f ? 1.0f / lt : 0.f;
+    const float o[8] = {oa.x * inv, oa.y * inv, oa.z * inv, oa.w * inv,
+                        ob.x * inv, ob.y * inv, ob.z * inv, ob.w * inv};
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) ss += o[k] * o[k];
+#pragma unroll
+    for (int off = 4; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    const float rn = 1.0f / sqrtf(ss * (1.0f / kHeadDim) + p.eps);
+    const uint32_t gv[4] = {gw.x, gw.y, gw.z, gw.w};
+    uint32_t res[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float g0 = __uint_as_float(gv[q] << 16), g1 = __uint_as_float(gv[q] & 0xffff0000u);
+        const float s0 = 1.0f / (1.0f + expf(-g0));
+        const float s1 = 1.0f / (1.0f + expf(-g1));
+        res[q] = pack_f2bf(o[2 * q] * rn * s0, o[2 * q + 1] * rn * s1);
+    }
+    if (store) {
+        const int tok = row >> 3, hj = 8 * g + (row & 7);
+        const size_t qrow = (size_t)r * 8 + tok;
+        *reinterpret_cast<uint4 *>(p.out + qrow * out_cols + (size_t)hj * kHeadDim + 8 * j) =
+            make_uint4(res[0], res[1], res[2], res[3]);
+    }
+}
+
 // kWorkspace = false: the S CTAs of (request, KV head) form a cluster and merge
 // over distributed shared memory.  true: no cluster; each CTA writes its
 // partial to its slot of the caller's workspace and attn2_merge_kernel, the
@@ -664,7 +698,18 @@ __global__ void __launch_bounds__(kA2Threads, 1)
         }
 
         // ---- merge the ranks' partials, o-norm, gate, store (64 / S rows each) ----
-        if (req_ok && table_ok) {
+        if (req_ok && table_ok && S == 1) {
+            // one CTA holds the whole partial: 8 lanes per row, 4 rows per warp at a time
+            const int sub = lane >> 3, j = lane & 7;
+            for (int base = 4 * warp; base < 64; base += 4 * (kA2ComputeWarps + 1)) {
+                const int row = base + sub;
+                const int rr = row < 64 ? row : 63;
+                const float4 oa = *reinterpret_cast<const float4 *>(o_part + rr * kA2OStride + 8 * j);
+                const float4 ob = *reinterpret_cast<const float4 *>(o_part + rr * kA2OStride + 8 * j + 4);
+                const uint4 gw = *reinterpret_cast<const uint4 *>(smem + LY.gate + rr * 128 + 16 * j);
+                a2_finish_row8(p, r, g, row, oa, ob, l_part[rr], j, gw, row < 64);
+            }
+        } else if (req_ok && table_ok) {
             const int rows = 64 / S;
             const uint32_t o_addr = smem_u32(o_part), m_addr = smem_u32(m_part), l_addr = smem_u32(l_part);
             for (int i = warp; i < rows; i += kA2ComputeWarps + 1) {
@@ -673,12 +718,7 @@ __global__ void __launch_bounds__(kA2Threads, 1)
                 // the ranks' partials in rank order (short loops: a fully unrolled
                 // merge over every possible rank cost ~3000 cycles a row)
                 float lt, o0, o1;
-                if (S == 1) {
-                    const float2 v = *reinterpret_cast<const float2 *>(o_part + row * kA2OStride + 2 * lane);
-                    o0 = v.x;
-                    o1 = v.y;
-                    lt = l_part[row];
-                } else {
+                {
                     float M = -INFINITY;
 #pragma unroll 4
                     for (int src = 0; src < S; ++src)
