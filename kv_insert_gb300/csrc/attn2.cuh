@@ -122,13 +122,16 @@ struct Attn2Params {
     float eps;
 };
 
+// `policy`: an L2 cache policy (createpolicy); the cache is streamed once, so
+// its lines go first and the rest of the working set (q, the partials, the
+// code) stays in L2
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *m, uint32_t bar, int c0,
-                                            int c1, int c2, int c3)
+                                            int c1, int c2, int c3, uint64_t policy)
 {
     asm volatile(
-        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "l"(policy)
         : "memory");
 }
 
@@ -346,6 +349,7 @@ __global__ void __launch_bounds__(kA2Threads, 1)
         // skipped by every rank) and page 0 copied instead, so the ring's
         // accounting does not change.
         if (lane == 0) tma_prefetch_map(&tmKV);
+        const uint64_t pol_kv = policy_evict_first();   // the cache is streamed once
         int issued = 0;   // blocks
         unsigned bad = 0u;
         bool stop = false;
@@ -376,9 +380,10 @@ __global__ void __launch_bounds__(kA2Threads, 1)
                     // the block's K rows together, then its V rows: 64 keys of
                     // 128 bytes each, one operand for Q K^T
                     const uint32_t blk = sRing + (uint32_t)rb * (kA2Block * kA2PageBytes);
-                    tma_load_4d(blk + (uint32_t)b * 2048, &tmKV, full0 + 8 * rb, 0, 0, 0, page * p.nkv + g);
+                    tma_load_4d(blk + (uint32_t)b * 2048, &tmKV, full0 + 8 * rb, 0, 0, 0, page * p.nkv + g,
+                                pol_kv);
                     tma_load_4d(blk + (uint32_t)(kA2Block + b) * 2048, &tmKV, full0 + 8 * rb, 0, 0, 1,
-                                page * p.nkv + g);
+                                page * p.nkv + g, pol_kv);
                 }
                 ++issued;
             }
