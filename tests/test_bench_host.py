@@ -97,3 +97,15 @@ def test_all_cores_baseline_shards_reproduce_the_whole_call():
         for t, slot in enumerate(slots):
             page, off = divmod(int(slot), 16)
             assert np.array_equal(shard_cache[0, 0, t], cache[page, g, off]), (g, t)
+
+
+def test_all_cores_baseline_line():
+    """The all-cores oracle baseline reports whole calls per second in the
+    metric's unit, the threads it used and what it ran."""
+    import bench
+    from kv_insert_gb300 import workloads as wl
+    w = wl.WORKLOADS["m1_nkv1_n1152"]
+    line = bench.cpu_baseline_all_cores(wl.make_inputs(w), w, 0.01)
+    assert line["kind"] == "oracle" and line["unit"] == bench.UNIT
+    assert line["value"] > 0 and 1 <= line["cores"] <= (os.cpu_count() or 1)
+    assert "KV-head shards" in line["sample"]
