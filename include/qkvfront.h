@@ -24,6 +24,10 @@
  *     caller and must be 16-byte aligned;
  *   - the library allocates no device memory per call and keeps no state
  *     across calls except a device status word (qkv_front_status);
+ *   - per device it caches, on first use, the kernels' attributes and the
+ *     device address of its no-allocation array (attn2_split_kv_noalloc);
+ *     after cudaDeviceReset on a device, do not call the library on that
+ *     device again in the same process;
  *   - `stream` is a cudaStream_t (NULL: the legacy default stream); calls are
  *     asynchronous on it.  The kernel is launched with programmatic stream
  *     serialization (PDL): it may start while the previous kernel on the
@@ -259,6 +263,24 @@ int attn2(const uint16_t *qkv, const uint16_t *kv_cache, int64_t num_pages,
           int N, int num_kv_heads, int window, float scale, float eps, uint16_t *out,
           void *stream);
 
+/*
+ * attn2_unsupported: why attn2 (and attn2_split_kv / _noalloc, given a valid
+ * workspace and split) would refuse this call, or NULL when it takes it
+ * (page cute_ops, unsupported_attn2).  Host-only checks, no CUDA call except
+ * the device query; returns a static string.  Of the page's refusals, the
+ * layout ones are fixed by this ABI: head_dim 64 and 8 q heads per KV head
+ * are implied by N = 1152 * num_kv_heads, and a layer without the o-norm and
+ * sigmoid gate has nothing to call here (the Python binding's
+ * unsupported_attn2 refuses such a layer).  The page's kernel is built for
+ * one softmax scale and one o-norm eps, whose values the page does not
+ * print; this kernel takes both per call and refuses only scale <= 0 and eps
+ * outside (0, 1].
+ */
+const char *attn2_unsupported(const uint16_t *qkv, const uint16_t *kv_cache, int64_t num_pages,
+                              const int32_t *block_table, int max_blocks, const int32_t *context_lens,
+                              int num_reqs, int N, int num_kv_heads, int window, float scale, float eps,
+                              uint16_t *out);
+
 /* attn2 at an explicit split (1, 2, 4, 8 or 16 CTAs per request and KV head;
  * otherwise QKVF_ERR_VARIANT), for tests and tuning. */
 int attn2_launch_splits(const uint16_t *qkv, const uint16_t *kv_cache, int64_t num_pages,
@@ -313,8 +335,10 @@ int attn2_split_kv_splits(int num_reqs, int num_kv_heads, int max_blocks, int wi
  * the partials go to a file-scope device array of the library, 256 slots of
  * 17152 bytes (4,390,912 bytes), which every GPU that loads the library holds
  * until the process exits.  The call allocates nothing.
- *   num_reqs * num_kv_heads * splits (after splits == 0 is resolved as
- *   attn2_split_kv_splits does) must be <= 256, else QKVF_ERR_SIZES.
+ *   When splits (after splits == 0 is resolved as attn2_split_kv_splits
+ *   does) is above 1, num_reqs * num_kv_heads * splits must be <= 256, else
+ *   QKVF_ERR_SIZES.  At one split the call runs the direct path (each CTA
+ *   finishes its own rows), touches no array slot and takes any num_reqs.
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
  * capture.  The array needs no clearing: a call reads only slots it wrote.

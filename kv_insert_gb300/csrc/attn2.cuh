@@ -32,34 +32,20 @@
 // rows: o-norm, gate, BF16 store.  Split-KV engine: no cluster; the partials
 // go to a caller's workspace and a second grid merges them.
 
-#ifndef A2_GROUPS
-#define A2_GROUPS 3
-#endif
-#ifndef A2_RING_BLOCKS
-#define A2_RING_BLOCKS 12
-#endif
-#ifndef A2_BLOCK
-#define A2_BLOCK 4
-#endif
-#ifndef A2_TC_QK
-#define A2_TC_QK 1   // 0: Q K^T with mma.sync + ldmatrix of K (2 - 3 % slower on GB300)
-#endif
-
 namespace qkvf {
 
-constexpr int kA2Groups = A2_GROUPS;                      // groups of 4 compute warps
+constexpr int kA2Groups = 3;                              // groups of 4 compute warps
 constexpr int kA2ComputeWarps = 4 * kA2Groups;
 constexpr int kA2Threads = 32 * (kA2ComputeWarps + 1);   // the last warp produces
-constexpr int kA2Block = A2_BLOCK;                        // pages per softmax step (16 per page)
-constexpr bool kA2TcQK = A2_TC_QK != 0;                   // Q K^T on tcgen05 (else mma.sync)
+constexpr int kA2Block = 4;                               // pages per softmax step (16 per page)
 constexpr int kA2TmemCols = 256;                          // one 64-column S tile per group
-constexpr int kA2RingBlocks = A2_RING_BLOCKS;
+constexpr int kA2RingBlocks = 12;
 constexpr int kA2Stages = kA2RingBlocks * kA2Block;       // pages in flight per CTA
 // ring slot k % stages always serves group (k / block) % groups: each group
 // waits on its own slots in order, so a full barrier's parity never aliases
 static_assert(kA2RingBlocks % kA2Groups == 0, "ring blocks must be a multiple of the groups");
 static_assert(32 % kA2Block == 0, "a block's table entries lie in one 32-entry chunk");
-static_assert(!kA2TcQK || (kA2Block == 4 && kA2Groups * 64 <= kA2TmemCols), "tcgen05 Q K^T: 64-key blocks");
+static_assert(kA2Block == 4 && kA2Groups * 64 <= kA2TmemCols, "tcgen05 Q K^T: 64-key blocks");
 constexpr uint32_t kA2PageBytes = 4096;                   // K box + V box
 constexpr int kA2OStride = 68;                            // floats per row of the O partial
 constexpr int kA2MaxSplits = 16;
@@ -312,18 +298,16 @@ __global__ void __launch_bounds__(kA2Threads, 1)
             mbar_init(full0 + 8 * s, 1);
             mbar_init(empty0 + 8 * s, 4);   // the 4 warps of the group that owns the block
         }
-        if constexpr (kA2TcQK)
-            for (int q = 0; q < kA2Groups; ++q) mbar_init(smem_u32(smem + LY.sbar) + 8 * q, 1);
+        for (int q = 0; q < kA2Groups; ++q) mbar_init(smem_u32(smem + LY.sbar) + 8 * q, 1);
         s_flags[0] = 0;
         s_flags[1] = 0;
         fence_barrier_init();
         griddep_launch_dependents();
     }
-    if constexpr (kA2TcQK)
-        if (warp == 0) a2_tmem_alloc(smem_u32(smem + LY.tslot));
-    if constexpr (kA2TcQK) tc_fence_before();
+    if (warp == 0) a2_tmem_alloc(smem_u32(smem + LY.tslot));
+    tc_fence_before();
     __syncthreads();
-    if constexpr (kA2TcQK) tc_fence_after();
+    tc_fence_after();
     griddep_wait();   // q, the cache, the table and the lengths come from earlier kernels
 
     // ---- the request: length and visible pages ----------------------------
@@ -423,23 +407,15 @@ __global__ void __launch_bounds__(kA2Threads, 1)
                 *reinterpret_cast<uint4 *>(smem + LY.gate + row * 128 + 16 * cc) = *reinterpret_cast<const uint4 *>(
                     p.qkv + ((size_t)r * 8 + (row >> 3)) * p.N + gate_col + (size_t)(8 * g + (row & 7)) * kHeadDim + 8 * cc);
             }
-            if constexpr (kA2TcQK)   // the tensor cores read Q through the async proxy
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            // the tensor cores read Q through the async proxy
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         }
         a2_compute_bar_sync();
         const int gq = lane >> 2, t = lane & 3;
-        uint32_t qa[4][4];   // the warp's 16 Q rows as mma A fragments (mma.sync Q K^T)
-        if constexpr (!kA2TcQK) {
-            const uint32_t a_row = (uint32_t)(wig * 16 + (lane & 7) + ((lane >> 3) & 1) * 8);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                ldsm_x4(sQ + a_row * 128u + ((((uint32_t)(2 * kk) + (uint32_t)(lane >> 4)) ^ (uint32_t)(lane & 7)) << 4),
-                        qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
-        }
         // tcgen05 Q K^T: the group's S tile [64 rows x 64 keys] in tensor memory
         // columns 64 grp.., rows 16 w .. 16 w + 15 in lanes 32 w .. 32 w + 15
         const uint32_t sbar = smem_u32(smem + LY.sbar) + 8 * grp;
-        const uint32_t tS = kA2TcQK ? *reinterpret_cast<volatile uint32_t *>(smem + LY.tslot) + 64u * grp : 0u;
+        const uint32_t tS = *reinterpret_cast<volatile uint32_t *>(smem + LY.tslot) + 64u * grp;
         const bool issuer = wig == 0 && lane == 0;
         uint32_t sph = 0;            // phase of sbar this block waits for
         int committed = 0, observed = 0;   // the issuer's commits, and those it saw complete
@@ -457,8 +433,6 @@ __global__ void __launch_bounds__(kA2Threads, 1)
             for (int e = 0; e < 4; ++e) o[nd][e] = 0.f;
         float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
 
-        const uint32_t k_key = (uint32_t)((lane & 7) + ((lane >> 4) << 3));   // K: ldmatrix row
-        const uint32_t k_hi = (uint32_t)((lane >> 3) & 1);
         const uint32_t v_key = (uint32_t)((lane & 7) + ((lane >> 3) & 1) * 8); // V: ldmatrix.trans row
         const uint32_t v_hi = (uint32_t)(lane >> 4);
         const uint32_t sw = (uint32_t)(lane & 7);
@@ -479,54 +453,32 @@ __global__ void __launch_bounds__(kA2Threads, 1)
             inside = inside && nb == kA2Block;
             const uint32_t kreg = sRing + (uint32_t)rb * (kA2Block * kA2PageBytes);   // the block's K rows
             const uint32_t vreg = kreg + kA2Block * 2048;                            // then its V rows
-            if constexpr (kA2TcQK) {
-                // every warp of the group is past the previous block's tcgen05.ld
-                tc_fence_before();
-                a2_group_bar_sync(grp);
-                if (issuer && landed) {
-                    tc_fence_after();
+            // every warp of the group is past the previous block's tcgen05.ld
+            tc_fence_before();
+            a2_group_bar_sync(grp);
+            if (issuer && landed) {
+                tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)   // K = 16 dims per instruction: 32 bytes along the rows
-                        umma_bf16(tS, umma_desc_sw128(sQ + 32u * kk), umma_desc_sw128(kreg + 32u * kk),
-                                  umma_idesc_bf16(64, 64), kk != 0 ? 1u : 0u);
-                    umma_commit(sbar);
-                    ++committed;
-                }
-                const bool s_ok = mbar_try_wait(sbar, sph) || bounded_wait(sbar, sph, s_flags, p.wait_limit_ns, true);
-                sph ^= 1u;
-                if (issuer && s_ok) observed = committed;
-                landed = landed && s_ok;
+                for (int kk = 0; kk < 4; ++kk)   // K = 16 dims per instruction: 32 bytes along the rows
+                    umma_bf16(tS, umma_desc_sw128(sQ + 32u * kk), umma_desc_sw128(kreg + 32u * kk),
+                              umma_idesc_bf16(64, 64), kk != 0 ? 1u : 0u);
+                umma_commit(sbar);
+                ++committed;
             }
+            const bool s_ok = mbar_try_wait(sbar, sph) || bounded_wait(sbar, sph, s_flags, p.wait_limit_ns, true);
+            sph ^= 1u;
+            if (issuer && s_ok) observed = committed;
+            landed = landed && s_ok;
             if (__all_sync(0xffffffffu, landed)) {
                 float sc[2 * kA2Block][4];
-                if constexpr (kA2TcQK) {
-                    tc_fence_after();
-                    uint32_t rr[32];
-                    a2_tmem_ld_16x256b_x8(tS + ((uint32_t)(32 * wig) << 16), rr);
-                    tmem_ld_wait();
+                tc_fence_after();
+                uint32_t rr[32];
+                a2_tmem_ld_16x256b_x8(tS + ((uint32_t)(32 * wig) << 16), rr);
+                tmem_ld_wait();
 #pragma unroll
-                    for (int nt = 0; nt < 2 * kA2Block; ++nt)
+                for (int nt = 0; nt < 2 * kA2Block; ++nt)
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) sc[nt][e] = __uint_as_float(rr[4 * nt + e]);
-                } else {
-#pragma unroll
-                    for (int nt = 0; nt < 2 * kA2Block; ++nt)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) sc[nt][e] = 0.f;
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-#pragma unroll
-                        for (int b = 0; b < kA2Block; ++b) {
-                            if (b < nb) {
-                                const uint32_t kbox = kreg + (uint32_t)b * 2048;
-                                uint32_t b0, b1, b2, b3;
-                                ldsm_x4(kbox + k_key * 128u + ((((uint32_t)(2 * kk) + k_hi) ^ sw) << 4), b0, b1, b2, b3);
-                                mma_bf16_16816(sc[2 * b], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
-                                mma_bf16_16816(sc[2 * b + 1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
-                            }
-                        }
-                    }
-                }
+                    for (int e = 0; e < 4; ++e) sc[nt][e] = __uint_as_float(rr[4 * nt + e]);
                 // (near the edges) mask: element e of tile nt = 2 b + h is key
                 // key0(b) + 8 h + 2 t + (e & 1), row a for e < 2
                 if (!inside) {
@@ -619,16 +571,12 @@ __global__ void __launch_bounds__(kA2Threads, 1)
             if (lane == 0)
                 mbar_arrive(empty0 + 8 * rb);
         }
-        if constexpr (kA2TcQK) {
-            if (issuer && committed != observed)   // an abandoned wait: let the MMAs finish first
-                bounded_wait(sbar, (uint32_t)((committed - 1) & 1), s_flags, p.wait_limit_ns, false);
-            tc_fence_before();
-        }
+        if (issuer && committed != observed)   // an abandoned wait: let the MMAs finish first
+            bounded_wait(sbar, (uint32_t)((committed - 1) & 1), s_flags, p.wait_limit_ns, false);
+        tc_fence_before();
         a2_ring_done_sync();   // every group is past the ring; the producer has drained
-        if constexpr (kA2TcQK) {
-            tc_fence_after();
-            if (warp == 0) a2_tmem_dealloc(*reinterpret_cast<volatile uint32_t *>(smem + LY.tslot));
-        }
+        tc_fence_after();
+        if (warp == 0) a2_tmem_dealloc(*reinterpret_cast<volatile uint32_t *>(smem + LY.tslot));
         // whole-row sums across the four threads of a row
 #pragma unroll
         for (int off = 1; off <= 2; off <<= 1) {
@@ -1036,6 +984,21 @@ int attn2(const uint16_t *qkv, const uint16_t *kv_cache, int64_t num_pages,
     const int splits = qkvf::attn2_splits_for(num_reqs, num_kv_heads, max_blocks, window, d->sms);
     return qkvf::launch_attn2(qkv, kv_cache, num_pages, block_table, max_blocks, context_lens,
                               num_reqs, N, num_kv_heads, window, scale, eps, out, splits, nullptr, stream);
+}
+
+const char *attn2_unsupported(const uint16_t *qkv, const uint16_t *kv_cache, int64_t num_pages,
+                              const int32_t *block_table, int max_blocks, const int32_t *context_lens,
+                              int num_reqs, int N, int num_kv_heads, int window, float scale, float eps,
+                              uint16_t *out)
+{
+    int code;
+    const char *why = qkvf::check_attn2_args(qkv, kv_cache, num_pages, block_table, max_blocks,
+                                             context_lens, num_reqs, N, num_kv_heads, window, scale,
+                                             eps, out, &code);
+    if (why) return why;
+    qkvf::DeviceState *d;
+    const int rc = qkvf::probe_device(&d);
+    return rc == QKVF_OK ? nullptr : qkv_front_strerror(rc);
 }
 
 int attn2_launch_splits(const uint16_t *qkv, const uint16_t *kv_cache, int64_t num_pages,

@@ -16,9 +16,11 @@
 // HBM-bound elementwise work: per token it reads the 9 nkv q/k heads and the
 // nkv v heads (contiguous in the row: 1280 nkv bytes) and its cos|sin row,
 // and writes the q/k heads back and 2 nkv slot halves.  A producer warp
-// streams whole token regions into a shared-memory ring with bulk copies
-// (up to ~100 KB in flight per CTA, two CTAs per SM); consumer warps work
-// from shared memory, 16 bytes per lane.
+// copies each token's region and table row into a shared-memory ring with
+// 16-byte cp.async from its 32 lanes (up to ~100 KB in flight per CTA, two
+// CTAs per SM); consumer warps work from shared memory, 16 bytes per lane.
+// (A bulk copy per token costs the SM's TMA unit ~0.2 us whatever its size,
+// which set the pace at two copies per token; 32 lanes of cp.async do not.)
 
 namespace qkvf {
 
@@ -39,18 +41,8 @@ struct EpiParams {
 constexpr int kEpiConsumerWarps = 8;
 constexpr int kEpiThreads = 32 * (kEpiConsumerWarps + 1);   // warp 0 produces
 constexpr int kEpiMaxTokens = 1 << 24;
-#ifndef EPI_CTAS_PER_SM
-#define EPI_CTAS_PER_SM 2
-#endif
-constexpr int kEpiCtasPerSm = EPI_CTAS_PER_SM;
-#ifndef EPI_CPASYNC
-#define EPI_CPASYNC 1
-#endif
-// token regions by 16-byte cp.async from the producer warp's 32 lanes (a
-// bulk copy costs the SM's TMA unit ~0.2 us whatever its size, which set
-// this kernel's pace at two copies per token), else by bulk copies
-constexpr bool kEpiCpAsync = EPI_CPASYNC != 0;
-constexpr int kEpiRingBudget = (kEpiCtasPerSm >= 3 ? 64 : 100) * 1024;   // per CTA
+constexpr int kEpiCtasPerSm = 2;
+constexpr int kEpiRingBudget = 100 * 1024;   // per CTA: two rings fit one SM
 constexpr int kEpiMaxSlots = 16;
 
 // bytes of one token's ring slot: its q | k | v heads, its cos|sin row, and a
@@ -171,18 +163,9 @@ __device__ __forceinline__ uint4 rope4_pairs(const uint64_t (&ev)[2], const uint
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
-{
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            dst),
-        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-        : "memory");
-}
-
 // CTA b takes tokens b, b + G, b + 2G, ... (G = gridDim.x).  Warp 0 copies
 // each token's q | k | v region (contiguous in its row) and its cos|sin row
-// into a ring slot with bulk copies; warps 1..8 take the token's heads in
+// into a ring slot with 16-byte cp.async; warps 1..8 take the token's heads in
 // groups of 8 (lane l: head 8 g + l / 4, columns 8c..8c+7 and 32+8c..32+8c+7
 // with c = l % 4), norm and
 // rotate q / k heads in place in global memory and write k / v heads into the
@@ -205,8 +188,8 @@ __global__ void __launch_bounds__(kEpiThreads, kEpiCtasPerSm) qknorm_rope_kv_ins
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < nslots; ++s) {
-            // cp.async: the 32 lanes' copies land (32) and lane 0's header (1)
-            mbar_init(full0 + 8 * s, kEpiCpAsync ? 33 : 1);
+            // the 32 lanes' copies land (32) and lane 0's header (1)
+            mbar_init(full0 + 8 * s, 33);
             mbar_init(empty0 + 8 * s, (heads + 7) >> 3);   // one arrival per 8-head group
         }
         *s_abort = 0;
@@ -217,9 +200,9 @@ __global__ void __launch_bounds__(kEpiThreads, kEpiCtasPerSm) qknorm_rope_kv_ins
     griddep_wait();   // qkv, indices and table are written by the kernels before this one
 
     if (warp == 0) {
-        // ---- produce: 32 tokens' indices per warp load, one bulk copy per row ----
+        // ---- produce: 32 tokens' indices per warp load, then each token's copies ----
         unsigned bad = 0u;
-        int i = 0, issued = 0;
+        int i = 0;
         bool stop = false;
         for (int64_t tb = blockIdx.x; tb < p.T && !stop; tb += 32 * G) {
             const int64_t tl = tb + lane * G;
@@ -254,34 +237,20 @@ __global__ void __launch_bounds__(kEpiThreads, kEpiCtasPerSm) qknorm_rope_kv_ins
                     hdr[1] = sl;
                     hdr[2] = (pos_ok ? 1 : 0) | (ins ? 2 : 0);
                 }
-                if constexpr (kEpiCpAsync) {
-                    const uint8_t *src = reinterpret_cast<const uint8_t *>(p.qkv + (size_t)t * p.N);
-                    for (uint32_t c = (uint32_t)lane; c < region / 16; c += 32)
-                        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(base) + 16 * c),
-                                     "l"(src + 16 * c)
-                                     : "memory");
-                    if (pos_ok && lane < kHeadDim * 4 / 16)
-                        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(base + region) + 16 * lane),
-                                     "l"(reinterpret_cast<const uint8_t *>(p.cos_sin + pos * kHeadDim) + 16 * lane)
-                                     : "memory");
-                    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-                    if (lane == 0) mbar_arrive(bar);   // the header
-                } else if (lane == 0) {
-                    mbar_expect_tx(bar, region + (pos_ok ? kHeadDim * 4 : 0));
-                    bulk_load(smem_u32(base), p.qkv + (size_t)t * p.N, region, bar);
-                    if (pos_ok)
-                        bulk_load(smem_u32(base + region), p.cos_sin + pos * kHeadDim, kHeadDim * 4, bar);
-                }
-                ++issued;
+                const uint8_t *src = reinterpret_cast<const uint8_t *>(p.qkv + (size_t)t * p.N);
+                for (uint32_t c = (uint32_t)lane; c < region / 16; c += 32)
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(base) + 16 * c),
+                                 "l"(src + 16 * c)
+                                 : "memory");
+                if (pos_ok && lane < kHeadDim * 4 / 16)
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(base + region) + 16 * lane),
+                                 "l"(reinterpret_cast<const uint8_t *>(p.cos_sin + pos * kHeadDim) + 16 * lane)
+                                 : "memory");
+                asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+                if (lane == 0) mbar_arrive(bar);   // the header
             }
         }
-        if constexpr (kEpiCpAsync) asm volatile("cp.async.wait_all;" ::: "memory");   // nothing left in flight
-        if (!kEpiCpAsync && lane == 0 && *s_abort) {   // drain our copies before leaving
-            const int first = issued > nslots ? issued - nslots : 0;
-            for (int k = first; k < issued; ++k)
-                bounded_wait(full0 + 8 * (k % nslots), (uint32_t)((k / nslots) & 1), s_abort,
-                             p.wait_limit_ns, false);
-        }
+        asm volatile("cp.async.wait_all;" ::: "memory");   // nothing of ours left in flight
         bad = __reduce_or_sync(0xffffffffu, bad);
         if (lane == 0 && bad != 0u) atomicOr(&g_status, bad);
     } else {

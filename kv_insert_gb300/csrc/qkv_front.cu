@@ -625,16 +625,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         // tensor-memory sub-partition w; warp w reads its own sub-partition.
         const bool ready = mbar_try_wait(done_bar, 0) ||
                            bounded_wait(done_bar, 0, s_abort, p.wait_limit_ns, false);
-        (void)ready;
         __syncwarp();
         tc_fence_after();
         const uint32_t taddr = tmem_d + ((uint32_t)(warp * 32) << 16);
         uint32_t r[MT];
-        if constexpr (MT == 8)
-            tmem_ld_x8(taddr, r);
-        else
-            tmem_ld_x16(taddr, r);
-        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < MT; ++i) r[i] = 0u;
+        // a timed-out wait leaves the MMAs possibly running: the accumulator
+        // is not read (the call's outputs are invalid and flagged anyway)
+        if (__all_sync(0xffffffffu, ready)) {
+            if constexpr (MT == 8)
+                tmem_ld_x8(taddr, r);
+            else
+                tmem_ld_x16(taddr, r);
+            tmem_ld_wait();
+        }
         if (lane < 16) {
 #pragma unroll
             for (int tok = 0; tok < MT; ++tok)
@@ -733,6 +738,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if constexpr (TC) {
         if (warp == 0) {   // every tensor-memory read is done
+            // and every issued MMA: the issuer (lane 0 of this warp) committed
+            // done_bar before this point, so after a timed-out wait above the
+            // MMAs still end within the bounded wait here
+            if (!mbar_try_wait(done_bar, 0)) bounded_wait(done_bar, 0, s_abort, p.wait_limit_ns, false);
+            __syncwarp();
             tc_fence_after();
             tmem_dealloc(tmem_d);
         }
@@ -1409,13 +1419,17 @@ int attn2_split_kv_noalloc(const uint16_t *qkv, const uint16_t *kv_cache, int64_
         return code;
     if (splits < 0 || splits > qkvf::kA2WsMaxSplits) return QKVF_ERR_VARIANT;
     if (num_reqs == 0) return QKVF_OK;
-    if (splits > 0 && (int64_t)num_reqs * num_kv_heads * splits > qkvf::kNoAllocSlots)
+    // one split writes no partials: only splits > 1 use the array's slots
+    if (splits > 1 && (int64_t)num_reqs * num_kv_heads * splits > qkvf::kNoAllocSlots)
         return QKVF_ERR_SIZES;   // more partial slots than the array holds
     qkvf::DeviceState *d;
     int rc = qkvf::probe_device(&d);
     if (rc != QKVF_OK) return rc;
     if (splits == 0)
         splits = qkvf::attn2_split_kv_splits_for(num_reqs, num_kv_heads, max_blocks, window, d->sms);
+    if (splits == 1)   // the direct path: each CTA finishes its own rows, no scratch
+        return qkvf::launch_attn2(qkv, kv_cache, num_pages, block_table, max_blocks, context_lens,
+                                  num_reqs, N, num_kv_heads, window, scale, eps, out, 1, nullptr, stream);
     if ((int64_t)num_reqs * num_kv_heads * splits > qkvf::kNoAllocSlots) return QKVF_ERR_SIZES;
     void *scratch = nullptr;
     rc = qkvf::noalloc_scratch(&scratch);

@@ -101,6 +101,8 @@ def load() -> ctypes.CDLL:
         a2 = [vp, vp, i64, vp, i32, vp, i32, i32, i32, i32, ctypes.c_float, ctypes.c_float, vp]
         lib.attn2.argtypes = a2 + [vp]
         lib.attn2.restype = i32
+        lib.attn2_unsupported.argtypes = a2
+        lib.attn2_unsupported.restype = ctypes.c_char_p
         lib.attn2_launch_splits.argtypes = a2 + [i32, vp]
         lib.attn2_launch_splits.restype = i32
         lib.attn2_splits.argtypes = [i32, i32, i32, i32]
@@ -161,14 +163,29 @@ def token_tiles(m: int) -> int:
     return (m + 7) // 8
 
 
+def head_spans(num_kv_heads: int) -> dict:
+    """Column range [start, end) of each head kind in an output row: the
+    kinds follow one another as q, k, v, gate, with Q_PER_KV q and gate
+    heads and one k and one v head per KV head, HEAD_DIM columns each."""
+    counts = (("q", Q_PER_KV), ("k", 1), ("v", 1), ("gate", Q_PER_KV))
+    spans, col = {}, 0
+    for kind, per_kv in counts:
+        width = per_kv * num_kv_heads * HEAD_DIM
+        spans[kind] = (col, col + width)
+        col += width
+    return spans
+
+
 def split_qkv(qkv: torch.Tensor, num_kv_heads: int):
-    """The q and gate column views of the front's output rows [q | k | v | gate]."""
-    q_width = Q_PER_KV * num_kv_heads * HEAD_DIM
-    kv_width = num_kv_heads * HEAD_DIM
-    if qkv.dim() != 2 or qkv.shape[1] != 2 * q_width + 2 * kv_width:
-        raise ValueError(f"qkv must be [tokens, {2 * q_width + 2 * kv_width}] for "
-                         f"{num_kv_heads} KV heads, got {tuple(qkv.shape)}")
-    return qkv[:, :q_width], qkv[:, q_width + 2 * kv_width:]
+    """Views of the q heads and of the gate heads of the front's output rows
+    (what attn2 reads), taken from the row layout of head_spans."""
+    spans = head_spans(num_kv_heads)
+    row = spans["gate"][1]
+    if qkv.dim() != 2 or qkv.shape[1] != row:
+        raise ValueError(f"split_qkv: a layer with {num_kv_heads} KV heads has output rows of "
+                         f"{row} columns; this tensor has shape {tuple(qkv.shape)}")
+    (q0, q1), (g0, g1) = spans["q"], spans["gate"]
+    return qkv[:, q0:q1], qkv[:, g0:g1]
 
 
 def _tensor_reason(x, weight, positions, cos_sin, slots, kv_cache, out):
@@ -228,9 +245,12 @@ def unsupported(x, weight, positions, cos_sin, slots, kv_cache, out=None) -> str
 
 
 def supports_call(x, weight, positions, cos_sin, slots, kv_cache, num_kv_heads, out=None) -> bool:
-    """Whether the front takes this call of a layer with num_kv_heads."""
-    return (unsupported(x, weight, positions, cos_sin, slots, kv_cache, out) is None
-            and kv_cache.shape[1] == num_kv_heads)
+    """Whether the front takes this call of a layer with num_kv_heads: the
+    cache must hold exactly the layer's KV heads, and every check of
+    `unsupported` must pass (otherwise the caller keeps its unfused path)."""
+    if kv_cache.dim() != 4 or kv_cache.shape[1] != num_kv_heads:
+        return False
+    return not unsupported(x, weight, positions, cos_sin, slots, kv_cache, out)
 
 
 def qkv_front(x, weight, positions, slots, cos_sin, kv_cache, out=None, stream=None):
@@ -476,6 +496,40 @@ def _attn2_args(qkv, kv_cache, block_table, context_lens, out, window, scale, ep
             block_table.shape[1], context_lens.data_ptr(), R, N, nkv, int(window), float(scale),
             float(eps), out.data_ptr())
     return out, args
+
+
+def unsupported_attn2(layer) -> str | None:
+    """Why attn2 cannot compute this attention layer, or None (page cute_ops,
+    unsupported_attn2).  `layer` is any object with the attention layer's
+    attributes use_o_norm, use_o_gate, head_dim, num_heads, num_kv_heads,
+    scaling and rms_norm_eps.  attn2 is the o-norm + sigmoid-gate variant of
+    the verify-step attention with 64-wide heads and 8 q heads per KV head;
+    its scale and eps are call arguments (scale > 0, eps in (0, 1])."""
+    if not layer.use_o_norm or not layer.use_o_gate:
+        return "a layer without both the output RMS norm and the sigmoid output gate"
+    if layer.head_dim != HEAD_DIM:
+        return f"heads of {layer.head_dim} dims (attn2 has {HEAD_DIM})"
+    if layer.num_kv_heads < 1 or layer.num_heads != Q_PER_KV * layer.num_kv_heads:
+        return (f"{layer.num_heads} q heads over {layer.num_kv_heads} KV heads "
+                f"(attn2 has {Q_PER_KV} q heads per KV head)")
+    if not layer.scaling > 0:
+        return f"a softmax scale of {layer.scaling} (attn2 takes a positive scale)"
+    if not 0 < layer.rms_norm_eps <= 1:
+        return f"an o-norm eps of {layer.rms_norm_eps} (attn2 takes eps in (0, 1])"
+    return None
+
+
+def attn2_unsupported_call(qkv, kv_cache, block_table, context_lens, out, window: int = 0,
+                           scale: float = 0.125, eps: float = 1e-6) -> str | None:
+    """Why attn2 would refuse this call into `out` (the binding's tensor
+    checks, then the C ABI's host checks), or None."""
+    try:
+        out, args = _attn2_args(qkv, kv_cache, block_table, context_lens, out, window, scale, eps)
+    except ValueError as e:
+        return str(e)
+    with torch.cuda.device(qkv.device):
+        r = load().attn2_unsupported(*args)
+    return None if r is None else r.decode()
 
 
 def attn2(qkv, kv_cache, block_table, context_lens, out=None, window: int = 0,

@@ -262,3 +262,53 @@ def test_unsupported_projection_reasons():
     assert qf.unsupported_projection(w, cos_sin=torch.zeros(16, 64)) is None
     assert "1152" in qf.unsupported_projection(torch.zeros(2000, 8192, dtype=torch.bfloat16))
     assert "shape" in qf.unsupported_projection(torch.zeros(2304, 4096, dtype=torch.bfloat16))
+
+
+def test_attn2_unsupported_reasons(lib):
+    """The C ABI's attn2_unsupported gives the reason of each host refusal
+    (NULL only past the checks, at the device query, which has no GPU here)."""
+    f = lib.attn2_unsupported
+    ok = dict(q=X, c=CACHE, pages=64, bt=POS, mb=8, cl=SL, R=2, N=2304, nkv=2, win=0, sc=0.125,
+              eps=1e-6, out=OUT)
+
+    def why(**kw):
+        a = dict(ok, **kw)
+        r = f(a["q"], a["c"], a["pages"], a["bt"], a["mb"], a["cl"], a["R"], a["N"], a["nkv"],
+              a["win"], a["sc"], a["eps"], a["out"])
+        return None if r is None else r.decode()
+    assert "num_reqs" in why(R=-1)
+    assert "1152" in why(N=1152)
+    assert "num_kv_heads" in why(nkv=0)
+    assert "window" in why(win=-1)
+    assert "scale" in why(sc=0.0) and "eps" in why(eps=2.0) and "eps" in why(eps=0.0)
+    assert "NULL" in why(q=0)
+    assert "aligned" in why(q=X + 8)
+    assert "overlaps" in why(out=X)
+    # past every check the device query answers (no GB300 here)
+    assert why() in ("a CUDA call failed", "the current GPU is not compute capability 10.3 (sm_103a)")
+
+
+def test_unsupported_attn2_layer_reasons():
+    """The binding's layer check (page cute_ops, unsupported_attn2): a layer
+    without the o-norm and sigmoid gate, another head_dim or q / KV ratio, and
+    a scale or eps outside what the kernel takes are refused."""
+    from types import SimpleNamespace as L
+    base = dict(use_o_norm=True, use_o_gate=True, head_dim=64, num_heads=64, num_kv_heads=8,
+                scaling=0.125, rms_norm_eps=1e-6)
+    assert qf.unsupported_attn2(L(**base)) is None
+    assert "gate" in qf.unsupported_attn2(L(**dict(base, use_o_gate=False)))
+    assert "norm" in qf.unsupported_attn2(L(**dict(base, use_o_norm=False)))
+    assert "128 dims" in qf.unsupported_attn2(L(**dict(base, head_dim=128)))
+    assert "q heads" in qf.unsupported_attn2(L(**dict(base, num_heads=32)))
+    assert "scale" in qf.unsupported_attn2(L(**dict(base, scaling=0.0)))
+    assert "eps" in qf.unsupported_attn2(L(**dict(base, rms_norm_eps=0.0)))
+    assert qf.unsupported_attn2(L(**dict(base, scaling=0.0883883))) is None
+
+
+def test_noalloc_refusals_without_a_device(lib):
+    """Above one split the 256-slot bound is checked before any device query;
+    at one split (no slots used) the same shape gets past it."""
+    f = lib.attn2_split_kv_noalloc
+    args = (X, CACHE, 256, POS, 8, SL, 40, 9216, 8, 0, 0.125, 1e-6, OUT)
+    assert f(*args, 2, None) == 7        # 40 x 8 x 2 = 640 slots > 256
+    assert f(*args, 1, None) in (5, 6)   # one split: reaches the device query
