@@ -12,13 +12,21 @@ us_per_call.
 
 Timing: W is rotated over R device copies with R x |W| >= 3 x L2, so every
 call streams its weights from HBM; calls are captured in CUDA graphs (their
-PDL edges kept) and timed with CUDA events on the launching stream; the max
-over ranks is taken.  Multi-GPU runs are independent replicas (each rank one
+PDL edges kept) and timed with CUDA events on the launching stream.  A timed
+region is exactly --steps calls, bracketed by a barrier and a device
+synchronize on both sides; a short spin kernel queued ahead of the region's
+start event covers the host's graph launch, as GPU benchmark harnesses do.
+Regions repeat until at least --min-seconds of timed GPU work; the line
+reports the median region (p10 / p90 beside it), the max over ranks, and the
+SM clocks nvidia-smi saw during the regions.  `per_config` repeats the
+measurement (back-to-back graph replays) on every workload of the metric's
+M = 1..16 range.  Multi-GPU runs are independent replicas (each rank one
 tensor-parallel shard of KV heads; no collective on the data path).
 """
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import math
@@ -53,13 +61,21 @@ OP_SOURCES = {
     "attn2_split_kv": ("qkv_front.cu", "attn2.cuh"),
 }
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
+# every workload of the metric's range, each measured in the same run
+PER_CONFIG = (["m1_nkv1_n1152", "m8_nkv8_n9216", "m16_nkv8_n9216_consecutive"]
+              + [f"sweep_m{m}_nkv8_n9216" for m in wl.SWEEP_M] + ["m8_nkv16_n18432"])
+SPIN_CYCLES = 100_000   # ~50 us at 2 GHz: the region's graph is queued before it starts
 
 
 def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=96)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--min-seconds", type=float, default=1.0,
+                    help="repeat the timed region of --steps calls until this much timed GPU work")
+    ap.add_argument("--per-config-seconds", type=float, default=0.3,
+                    help="timed GPU work per workload of the per_config records (0: skip them)")
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--op", choices=("qkv_front", "qknorm_rope_kv_insert", "chain", "attn2"),
                     default="qkv_front",
@@ -172,16 +188,25 @@ def recorded_traffic(op: str, workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled while the GPU works."""
+    """nvidia-smi clocks and throttle reasons sampled while the GPU works.
+    Every sample carries nvidia-smi's own timestamp, so a summary can keep
+    only the samples taken inside a timed window (host wall-clock times from
+    `now()`)."""
 
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
         self.file = None
+        self.rows = []
+
+    @staticmethod
+    def now() -> datetime.datetime:
+        return datetime.datetime.now()
 
     def start(self):
         try:
@@ -194,8 +219,9 @@ class ClockSampler:
             self.proc = None
 
     def stop(self):
+        """Ends sampling and parses the samples (kept for `summary`)."""
         if self.proc is None:
-            return None
+            return
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -203,28 +229,84 @@ class ClockSampler:
             self.proc.kill()
         self.file.flush()
         self.file.seek(0)
-        rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.strip()]
+        text = self.file.read()
         self.file.close()
         os.unlink(self.file.name)
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
-            r = [c.strip() for c in r]
-            if len(r) < 9:
+        self.rows = self.parse(text)
+
+    @classmethod
+    def parse(cls, text: str) -> list:
+        rows = []
+        for line in text.strip().splitlines():
+            r = [c.strip() for c in line.split(",")]
+            if len(r) < 10:
                 continue
             try:
-                sm.append(float(r[1]))
-                mx.append(float(r[2]))
+                ts = datetime.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f")
+                sm, mx = float(r[2]), float(r[3])
             except ValueError:
                 continue
-            for name, flag in zip(names, r[5:9]):
-                if flag.lower() == "active":
-                    reasons.add(name)
-        if not sm:
+            reasons = {n for n, f in zip(cls.REASONS, r[6:10]) if f.lower() == "active"}
+            rows.append((ts, sm, mx, reasons))
+        return rows
+
+    def summary(self, t0=None, t1=None):
+        """Median SM clock, max clock and throttle reasons of the samples
+        taken in [t0, t1] (all samples when no window is given), or None."""
+        rows = [r for r in self.rows if (t0 is None or r[0] >= t0) and (t1 is None or r[0] <= t1)]
+        if not rows:
             return None
-        busy = [s for s in sm if s > 0.5 * max(sm)] or sm
-        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        sm = [r[1] for r in rows]
+        reasons = set().union(*[r[3] for r in rows])
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(r[2] for r in rows),
+                "sm_mhz_min": min(sm), "reasons": sorted(reasons), "samples": len(rows),
+                "window": "samples taken while the timed work ran"}
+
+
+def spin(stream):
+    """A short device-side spin queued ahead of a timed region (outside it),
+    so the region's start event fires only after the host has queued the
+    region's work: the region measures the GPU, not the host's launch."""
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(SPIN_CYCLES)
+
+
+def time_regions(region, stream, dev, min_seconds: float, min_regions: int = 3,
+                 max_regions: int = 100000):
+    """Times `region()` (which queues exactly one region's calls on `stream`)
+    repeatedly: each time bracketed by a barrier and a device synchronize on
+    both sides, with CUDA events on `stream` right around the region.  Runs
+    `min_regions` first to size the count, then as many as make
+    `min_seconds` of timed GPU work (the same count on every rank).  Returns
+    (seconds of each region, wall-clock window of the timed regions)."""
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def one():
+        barrier()
+        torch.cuda.synchronize(dev)
+        spin(stream)
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            region()
+            end.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        return start.elapsed_time(end) / 1e3
+
+    est = statistics.median([one() for _ in range(min_regions)])
+    n = int(min(max_regions, max(min_regions, math.ceil(min_seconds / max(est, 1e-9)))))
+    n = int(max_over_ranks(float(n), dev))
+    t0 = ClockSampler.now()
+    times = [one() for _ in range(n)]
+    return times, (t0, ClockSampler.now())
+
+
+def region_stats(times: list, steps: int) -> dict:
+    """Median, p10 and p90 of the regions in microseconds per call."""
+    q = np.percentile(np.asarray(times), [10, 50, 90]) / steps * 1e6
+    return {"us_per_call_p10": float(q[0]), "us_per_call_median": float(q[1]),
+            "us_per_call_p90": float(q[2]), "regions": len(times),
+            "timed_seconds": float(sum(times))}
 
 
 # ---- the CPU oracle (baseline and reference arm) ---------------------------
@@ -377,6 +459,93 @@ def run_reference(args, w: wl.Workload):
 
 # ---- our arm ----------------------------------------------------------------
 
+def front_setup(qf, w: wl.Workload, dev, stream, graph_calls: int, inp=None):
+    """Device inputs of a front workload, W rotated over enough copies to
+    exceed 3 x L2, and a capture helper.  Returns a dict of the pieces."""
+    inp = wl.make_inputs(w) if inp is None else inp
+    g = {k: v.to(dev) for k, v in inp.items()}
+    qf.prepare(w.N, w.num_kv_heads)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    w_bytes = w.N * wl.HIDDEN * 2
+    copies = max(2, math.ceil(3 * l2 / w_bytes))
+    Ws = [g["W"]] + [g["W"].clone() for _ in range(copies - 1)]
+    torch.cuda.synchronize(dev)   # W is read before the PDL wait: no writer may be in flight
+    out = torch.empty(w.M, w.N, dtype=torch.bfloat16, device=dev)
+    per_graph = max(copies, (graph_calls // copies) * copies)
+
+    def call(i):
+        qf.launch(g["x"], Ws[i % copies], g["positions"], g["slots"], g["cos_sin"],
+                  g["kv_cache"], out)
+
+    def capture(n, start=0):
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(n):
+                call(start + i)
+        return graph
+
+    return {"inp": inp, "g": g, "Ws": Ws, "copies": copies, "out": out, "call": call,
+            "capture": capture, "per_graph": per_graph, "l2": l2, "w_bytes": w_bytes}
+
+
+def per_config_records(qf, dev, stream, sampler, seconds: float, graph_calls: int) -> list:
+    """Every workload of the metric's range measured the same way: a CUDA
+    graph of PDL-linked calls (W rotated past L2) replayed back to back, each
+    replay timed by CUDA events on the stream, until `seconds` of timed work;
+    the median replay per call, its p10 / p90, GB/s and fraction of the
+    measured copy peak, and the clocks sampled while the replays ran."""
+    peak, peak_kind = hbm_peak()
+    recs = []
+    for name in PER_CONFIG:
+        w = wl.WORKLOADS[name]
+        f = front_setup(qf, w, dev, stream, graph_calls)
+        with torch.cuda.stream(stream):
+            for i in range(8):
+                f["call"](i)
+        stream.synchronize()
+        graph = f["capture"](f["per_graph"])
+        with torch.cuda.stream(stream):
+            graph.replay()
+        stream.synchronize()
+        if qf.status():
+            raise RuntimeError(f"device status raised during the warm-up of {name}")
+        # size the run from one replay
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        reps = int(min(5000, max(20, math.ceil(seconds / max(e0.elapsed_time(e1) / 1e3, 1e-6)))))
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+        t0 = sampler.now()
+        with torch.cuda.stream(stream):
+            evs[0].record(stream)
+            for k in range(reps):
+                graph.replay()
+                evs[k + 1].record(stream)
+        torch.cuda.synchronize(dev)
+        t1 = sampler.now()
+        if qf.status():
+            raise RuntimeError(f"device status raised while timing {name}")
+        per_replay = np.asarray([evs[k].elapsed_time(evs[k + 1]) for k in range(reps)]) / 1e3
+        q = np.percentile(per_replay, [10, 50, 90]) / f["per_graph"] * 1e6
+        gbs = w.roofline_bytes() / (q[1] * 1e-6) / 1e9
+        recs.append({
+            "workload": name, "M": w.M, "N": w.N, "num_kv_heads": w.num_kv_heads,
+            "variant": qf.variant_full(w.N, w.M),
+            "us_per_call": float(q[1]), "us_per_call_p10": float(q[0]),
+            "us_per_call_p90": float(q[2]), "bytes_per_call": w.roofline_bytes(), "gbs": gbs,
+            "frac": gbs / peak, "frac_of_measured_peak": gbs / peak, "peak_kind": peak_kind,
+            "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS,
+            "calls": reps * f["per_graph"], "graph_calls": f["per_graph"],
+            "l2": f"W rotated over {f['copies']} copies of {f['w_bytes'] / 1e6:.1f} MB",
+            "clocks": sampler.summary(t0, t1)})
+        del f, graph
+        torch.cuda.empty_cache()
+    return recs
+
+
 def run_ours(args, w: wl.Workload):
     from kv_insert_gb300 import qkv_front as qf
 
@@ -388,39 +557,21 @@ def run_ours(args, w: wl.Workload):
     dist_init("nccl")
     qf.load()
 
-    inp = wl.make_inputs(w)
-    g = {k: v.to(dev) for k, v in inp.items()}
-    M, N, nkv = w.M, w.N, w.num_kv_heads
-    qf.prepare(N, nkv)
-    variant = qf.variant_full(N, M)
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    w_bytes = N * wl.HIDDEN * 2
-    copies = max(2, math.ceil(3 * l2 / w_bytes))
-    Ws = [g["W"]] + [g["W"].clone() for _ in range(copies - 1)]
-    torch.cuda.synchronize(dev)   # W is read before the PDL wait: no writer may be in flight
-    out = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.Stream(device=dev)
-    per_graph = max(copies, (args.graph_calls // copies) * copies)
-
-    def call(i):
-        qf.launch(g["x"], Ws[i % copies], g["positions"], g["slots"], g["cos_sin"],
-                  g["kv_cache"], out)
-
-    def capture(n, start):
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
-            for i in range(n):
-                call(start + i)
-        return graph
+    f = front_setup(qf, w, dev, stream, args.graph_calls)
+    inp, g, Ws, copies, out = f["inp"], f["g"], f["Ws"], f["copies"], f["out"]
+    M, N = w.M, w.N
+    variant = qf.variant_full(N, M)
+    per_graph = f["per_graph"]
 
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
-            call(i)
+            f["call"](i)
     stream.synchronize()
     assert qf.status() == 0, "device status raised during warm-up"
     full, rem = divmod(args.steps, per_graph)
-    g_full = capture(per_graph, 0) if full else None
-    g_rem = capture(rem, 0) if rem else None
+    g_full = f["capture"](per_graph) if full else None
+    g_rem = f["capture"](rem) if rem else None
     # graph upload before timing (part of set-up, not a timed step)
     with torch.cuda.stream(stream):
         if g_full:
@@ -429,28 +580,22 @@ def run_ours(args, w: wl.Workload):
             g_rem.replay()
     stream.synchronize()
 
-    sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.3)
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
-    torch.cuda.synchronize(dev)
-    with torch.cuda.stream(stream):
-        start.record(stream)
+    def region():
         for _ in range(full):
             g_full.replay()
         if g_rem:
             g_rem.replay()
-        end.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier()
-    clocks = sampler.stop()
-    el = start.elapsed_time(end) / 1e3
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    times, (t0, t1) = time_regions(region, stream, dev, args.min_seconds)
     st = qf.status()
     if st:
         raise RuntimeError(f"device status {st:#x} raised in the timed region")
-    el_max = max_over_ranks(el, dev)
+    el_med = statistics.median(times)
+    el_max = max_over_ranks(el_med, dev)
     res = aggregate(w.roofline_bytes(), args.steps, world, el_max)
+    stats = region_stats(times, args.steps)
 
     # the same calls on one W copy (the warm case: whatever of W the L2 keeps
     # between calls is not re-read), outside the timed region, labelled
@@ -462,7 +607,7 @@ def run_ours(args, w: wl.Workload):
         warm_graph.replay()
     stream.synchronize()
     w_start, w_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    warm_reps = max(1, min(20, args.steps // per_graph))
+    warm_reps = 20
     with torch.cuda.stream(stream):
         w_start.record(stream)
         for _ in range(warm_reps):
@@ -484,29 +629,35 @@ def run_ours(args, w: wl.Workload):
         def e2e_step(i):
             # one library call: host x / positions / slots in, the front, out back to host
             qf.qkv_front_from_host(xh, ph, sh, oh, Ws[i % copies], g["cos_sin"], g["kv_cache"],
-                                   staging)
+                                   staging, stream=stream)
 
-        with torch.cuda.stream(stream):
-            for i in range(args.warmup):
-                e2e_step(i)
+        for i in range(args.warmup):
+            e2e_step(i)
         stream.synchronize()
-        e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        barrier()
-        torch.cuda.synchronize(dev)
-        with torch.cuda.stream(stream):
-            e_start.record(stream)
+
+        def e2e_region():
             for i in range(args.steps):
                 e2e_step(i)
-            e_end.record(stream)
-        torch.cuda.synchronize(dev)
-        barrier()
-        e_el = max_over_ranks(e_start.elapsed_time(e_end) / 1e3, dev)
+
+        e_times, _ = time_regions(e2e_region, stream, dev, args.min_seconds / 2)
+        if qf.status():
+            raise RuntimeError("device status raised in the end-to-end leg")
+        e_el = max_over_ranks(statistics.median(e_times), dev)
         e_res = aggregate(w.roofline_bytes(), args.steps, world, e_el)
         e2e = {"value": e_res["value"], "unit": UNIT, "us_per_call": e_res["us_per_call"],
                "h2d_bytes_per_step": xh.numel() * 2 + ph.numel() * 8 + sh.numel() * 8,
-               "d2h_bytes_per_step": oh.numel() * 2}
-        if qf.status():
-            raise RuntimeError("device status raised in the end-to-end leg")
+               "d2h_bytes_per_step": oh.numel() * 2,
+               "timing": f"median of {len(e_times)} regions of {args.steps} library calls from "
+                         "pinned host buffers"}
+
+    per_config = None
+    if args.per_config_seconds > 0 and rank == 0:
+        del warm_graph, g_full, g_rem
+        torch.cuda.empty_cache()
+        per_config = per_config_records(qf, dev, stream, sampler, args.per_config_seconds,
+                                        args.graph_calls)
+    sampler.stop()
+    clocks = sampler.summary(t0, t1)
 
     if rank != 0:
         return None
@@ -521,12 +672,16 @@ def run_ours(args, w: wl.Workload):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": dict(w.describe(), **{
             "variant": variant,
-            "l2": f"inputs larger than L2: W rotated over {copies} copies of {w_bytes / 1e6:.1f} MB "
-                  f"(L2 {l2 / 1e6:.1f} MB)",
+            "l2": f"inputs larger than L2: W rotated over {copies} copies of {f['w_bytes'] / 1e6:.1f} MB "
+                  f"(L2 {f['l2'] / 1e6:.1f} MB)",
             "graph_calls": per_graph, "parallelism": f"replicas x{world}"}),
+        "timing": dict(stats, **{
+            "region": f"exactly {args.steps} calls between CUDA events, barrier + synchronize on "
+                      "both sides, a spin kernel queued ahead of the start event",
+            "reported": "median region (max over ranks)"}),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_kind": peak_kind,
-                     "traffic": traffic, "bytes_per_launch": bytes_call,
+                     "frac": achieved / peak, "frac_of_measured_peak": achieved / peak,
+                     "peak_kind": peak_kind, "traffic": traffic, "bytes_per_launch": bytes_call,
                      "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS},
         "gpu_launches": args.steps,
         "clocks": clocks,
@@ -534,6 +689,7 @@ def run_ours(args, w: wl.Workload):
         "warm_same_w": {"us_per_call": warm_us, "calls": warm_reps * per_graph,
                         "note": "one W copy for every call, timed after and apart from the "
                                 "headline; not the headline"},
+        "per_config": per_config,
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(inp, w, args.cpu_seconds)
@@ -589,23 +745,18 @@ def run_epilogue(args, w):
             if gr:
                 gr.replay()
     stream.synchronize()
-    sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.3)
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
-    torch.cuda.synchronize(dev)
-    with torch.cuda.stream(stream):
-        start.record(stream)
+    def region():
         for _ in range(full):
             g_full.replay()
         if g_rem:
             g_rem.replay()
-        end.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier()
-    clocks = sampler.stop()
-    el_max = max_over_ranks(start.elapsed_time(end) / 1e3, dev)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    times, (t0, t1) = time_regions(region, stream, dev, args.min_seconds)
+    sampler.stop()
+    clocks = sampler.summary(t0, t1)
+    el_max = max_over_ranks(statistics.median(times), dev)
     if qf.status():
         raise RuntimeError("device status raised in the timed region")
     res = aggregate(w.roofline_bytes(), args.steps, world, el_max)
@@ -613,7 +764,7 @@ def run_epilogue(args, w):
         return None
     peak, peak_kind = hbm_peak()
     achieved = w.roofline_bytes() / (el_max / args.steps) / 1e9
-    return {"metric": EPI_METRIC, "value": res["value"], "unit": UNIT, "n_gpus": world,
+    return {"metric": EPI_METRIC, "timing": region_stats(times, args.steps), "value": res["value"], "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
             "us_per_call": res["us_per_call"], "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
@@ -683,23 +834,18 @@ def run_attn2(args, w):
         for gr in graphs:
             gr.replay()
     stream.synchronize()
-    sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.3)
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
-    torch.cuda.synchronize(dev)
-    with torch.cuda.stream(stream):
-        start.record(stream)
+    def region():
         for _ in range(full):
             graphs[0].replay()
         if rem:
             graphs[-1].replay()
-        end.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier()
-    clocks = sampler.stop()
-    el_max = max_over_ranks(start.elapsed_time(end) / 1e3, dev)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    times, (t0, t1) = time_regions(region, stream, dev, args.min_seconds)
+    sampler.stop()
+    clocks = sampler.summary(t0, t1)
+    el_max = max_over_ranks(statistics.median(times), dev)
     if qf.status():
         raise RuntimeError("device status raised in the timed region")
     res = aggregate(w.roofline_bytes(), args.steps, world, el_max)
@@ -707,7 +853,7 @@ def run_attn2(args, w):
         return None
     peak, peak_kind = hbm_peak()
     achieved = w.roofline_bytes() / (el_max / args.steps) / 1e9
-    return {"metric": ATTN_METRIC, "value": res["value"], "unit": UNIT, "n_gpus": world,
+    return {"metric": ATTN_METRIC, "timing": region_stats(times, args.steps), "value": res["value"], "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
             "us_per_call": res["us_per_call"], "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
@@ -794,19 +940,14 @@ def run_chain(args, w: wl.Workload):
             for gr in graphs:
                 gr.replay()
         s.synchronize()
-        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        barrier()
-        torch.cuda.synchronize(dev)
-        with torch.cuda.stream(s):
-            start.record(s)
+        def region():
             for _ in range(full):
                 graphs[0].replay()
             if rem:
                 graphs[-1].replay()
-            end.record(s)
-        torch.cuda.synchronize(dev)
-        barrier()
-        timings[name] = max_over_ranks(start.elapsed_time(end) / 1e3, dev) / args.steps * 1e6
+
+        times, _ = time_regions(region, s, dev, args.min_seconds / 2)
+        timings[name] = max_over_ranks(statistics.median(times), dev) / args.steps * 1e6
     qf.set_pdl(True)
     if qf.status():
         raise RuntimeError("device status raised in the timed region")

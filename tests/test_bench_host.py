@@ -109,3 +109,36 @@ def test_all_cores_baseline_line():
     assert line["kind"] == "oracle" and line["unit"] == bench.UNIT
     assert line["value"] > 0 and 1 <= line["cores"] <= (os.cpu_count() or 1)
     assert "KV-head shards" in line["sample"]
+
+
+def test_clock_samples_are_kept_only_inside_the_timed_window():
+    import bench
+    """The sampler keeps nvidia-smi's own timestamps; a summary over a window
+    uses only the samples taken while the timed work ran."""
+    import datetime
+    text = "\n".join([
+        "2026/12/03 05:29:31.000, 0, 1980, 2070, 180.1, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "2026/12/03 05:29:31.500, 0, 1410, 2070, 1390.0, 0x4, Not Active, Not Active, Not Active, Active",
+        "2026/12/03 05:29:31.550, 0, 1430, 2070, 1395.0, 0x4, Not Active, Not Active, Not Active, Active",
+        "2026/12/03 05:29:31.600, 0, 1450, 2070, 1380.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "2026/12/03 05:29:32.500, 0, 1995, 2070, 170.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "garbage line",
+    ])
+    s = bench.ClockSampler(0)
+    s.rows = s.parse(text)
+    assert len(s.rows) == 5
+    t0 = datetime.datetime(2026, 12, 3, 5, 29, 31, 400000)
+    t1 = datetime.datetime(2026, 12, 3, 5, 29, 31, 700000)
+    w = s.summary(t0, t1)
+    assert w["samples"] == 3 and w["sm_mhz"] == 1430 and w["sm_mhz_min"] == 1410
+    assert w["reasons"] == ["sw_power_cap"] and w["sm_max_mhz"] == 2070
+    assert s.summary()["samples"] == 5
+    assert s.summary(t1, t1) is None
+
+
+def test_region_stats_per_call():
+    import bench
+    st = bench.region_stats([0.002, 0.001, 0.003, 0.001, 0.002], 100)
+    assert st["regions"] == 5 and abs(st["us_per_call_median"] - 20.0) < 1e-9
+    assert st["us_per_call_p10"] <= st["us_per_call_median"] <= st["us_per_call_p90"]
+    assert abs(st["timed_seconds"] - 0.009) < 1e-12
