@@ -493,7 +493,8 @@ def per_config_records(qf, dev, stream, sampler, seconds: float, graph_calls: in
     graph of PDL-linked calls (W rotated past L2) replayed back to back, each
     replay timed by CUDA events on the stream, until `seconds` of timed work;
     the median replay per call, its p10 / p90, GB/s and fraction of the
-    measured copy peak, and the clocks sampled while the replays ran."""
+    measured copy peak.  Each record keeps its wall-clock window, for the
+    clocks sampled while its replays ran (filled in once sampling stops)."""
     peak, peak_kind = hbm_peak()
     recs = []
     for name in PER_CONFIG:
@@ -540,7 +541,7 @@ def per_config_records(qf, dev, stream, sampler, seconds: float, graph_calls: in
             "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS,
             "calls": reps * f["per_graph"], "graph_calls": f["per_graph"],
             "l2": f"W rotated over {f['copies']} copies of {f['w_bytes'] / 1e6:.1f} MB",
-            "clocks": sampler.summary(t0, t1)})
+            "clocks": None, "window": (t0, t1)})
         del f, graph
         torch.cuda.empty_cache()
     return recs
@@ -658,6 +659,8 @@ def run_ours(args, w: wl.Workload):
                                         args.graph_calls)
     sampler.stop()
     clocks = sampler.summary(t0, t1)
+    for r in per_config or []:   # the samples are parsed once sampling has stopped
+        r["clocks"] = sampler.summary(*r.pop("window"))
 
     if rank != 0:
         return None

@@ -113,6 +113,9 @@ int qkv_front_launch(const uint16_t *x, const uint16_t *W, const int64_t *positi
 #define QKVF_CONSUMER_DEFAULT 0   /* the library's choice */
 #define QKVF_CONSUMER_MMA_SYNC 1  /* mma.sync m16n8k16 in four consumer warps */
 #define QKVF_CONSUMER_TCGEN05 2   /* tcgen05.mma M=64 into tensor memory, one issuing thread */
+#define QKVF_CONSUMER_RESIDENT 3  /* mma.sync with the CTA's whole W share on chip (shared memory and
+                                     registers) before the PDL wait, partials pushed to the owner
+                                     rank with st.async: splits 8, kb 4, stages 4 only */
 
 /*
  * qkv_front_variant: the launch shape qkv_front uses for N columns and M
@@ -121,7 +124,8 @@ int qkv_front_launch(const uint16_t *x, const uint16_t *W, const int64_t *positi
  *   *stages   depth of the shared-memory weight ring,
  *   *splits   CTAs per head (the cluster size; K is split cyclically among them),
  *   *kb       64-wide K boxes per ring stage (1, 2 or 4),
- *   *consumer QKVF_CONSUMER_MMA_SYNC or QKVF_CONSUMER_TCGEN05.
+ *   *consumer QKVF_CONSUMER_MMA_SYNC, QKVF_CONSUMER_TCGEN05 or
+ *             QKVF_CONSUMER_RESIDENT (chosen when splits is 8: N = 1152).
  * Any output pointer may be NULL.  The result depends on the launch shape:
  * `splits` and `kb` fix how K is divided among CTAs, and the consumer fixes
  * the order inside one CTA; `stages` never changes it.
@@ -132,8 +136,8 @@ int qkv_front_variant(int N, int M, int *tiles, int *stages, int *splits, int *k
  * qkv_front_launch_variant: qkv_front (with its checks) at an explicit
  * variant, for tests and tuning.  splits in {1, 2, 4, 8, 16}; kb in {1, 2, 4}
  * (0: the default) with splits * kb <= 128; stages >= 2 within the
- * shared-memory limit; consumer one of QKVF_CONSUMER_*.  Otherwise
- * QKVF_ERR_VARIANT.
+ * shared-memory limit; consumer one of QKVF_CONSUMER_* (the resident engine
+ * takes splits 8, kb 4 or 0, stages 4).  Otherwise QKVF_ERR_VARIANT.
  */
 int qkv_front_launch_variant(const uint16_t *x, const uint16_t *W, const int64_t *positions,
                              const int64_t *slots, const float *cos_sin,

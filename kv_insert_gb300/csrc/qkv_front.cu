@@ -69,6 +69,7 @@ enum HeadKind { kQ = 0, kK = 1, kV = 2, kGate = 3 };
 __device__ unsigned int g_status;
 
 struct FrontParams {
+    const uint16_t *W;   // [N, 8192] (the resident engine loads part of its share with plain loads)
     const int64_t *positions;
     const int64_t *slots;
     const float *cos_sin;
@@ -437,6 +438,35 @@ __device__ __forceinline__ uint32_t qk_norm_rope_pair(float f0, float f1, float 
     return pack_bf16x2(__float2bfloat16_rn(y0), __float2bfloat16_rn(y1));
 }
 
+// The finish of token u's 64 columns of head `head`: lane l holds the FP32
+// sums (v.x, v.y) of columns 2l, 2l+1.  Round to BF16; for q and k heads the
+// norm and RoPE with the position's (c, sn) of pair l; store the row segment;
+// for k and v heads write the slot's K or V half.  flag bit 0: the position
+// is in the table (else a q / k head writes nothing); bit 1: the token
+// inserts.  The whole warp calls it (the norm shuffles across lanes).
+__device__ __forceinline__ void finish_pair(const FrontParams &p, int head, int kind, int u, int lane,
+                                            float2 v, int flag, float c, float sn, int64_t slot)
+{
+    const __nv_bfloat16 p0 = __float2bfloat16_rn(v.x);
+    const __nv_bfloat16 p1 = __float2bfloat16_rn(v.y);
+    uint32_t word;
+    if (kind == kQ || kind == kK) {
+        if (!(flag & 1)) return;   // no table row for this position: nothing written
+        word = qk_norm_rope_pair(__bfloat162float(p0), __bfloat162float(p1), c, sn);
+    } else {
+        word = pack_bf16x2(p0, p1);
+    }
+    uint32_t *orow = reinterpret_cast<uint32_t *>(p.out + (size_t)u * p.N + (size_t)head * kHeadDim);
+    orow[lane] = word;
+    if ((kind == kK || kind == kV) && (flag & 2)) {
+        const int64_t page = slot / kPageSlots, offs = slot % kPageSlots;
+        const int gkv = head - kQPerKv * p.nkv - (kind == kV ? p.nkv : 0);
+        uint16_t *dst = p.kv_cache + ((page * p.nkv + gkv) * kPageSlots + offs) * kSlotWidth +
+                        (kind == kV ? kHeadDim : 0);
+        reinterpret_cast<uint32_t *>(dst)[lane] = word;
+    }
+}
+
 // ---- the front kernel ------------------------------------------------------
 
 // TC: the contraction runs on tcgen05 (one thread issues M=64 x N=MT x K=16
@@ -774,31 +804,325 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-        const int flag = s_flag[u];
-        const __nv_bfloat16 p0 = __float2bfloat16_rn(v.x);
-        const __nv_bfloat16 p1 = __float2bfloat16_rn(v.y);
-        uint32_t word;
-        if (kind == kQ || kind == kK) {
-            if (!(flag & 1)) continue;   // no table row for this position: nothing written
-            // norm and RoPE: pair (2 lane, 2 lane + 1), cos in column lane, sin
-            // in column 32 + lane of the position's row
-            word = qk_norm_rope_pair(__bfloat162float(p0), __bfloat162float(p1),
-                                     s_cs[u * kHeadDim + lane], s_cs[u * kHeadDim + 32 + lane]);
-        } else {
-            word = pack_bf16x2(p0, p1);
-        }
-        uint32_t *orow = reinterpret_cast<uint32_t *>(p.out + (size_t)u * p.N + (size_t)head * kHeadDim);
-        orow[lane] = word;
-        if ((kind == kK || kind == kV) && (flag & 2)) {
-            const int64_t slot = s_slot[u];
-            const int64_t page = slot / kPageSlots, offs = slot % kPageSlots;
-            const int gkv = head - q_heads - (kind == kV ? p.nkv : 0);
-            uint16_t *dst = p.kv_cache + ((page * p.nkv + gkv) * kPageSlots + offs) * kSlotWidth +
-                            (kind == kV ? kHeadDim : 0);
-            reinterpret_cast<uint32_t *>(dst)[lane] = word;
-        }
+        // norm and RoPE of pair (2 lane, 2 lane + 1): cos in column lane, sin
+        // in column 32 + lane of the position's row
+        const bool qk = kind == kQ || kind == kK;
+        finish_pair(p, head, kind, u, lane, v, s_flag[u], qk ? s_cs[u * kHeadDim + lane] : 0.f,
+                    qk ? s_cs[u * kHeadDim + 32 + lane] : 0.f, s_slot[u]);
     }
     if (S > 1) cluster_sync_all();   // no CTA leaves while its partial may still be read
+}
+
+// ---- the resident front: a CTA's whole weight share on chip before the wait --
+//
+// For a small projection (N = 1152: 18 heads, K split 8 ways, 128 KB of W per
+// CTA) the call is short enough that the time after the PDL wait decides it.
+// Here every byte of W a CTA needs is on chip before that wait, in the
+// previous call's shadow: stages 0 and 1 (64 KB) in shared memory through one
+// 4-D TMA copy, stages 2 and 3 (64 KB) in the registers of the four warps
+// through 16-byte loads.  After the wait one TMA copy brings the CTA's x
+// stripe; the warps contract it with both halves (mma.sync), and each CTA
+// pushes its FP32 partial of token u to the owner rank u % S with st.async,
+// completing on the owner's barrier.  The owner adds the S partials in rank
+// order 0..S-1 (the same fixed order for every launch) and runs the finish;
+// the other CTAs exit as soon as their partials are sent.
+//
+// Register stages use a k order of their own inside each 32-k chunk: lane
+// (g, t) holds W[row][c + 8t .. c + 8t + 7] (one 16-byte load) and feeds it
+// to two k16 steps, the first taking k c + 8t + {0,1,2,3}, the second
+// c + 8t + {4,5,6,7}; the x fragment takes the same k from shared memory.
+// A dot product may visit its k in any order, so only the FP32 summation
+// order differs from a ring stage.
+
+constexpr int kResThreads = 128;        // 4 warps of 16 W rows
+constexpr int kResSplits = 8;           // CTAs per head (cluster size)
+constexpr int kResSteps = 4;            // 256-k stages per CTA (8192 / 256 / 8)
+constexpr int kResSmemStages = 2;       // in shared memory (one TMA copy)
+constexpr int kResRegStages = kResSteps - kResSmemStages;   // in registers
+constexpr int kResChunks = 8;           // 32-k chunks per stage
+
+struct ResLayout {
+    uint32_t w, x, recv, full, recv_bar, abort_flag, total;
+};
+
+// owned: tokens per rank at most (ceil(mt / S))
+__host__ __device__ inline ResLayout res_layout(int mt)
+{
+    ResLayout L;
+    uint32_t off = 0;
+    L.w = off;
+    off += kResSmemStages * 4 * kBoxBytesW;
+    L.x = off;
+    off += kResSteps * 4 * (uint32_t)mt * 128;
+    L.recv = off;   // [local token][source rank][64] FP32 partials
+    off += (uint32_t)((mt + kResSplits - 1) / kResSplits) * kResSplits * kHeadDim * 4;
+    L.full = off;
+    off += 8;
+    L.recv_bar = off;
+    off += 8;
+    L.abort_flag = off;
+    off += 8;
+    L.total = off;
+    return L;
+}
+
+__host__ __device__ inline uint32_t res_smem_bytes(int mt) { return res_layout(mt).total + 1024; }
+
+__device__ __forceinline__ void tma_load_4d_front(uint32_t dst, const CUtensorMap *m, uint32_t bar, int c0,
+                                                  int c1, int c2, int c3, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "l"(policy)
+        : "memory");
+}
+
+// 16 bytes of W, streamed once: not kept in L1, first out of L2
+__device__ __forceinline__ uint4 ldg_stream(const void *ptr, uint64_t policy)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(ptr), "l"(policy));
+    return v;
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ void st_async_f32(uint32_t remote_addr, float v, uint32_t remote_bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(remote_addr),
+                 "r"(__float_as_uint(v)), "r"(remote_bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cluster_arrive_release()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait_acquire()
+{
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+template <int MT>
+__global__ void __launch_bounds__(kResThreads, 2)
+    qkv_front_resident_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                              const FrontParams p)
+{
+    constexpr int NT = MT / 8;
+    constexpr int kOwnedMax = (MT + kResSplits - 1) / kResSplits;
+    extern __shared__ uint8_t smem_dyn[];
+    uint8_t *smem = smem_dyn + ((1024u - (smem_u32(smem_dyn) & 1023u)) & 1023u);
+    const ResLayout L = res_layout(MT);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int S = kResSplits;
+    const uint32_t rank = cluster_rank();
+    const int head = blockIdx.y;
+    const uint32_t sW = smem_u32(smem + L.w), sX = smem_u32(smem + L.x), sRecv = smem_u32(smem + L.recv);
+    const uint32_t full_bar = smem_u32(smem + L.full), recv_bar = smem_u32(smem + L.recv_bar);
+    volatile int *s_abort = reinterpret_cast<volatile int *>(smem + L.abort_flag);
+    const int q_heads = kQPerKv * p.nkv;
+    const int kind = head < q_heads ? kQ : head < q_heads + p.nkv ? kK : head < q_heads + 2 * p.nkv ? kV : kGate;
+    // tokens this rank owns: u = rank + lt * S for lt < owned
+    const int owned = (int)rank < p.M ? (p.M - 1 - (int)rank) / S + 1 : 0;
+    const uint32_t smem_tx = kResSmemStages * 4 * kBoxBytesW + kResSteps * 4 * MT * 128;
+
+    if (threadIdx.x == 0) {
+        mbar_init(full_bar, 1);
+        mbar_init(recv_bar, 1);
+        *s_abort = 0;
+        // the arrivals now, the bytes as they land (the partials from the
+        // other ranks may complete before this CTA gets to its own wait)
+        mbar_expect_tx(full_bar, smem_tx);
+        mbar_expect_tx(recv_bar, (uint32_t)((S - 1) * owned * kHeadDim * 4));
+        fence_barrier_init();
+        griddep_launch_dependents();
+    }
+    __syncthreads();
+    cluster_arrive_release();   // every rank's barriers are initialised before any st.async
+
+    // ---- before the PDL wait: the weights (never written by a kernel in flight) ----
+    const uint64_t pol_w = policy_evict_first();
+    uint4 wr[kResRegStages][kResChunks][2];   // rows g and g + 8 of the warp's 16
+    {
+        const uint16_t *row0 = p.W + (size_t)(head * kHeadDim + warp * 16 + g) * kHidden + 8 * t;
+#pragma unroll
+        for (int i = 0; i < kResRegStages; ++i) {
+            const int k0 = ((int)rank + (kResSmemStages + i) * S) * (kBoxK * 4);
+#pragma unroll
+            for (int c = 0; c < kResChunks; ++c) {
+                wr[i][c][0] = ldg_stream(row0 + k0 + 32 * c, pol_w);
+                wr[i][c][1] = ldg_stream(row0 + 8 * kHidden + k0 + 32 * c, pol_w);
+            }
+        }
+    }
+    // stages 0 and 1: 64 rows x 4 boxes x 2 stages in one copy, issued after
+    // this thread's own register loads (issued before them, the copy was
+    // measured to land about 1.5 us later per call at N = 1152)
+    if (threadIdx.x == 0) {
+        tma_prefetch_map(&tmW);
+        tma_prefetch_map(&tmX);
+        tma_load_4d_front(sW, &tmW, full_bar, 0, head * kHeadDim, 4 * (int)rank, 0, pol_w);
+    }
+
+    griddep_wait();   // x, positions, slots, cos|sin come from the kernels before this one
+    if (threadIdx.x == 0)
+        tma_load_4d_front(sX, &tmX, full_bar, 0, 0, 4 * (int)rank, 0, policy_evict_last());
+
+    // this warp's token (the finish: warp lt takes local token lt)
+    const int u = (int)rank + warp * S;
+    int flag = 0;
+    int64_t slot = -1;
+    float cs_c = 0.f, cs_s = 0.f;
+    if (warp < owned) {
+        const int64_t pos = p.positions[u];
+        slot = p.slots[u];
+        const bool pos_ok = pos >= 0 && pos < p.cos_rows;
+        const bool slot_over = slot >= p.num_pages * (int64_t)kPageSlots;
+        flag = (pos_ok ? 1 : 0) | (slot >= 0 && !slot_over && pos_ok ? 2 : 0);
+        if (pos_ok && (kind == kQ || kind == kK)) {
+            cs_c = p.cos_sin[pos * kHeadDim + lane];
+            cs_s = p.cos_sin[pos * kHeadDim + 32 + lane];
+        }
+        if (head == 0 && lane == 0 && (!pos_ok || slot_over))
+            atomicOr(&g_status, (pos_ok ? 0u : QKVF_STATUS_BAD_POSITION) | (slot_over ? QKVF_STATUS_BAD_SLOT : 0u));
+    }
+
+    // ---- contraction ---------------------------------------------------
+    // Each step takes one shared-memory box (four k16 steps, ldmatrix) and
+    // two register chunks (four k16 steps, W already in registers), so the
+    // two instruction streams hide each other's latency.  One token tile:
+    // eight independent accumulator chains (box steps 0..3, register steps
+    // 4..7); two tiles: four chains per tile, shared by both streams.
+    constexpr int kChains = NT == 1 ? 8 : 4;
+    float acc[NT][kChains][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int kk = 0; kk < kChains; ++kk)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) acc[nt][kk][r] = 0.f;
+    const bool landed = mbar_try_wait(full_bar, 0) || bounded_wait(full_bar, 0, s_abort, p.wait_limit_ns, true);
+    if (__all_sync(0xffffffffu, landed)) {
+        const uint32_t a_row = (uint32_t)(warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8);
+        const uint32_t a_off = a_row * 128u, a_hi = (uint32_t)(lane >> 4);
+        const uint32_t b_tok = NT == 2 ? (uint32_t)((lane & 7) + ((lane >> 4) << 3)) : (uint32_t)(lane & 7);
+        const uint32_t b_off = b_tok * 128u, b_hi = (uint32_t)((lane >> 3) & 1);
+        const uint32_t sw = (uint32_t)(lane & 7);
+        constexpr int kBoxes = kResSmemStages * 4;                        // 8
+        constexpr int kRegChunksPerBox = kResRegStages * kResChunks / kBoxes;   // 2
+#pragma unroll
+        for (int bx = 0; bx < kBoxes; ++bx) {
+            // shared-memory box bx: ldmatrix from the 128-byte swizzled rows
+            const uint32_t wbox = sW + (uint32_t)bx * kBoxBytesW;
+            const uint32_t xbox = sX + (uint32_t)bx * (MT * 128);
+            uint32_t a[4][4], bb[4][4];
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                ldsm_x4(wbox + a_off + ((((uint32_t)(2 * kk) + a_hi) ^ sw) << 4), a[kk][0], a[kk][1], a[kk][2],
+                        a[kk][3]);
+                const uint32_t baddr = xbox + b_off + ((((uint32_t)(2 * kk) + b_hi) ^ sw) << 4);
+                if constexpr (NT == 2)
+                    ldsm_x4(baddr, bb[kk][0], bb[kk][1], bb[kk][2], bb[kk][3]);
+                else
+                    ldsm_x2(baddr, bb[kk][0], bb[kk][1]);
+            }
+            // register chunks: x in the same k order, 16 bytes per lane from the box
+            uint4 xv[kRegChunksPerBox][NT];
+#pragma unroll
+            for (int q = 0; q < kRegChunksPerBox; ++q) {
+                const int rc = bx * kRegChunksPerBox + q, i = rc / kResChunks, c = rc % kResChunks;
+                const uint32_t xrb = sX + (uint32_t)((kResSmemStages + i) * 4 + c / 2) * (MT * 128);
+                const uint32_t chunk = (uint32_t)(4 * (c & 1) + t);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {   // token row nt 8 + g: swizzle phase g
+                    // rows past M hold zeros: only lanes of real tokens read
+                    xv[q][nt] = make_uint4(0u, 0u, 0u, 0u);
+                    if (nt * 8 + g < p.M)
+                        xv[q][nt] = lds128(xrb + (uint32_t)(nt * 8 + g) * 128u + ((chunk ^ (uint32_t)g) << 4));
+                }
+            }
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                mma_bf16_16816(acc[0][kk], a[kk][0], a[kk][1], a[kk][2], a[kk][3], bb[kk][0], bb[kk][1]);
+                if constexpr (NT == 2)
+                    mma_bf16_16816(acc[1][kk], a[kk][0], a[kk][1], a[kk][2], a[kk][3], bb[kk][2], bb[kk][3]);
+            }
+#pragma unroll
+            for (int q = 0; q < kRegChunksPerBox; ++q) {
+                const int rc = bx * kRegChunksPerBox + q, i = rc / kResChunks, c = rc % kResChunks;
+                const uint4 wg = wr[i][c][0], wg8 = wr[i][c][1];
+                constexpr int base = NT == 1 ? 4 : 0;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    mma_bf16_16816(acc[nt][base + ((2 * q) & 3)], wg.x, wg8.x, wg.y, wg8.y, xv[q][nt].x, xv[q][nt].y);
+                    mma_bf16_16816(acc[nt][base + ((2 * q + 1) & 3)], wg.z, wg8.z, wg.w, wg8.w, xv[q][nt].z,
+                                   xv[q][nt].w);
+                }
+            }
+        }
+    }
+    float sum[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            float v = __fadd_rn(__fadd_rn(acc[nt][0][r], acc[nt][1][r]), __fadd_rn(acc[nt][2][r], acc[nt][3][r]));
+            if constexpr (kChains == 8)
+                v = __fadd_rn(v, __fadd_rn(__fadd_rn(acc[nt][4][r], acc[nt][5][r]),
+                                           __fadd_rn(acc[nt][6][r], acc[nt][7][r])));
+            sum[nt][r] = v;
+        }
+
+    // ---- send: token tok's rows to rank tok % S, slot [tok / S][rank][row] ----
+    cluster_wait_acquire();
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int tok = nt * 8 + 2 * t + (e & 1);
+            const int row = warp * 16 + g + ((e >> 1) << 3);
+            if (tok < p.M) {
+                const uint32_t owner = (uint32_t)(tok % S);
+                const uint32_t off = (uint32_t)((((tok / S) * S + (int)rank) * kHeadDim + row) * 4);
+                if (owner == rank)
+                    *reinterpret_cast<float *>(smem + L.recv + off) = sum[nt][e];
+                else
+                    st_async_f32(map_to_rank(sRecv + off, owner), sum[nt][e], map_to_rank(recv_bar, owner));
+            }
+        }
+    if (owned == 0) {
+        if (threadIdx.x == 0 && *s_abort)   // the copies into this CTA land before it leaves
+            bounded_wait(full_bar, 0, s_abort, p.wait_limit_ns, false);
+        return;   // nothing is read from this CTA's shared memory
+    }
+    __syncthreads();   // this rank's own partials are in its slots
+    const bool got = mbar_try_wait(recv_bar, 0) || bounded_wait(recv_bar, 0, s_abort, p.wait_limit_ns, false);
+    if (threadIdx.x == 0 && *s_abort) bounded_wait(full_bar, 0, s_abort, p.wait_limit_ns, false);
+
+    // ---- finish: rank-order sum, round, norm, RoPE, store, insert ----------
+    if (warp < owned && __all_sync(0xffffffffu, got)) {
+        const float *part = reinterpret_cast<const float *>(smem + L.recv) + (size_t)warp * S * kHeadDim;
+        float2 v = reinterpret_cast<const float2 *>(part)[lane];
+#pragma unroll
+        for (int src = 1; src < S; ++src) {
+            const float2 w = reinterpret_cast<const float2 *>(part + src * kHeadDim)[lane];
+            v.x = __fadd_rn(v.x, w.x);
+            v.y = __fadd_rn(v.y, w.y);
+        }
+        finish_pair(p, head, kind, u, lane, v, flag, cs_c, cs_s, slot);
+    }
+    (void)kOwnedMax;
 }
 
 // One CTA waits on a barrier that nothing completes, through the front's own
@@ -889,6 +1213,11 @@ int probe_device(DeviceState **out)
                                      cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
                 return QKVF_ERR_CUDA;
         }
+        const void *res[2] = {(const void *)qkv_front_resident_kernel<8>, (const void *)qkv_front_resident_kernel<16>};
+        for (int i = 0; i < 2; ++i)
+            if (cudaFuncSetAttribute(res[i], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)res_smem_bytes(i ? 16 : 8)) != cudaSuccess)
+                return QKVF_ERR_CUDA;
         if (!prepare_epi_kernel() || !prepare_attn2_kernel()) return QKVF_ERR_CUDA;
         d.prepared = true;
     }
@@ -898,7 +1227,8 @@ int probe_device(DeviceState **out)
 
 struct Variant {
     int mt, splits, stages, kb, l2_prefetch;
-    bool tc;   // tcgen05 consumer (else mma.sync)
+    bool tc;         // tcgen05 consumer (else mma.sync)
+    bool resident;   // the resident engine: the CTA's whole W share on chip before the wait
 };
 
 int max_stages(int mt, int kb, int per_sm)
@@ -913,7 +1243,8 @@ int max_stages(int mt, int kb, int per_sm)
 // largest power of two (<= 16) that keeps heads x splits within the SM count;
 // stages: as deep as shared memory allows, with one CTA per SM when each
 // head is one CTA and two per SM for clusters (so that a GPC holds whole
-// clusters), and no deeper than the CTA's number of K stages.
+// clusters), and no deeper than the CTA's number of K stages.  A split of 8
+// leaves each CTA 128 KB of W, which the resident engine holds on chip.
 Variant choose_variant(int N, int M, int sms)
 {
     Variant v;
@@ -922,8 +1253,14 @@ Variant choose_variant(int N, int M, int sms)
     v.kb = kDefaultKB;
     v.l2_prefetch = kDefaultL2Prefetch;
     v.tc = kDefaultTC;
+    v.resident = false;
     v.splits = 1;
     while (v.splits < 16 && heads * v.splits * 2 <= sms) v.splits *= 2;
+    if (v.splits == kResSplits && v.kb * kResSplits * kResSteps == kHidden / kBoxK) {
+        v.resident = true;
+        v.stages = kResSteps;
+        return v;
+    }
     const int per_sm = v.splits > 1 ? 2 : 1;
     const int steps = kHidden / (kBoxK * v.kb) / v.splits;
     v.stages = max_stages(v.mt, v.kb, per_sm);
@@ -936,6 +1273,9 @@ Variant choose_variant(int N, int M, int sms)
 // the 128 boxes of K, and a ring that fits the shared-memory limit.
 bool variant_ok(const Variant &v)
 {
+    if (v.resident)   // fixed shape: 8 CTAs per head, 4 stages of 4 boxes
+        return !v.tc && v.splits == kResSplits && v.kb * kResSplits * kResSteps == kHidden / kBoxK &&
+               v.stages == kResSteps;
     const bool pow2_s = v.splits == 1 || v.splits == 2 || v.splits == 4 || v.splits == 8 ||
                         v.splits == 16;
     const bool kb_ok = v.kb == 1 || v.kb == 2 || v.kb == 4;
@@ -1018,15 +1358,42 @@ int encode_maps(const uint16_t *x, const uint16_t *W, int M, int N, int mt, CUte
     return QKVF_OK;
 }
 
+// The resident engine's maps: W and x viewed as 4-D (64 k, rows, 4S blocks of
+// 64 k with a stride of 128 bytes, the CTA's stages 512 S bytes apart), so
+// that one box is a CTA's whole stripe of stages (x) or its first two (W).
+int encode_resident_maps(const uint16_t *x, const uint16_t *W, int M, int N, int mt, CUtensorMap *mw,
+                         CUtensorMap *mx)
+{
+    const int S = kResSplits;
+    const cuuint64_t stride[3] = {(cuuint64_t)kHidden * 2, 128, (cuuint64_t)512 * S};
+    const cuuint32_t estride[4] = {1, 1, 1, 1};
+    const cuuint64_t wdim[4] = {(cuuint64_t)kBoxK, (cuuint64_t)N, (cuuint64_t)4 * S, (cuuint64_t)kResSteps};
+    const cuuint32_t wbox[4] = {(cuuint32_t)kBoxK, (cuuint32_t)kHeadDim, 4, (cuuint32_t)kResSmemStages};
+    if (g_encode(mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, (void *)W, wdim, stride, wbox, estride,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return QKVF_ERR_CUDA;
+    // rows past M read as zeros
+    const cuuint64_t xdim[4] = {(cuuint64_t)kBoxK, (cuuint64_t)M, (cuuint64_t)4 * S, (cuuint64_t)kResSteps};
+    const cuuint32_t xbox[4] = {(cuuint32_t)kBoxK, (cuuint32_t)mt, 4, (cuuint32_t)kResSteps};
+    if (g_encode(mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, (void *)x, xdim, stride, xbox, estride,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return QKVF_ERR_CUDA;
+    return QKVF_OK;
+}
+
 int launch_front(const uint16_t *x, const uint16_t *W, const int64_t *positions,
                  const int64_t *slots, const float *cos_sin, int64_t cos_sin_rows, uint16_t *out,
                  uint16_t *kv_cache, int64_t num_pages, int M, int N, int num_kv_heads,
                  const Variant &v, void *stream)
 {
     CUtensorMap mw, mx;
-    int rc = encode_maps(x, W, M, N, v.mt, &mw, &mx);
+    int rc = v.resident ? encode_resident_maps(x, W, M, N, v.mt, &mw, &mx)
+                        : encode_maps(x, W, M, N, v.mt, &mw, &mx);
     if (rc != QKVF_OK) return rc;
     FrontParams prm;
+    prm.W = W;
     prm.positions = positions;
     prm.slots = slots;
     prm.cos_sin = cos_sin;
@@ -1045,10 +1412,10 @@ int launch_front(const uint16_t *x, const uint16_t *W, const int64_t *positions,
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)v.splits, (unsigned)(N / kHeadDim), 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem_bytes(v.mt, v.kb, v.stages);
+    cfg.blockDim = dim3(v.resident ? kResThreads : kThreads, 1, 1);
+    cfg.dynamicSmemBytes = v.resident ? res_smem_bytes(v.mt) : smem_bytes(v.mt, v.kb, v.stages);
     cfg.stream = (cudaStream_t)stream;
-    cudaLaunchAttribute attrs[2];
+    cudaLaunchAttribute attrs[3];
     int na = 0;
     if (v.splits > 1) {
         attrs[na].id = cudaLaunchAttributeClusterDimension;
@@ -1056,13 +1423,21 @@ int launch_front(const uint16_t *x, const uint16_t *W, const int64_t *positions,
         attrs[na].val.clusterDim.y = 1;
         attrs[na].val.clusterDim.z = 1;
         ++na;
+        // a cluster's CTAs on distinct SMs where possible: two CTAs of one
+        // call on one SM share its shared-memory path and tensor pipes
+        attrs[na].id = cudaLaunchAttributeClusterSchedulingPolicyPreference;
+        attrs[na].val.clusterSchedulingPolicyPreference = cudaClusterSchedulingPolicySpread;
+        ++na;
     }
     attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attrs[na].val.programmaticStreamSerializationAllowed = g_pdl ? 1 : 0;
     ++na;
     cfg.attrs = attrs;
     cfg.numAttrs = (unsigned)na;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel_for(v.mt, v.tc), mw, mx, prm);
+    const KernelFn k = v.resident ? (v.mt == 8 ? (KernelFn)qkv_front_resident_kernel<8>
+                                               : (KernelFn)qkv_front_resident_kernel<16>)
+                                  : kernel_for(v.mt, v.tc);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k, mw, mx, prm);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         return QKVF_ERR_CUDA;
@@ -1150,7 +1525,8 @@ int qkv_front_variant(int N, int M, int *tiles, int *stages, int *splits, int *k
     if (stages) *stages = v.stages;
     if (splits) *splits = v.splits;
     if (kb) *kb = v.kb;
-    if (consumer) *consumer = v.tc ? QKVF_CONSUMER_TCGEN05 : QKVF_CONSUMER_MMA_SYNC;
+    if (consumer)
+        *consumer = v.resident ? QKVF_CONSUMER_RESIDENT : v.tc ? QKVF_CONSUMER_TCGEN05 : QKVF_CONSUMER_MMA_SYNC;
     return QKVF_OK;
 }
 
@@ -1166,7 +1542,7 @@ int qkv_front_launch_variant(const uint16_t *x, const uint16_t *W, const int64_t
         return code;
     if (M == 0) return QKVF_OK;
     if (consumer != QKVF_CONSUMER_DEFAULT && consumer != QKVF_CONSUMER_MMA_SYNC &&
-        consumer != QKVF_CONSUMER_TCGEN05)
+        consumer != QKVF_CONSUMER_TCGEN05 && consumer != QKVF_CONSUMER_RESIDENT)
         return QKVF_ERR_VARIANT;
     Variant v;
     v.mt = M <= 8 ? 8 : 16;
@@ -1175,6 +1551,7 @@ int qkv_front_launch_variant(const uint16_t *x, const uint16_t *W, const int64_t
     v.kb = kb == 0 ? kDefaultKB : kb;
     v.l2_prefetch = kDefaultL2Prefetch;
     v.tc = consumer == QKVF_CONSUMER_DEFAULT ? kDefaultTC : consumer == QKVF_CONSUMER_TCGEN05;
+    v.resident = consumer == QKVF_CONSUMER_RESIDENT;
     if (!variant_ok(v)) return QKVF_ERR_VARIANT;
     DeviceState *d;
     int rc = probe_device(&d);

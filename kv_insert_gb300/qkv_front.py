@@ -30,7 +30,7 @@ PAGE_SLOTS = 16
 SLOT_WIDTH = 128
 MAX_TOKENS = 16
 
-CONSUMER_DEFAULT, CONSUMER_MMA_SYNC, CONSUMER_TCGEN05 = 0, 1, 2
+CONSUMER_DEFAULT, CONSUMER_MMA_SYNC, CONSUMER_TCGEN05, CONSUMER_RESIDENT = 0, 1, 2, 3
 
 STATUS_BAD_SLOT = 1
 STATUS_BAD_POSITION = 2
@@ -300,7 +300,8 @@ def variant_full(n: int, m: int) -> dict:
     _check(load().qkv_front_variant(n, m, *[ctypes.byref(v) for v in f]))
     names = ("tiles", "stages", "splits", "kb", "consumer")
     out = {k: v.value for k, v in zip(names, f)}
-    out["consumer"] = {CONSUMER_MMA_SYNC: "mma.sync", CONSUMER_TCGEN05: "tcgen05"}[out["consumer"]]
+    out["consumer"] = {CONSUMER_MMA_SYNC: "mma.sync", CONSUMER_TCGEN05: "tcgen05",
+                       CONSUMER_RESIDENT: "resident"}[out["consumer"]]
     return out
 
 

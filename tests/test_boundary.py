@@ -140,6 +140,20 @@ def test_variants_the_gpu_tests_launch_are_accepted(lib):
                 assert rc in (5, 6), (name, splits, stages, kb, consumer, rc)
 
 
+def test_resident_engine_variant_rule(lib):
+    """The resident engine runs only at its fixed shape (8 CTAs per head, kb
+    4, 4 stages): other explicit shapes are refused on the host, the fixed
+    one gets past the check to the device query."""
+    lv = lib.qkv_front_launch_variant
+    args = (X, W, POS, SL, CS, 4096, OUT, CACHE, 4, 1, 1152, 1)
+    assert lv(*args, 8, 4, 4, 3, None) in (5, 6)
+    assert lv(*args, 8, 4, 0, 3, None) in (5, 6)
+    assert lv(*args, 4, 4, 4, 3, None) == 8
+    assert lv(*args, 8, 3, 4, 3, None) == 8
+    assert lv(*args, 8, 4, 2, 3, None) == 8
+    assert lv(*args, 8, 4, 4, 4, None) == 8   # no such engine
+
+
 def test_from_host_refusals(lib):
     fh = lib.qkv_front_from_host
     need = lib.qkv_front_staging_bytes(8, 9216)

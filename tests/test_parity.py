@@ -69,6 +69,60 @@ def test_every_token_count_one_kv_head(M, consumer):
     check_workload(w, splits=v["splits"], stages=v["stages"], kb=v["kb"], consumer=consumer)
 
 
+@pytest.mark.parametrize("M", list(range(1, 17)))
+def test_resident_engine_every_token_count(M):
+    """The library's choice at N = 1152 (K split 8 ways): the resident engine
+    (the whole W share on chip before the wait, partials pushed to the owner
+    rank), every M from 1 to 16, against the oracle; a second run gives the
+    same bits in out and in the cache."""
+    w = wl.Workload(f"r{M}_nkv1", M=M, num_kv_heads=1, max_pos=4096, num_pages=8, seed=2300 + M)
+    v = qf.variant_full(w.N, w.M)
+    assert (v["consumer"], v["splits"], v["kb"], v["stages"]) == ("resident", 8, 4, 4)
+    inp, out_bits, _ = check_workload(w)
+    g = device_inputs(inp)
+    again = run_device(g)
+    assert np.array_equal(wl.bits(again.cpu()), out_bits)
+    g2 = device_inputs(inp)
+    run_device(g2, splits=8, stages=4, kb=4, consumer=qf.CONSUMER_RESIDENT)
+    assert torch.equal(g2["kv_cache"].view(torch.int16), g["kv_cache"].view(torch.int16))
+
+
+@pytest.mark.parametrize("M", [1, 8, 9, 16])
+def test_resident_engine_integer_inputs_bit_exact(M):
+    """Integer-valued x and W: every partial sum is exact, so the resident
+    engine's own k order inside its register stages cannot change a bit of
+    the v and gate columns."""
+    w = wl.Workload(f"ri{M}_nkv1", M=M, num_kv_heads=1, max_pos=4096, num_pages=8, seed=2400 + M)
+    _, out_bits, out_ref = check_workload(w, integer_valued=True)
+    vg = _vg_cols(1)
+    assert np.array_equal(out_bits[:, vg], out_ref[:, vg])
+
+
+def test_resident_engine_index_rules():
+    """Negative, past-the-cache slots and a position past the table on the
+    resident engine: flagged, skipped, nothing written outside a cache view."""
+    w = wl.Workload("rbad", M=7, num_kv_heads=1, max_pos=512, num_pages=4, seed=2501)
+    inp = wl.make_inputs(w)
+    inp["slots"][1] = -1
+    inp["slots"][4] = w.num_pages * 16 + 3
+    inp["positions"][6] = w.max_pos
+    g = device_inputs(inp)
+    parent = torch.zeros(2 * w.num_pages, 1, 16, 128, dtype=torch.bfloat16, device="cuda:0")
+    parent[: w.num_pages].copy_(g["kv_cache"])
+    g["kv_cache"] = parent[: w.num_pages]
+    sentinel = torch.full((w.M, w.N), 3.0, dtype=torch.bfloat16)
+    out = run_device(g, out=sentinel.to("cuda:0"))
+    st = qf.status()
+    assert int(parent[w.num_pages:].view(torch.int16).abs().sum()) == 0, "insert past the cache"
+    out_bits = wl.bits(out.cpu())
+    out_ref, cache_ref, err = run_oracle(inp, w.num_kv_heads, out_bits=wl.bits(sentinel))
+    assert err == 3
+    assert np.array_equal(out_bits[6, : 9 * 64], out_ref[6, : 9 * 64])   # untouched sentinel
+    assert_values(out_bits, out_ref)
+    assert_cache(inp, w.num_kv_heads, g["kv_cache"], out_bits, cache_ref)
+    assert st == qf.STATUS_BAD_SLOT | qf.STATUS_BAD_POSITION, st
+
+
 @pytest.mark.parametrize("nkv", [2, 3, 4])
 def test_other_kv_head_counts(nkv):
     w = wl.Workload(f"m5_nkv{nkv}", M=5, num_kv_heads=nkv, max_pos=8192, num_pages=64,
