@@ -94,6 +94,11 @@ def parse_args(argv=None):
                     help="attn2 engine: clusters merging over DSMEM (the attn2 entry point, no "
                          "workspace) or split-KV over the whole GPU with partials in a workspace")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--ncu-range", type=int, default=0,
+                    help="after warm-up, run this many calls (direct launches, inputs rotated as in "
+                         "the timed region) between cudaProfilerStart and cudaProfilerStop, print "
+                         "one line and exit: the range an `ncu --replay-mode app-range` capture "
+                         "measures, so that DRAM bytes include the write-backs later calls cause")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seconds", type=float, default=90.0,
                     help="target duration of the whole --impl reference run")
@@ -269,6 +274,18 @@ def spin(stream):
     region's work: the region measures the GPU, not the host's launch."""
     with torch.cuda.stream(stream):
         torch.cuda._sleep(SPIN_CYCLES)
+
+
+def profile_range(call, calls: int, stream, dev) -> dict:
+    """`calls` calls of call(i) on `stream` inside one profiler range."""
+    torch.cuda.synchronize(dev)
+    torch.cuda.profiler.start()
+    with torch.cuda.stream(stream):
+        for i in range(calls):
+            call(i)
+    torch.cuda.synchronize(dev)
+    torch.cuda.profiler.stop()
+    return {"ncu_range_calls": calls}
 
 
 def time_regions(region, stream, dev, min_seconds: float, min_regions: int = 3,
@@ -570,6 +587,8 @@ def run_ours(args, w: wl.Workload):
             f["call"](i)
     stream.synchronize()
     assert qf.status() == 0, "device status raised during warm-up"
+    if args.ncu_range:
+        return dict(profile_range(f["call"], args.ncu_range, stream, dev), workload=w.name)
     full, rem = divmod(args.steps, per_graph)
     g_full = f["capture"](per_graph) if full else None
     g_rem = f["capture"](rem) if rem else None
@@ -740,6 +759,8 @@ def run_epilogue(args, w):
         for i in range(args.warmup):
             call(i)
     stream.synchronize()
+    if args.ncu_range:
+        return dict(profile_range(call, args.ncu_range, stream, dev), workload=w.name)
     full, rem = divmod(args.steps, per_graph)
     g_full = capture(per_graph) if full else None
     g_rem = capture(rem) if rem else None
@@ -825,6 +846,8 @@ def run_attn2(args, w):
         for i in range(args.warmup):
             call(i)
     stream.synchronize()
+    if args.ncu_range:
+        return dict(profile_range(call, args.ncu_range, stream, dev), workload=w.name)
     full, rem = divmod(args.steps, per_graph)
     graphs = []
     for n in ([per_graph] if full else []) + ([rem] if rem else []):

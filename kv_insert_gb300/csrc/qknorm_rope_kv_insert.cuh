@@ -201,6 +201,9 @@ __global__ void __launch_bounds__(kEpiThreads, kEpiCtasPerSm) qknorm_rope_kv_ins
 
     if (warp == 0) {
         // ---- produce: 32 tokens' indices per warp load, then each token's copies ----
+        // A token's q | k | v region needs no index, so its copy is issued
+        // before the index loads are first used: the data and the indices
+        // come in side by side.
         unsigned bad = 0u;
         int i = 0;
         bool stop = false;
@@ -210,15 +213,10 @@ __global__ void __launch_bounds__(kEpiThreads, kEpiCtasPerSm) qknorm_rope_kv_ins
             if (tl < p.T) {
                 pos_l = p.positions[tl];
                 slot_l = p.slots[tl];
-                const bool pos_ok = pos_l >= 0 && pos_l < p.cos_rows;
-                bad |= (pos_ok ? 0u : QKVF_STATUS_BAD_POSITION) |
-                       (slot_l >= slot_end ? QKVF_STATUS_BAD_SLOT : 0u);
             }
             for (int j = 0; j < 32; ++j, ++i) {
                 const int64_t t = tb + j * G;
                 if (t >= p.T) break;   // the same for every lane
-                const int64_t pos = __shfl_sync(0xffffffffu, pos_l, j);
-                const int64_t sl = __shfl_sync(0xffffffffu, slot_l, j);
                 const int s = i % nslots, use = i / nslots;
                 int ok = 1;
                 if (lane == 0 && use > 0)
@@ -228,20 +226,22 @@ __global__ void __launch_bounds__(kEpiThreads, kEpiCtasPerSm) qknorm_rope_kv_ins
                     break;
                 }
                 uint8_t *base = smem + (size_t)s * slot_bytes;
+                const uint32_t bar = full0 + 8 * s;
+                const uint8_t *src = reinterpret_cast<const uint8_t *>(p.qkv + (size_t)t * p.N);
+                for (uint32_t c = (uint32_t)lane; c < region / 16; c += 32)
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(base) + 16 * c),
+                                 "l"(src + 16 * c)
+                                 : "memory");
+                const int64_t pos = __shfl_sync(0xffffffffu, pos_l, j);
+                const int64_t sl = __shfl_sync(0xffffffffu, slot_l, j);
                 const bool pos_ok = pos >= 0 && pos < p.cos_rows;
                 const bool ins = sl >= 0 && sl < slot_end && pos_ok;
-                const uint32_t bar = full0 + 8 * s;
                 if (lane == 0) {
                     int64_t *hdr = reinterpret_cast<int64_t *>(base + region + kHeadDim * 4);
                     hdr[0] = pos;
                     hdr[1] = sl;
                     hdr[2] = (pos_ok ? 1 : 0) | (ins ? 2 : 0);
                 }
-                const uint8_t *src = reinterpret_cast<const uint8_t *>(p.qkv + (size_t)t * p.N);
-                for (uint32_t c = (uint32_t)lane; c < region / 16; c += 32)
-                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(base) + 16 * c),
-                                 "l"(src + 16 * c)
-                                 : "memory");
                 if (pos_ok && lane < kHeadDim * 4 / 16)
                     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(base + region) + 16 * lane),
                                  "l"(reinterpret_cast<const uint8_t *>(p.cos_sin + pos * kHeadDim) + 16 * lane)
@@ -249,6 +249,9 @@ __global__ void __launch_bounds__(kEpiThreads, kEpiCtasPerSm) qknorm_rope_kv_ins
                 asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
                 if (lane == 0) mbar_arrive(bar);   // the header
             }
+            if (tl < p.T)
+                bad |= (pos_l >= 0 && pos_l < p.cos_rows ? 0u : QKVF_STATUS_BAD_POSITION) |
+                       (slot_l >= slot_end ? QKVF_STATUS_BAD_SLOT : 0u);
         }
         asm volatile("cp.async.wait_all;" ::: "memory");   // nothing of ours left in flight
         bad = __reduce_or_sync(0xffffffffu, bad);
