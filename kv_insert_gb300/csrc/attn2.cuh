@@ -443,14 +443,13 @@ __global__ void __launch_bounds__(kA2Threads, 1)
             const int nb = npages - k0 < kA2Block ? npages - k0 : kA2Block;   // same for every lane
             const int jb = k0 / kA2Block, rb = jb % kA2RingBlocks;
             const uint32_t ph = (uint32_t)((jb / kA2RingBlocks) & 1);
-            bool inside = true;
-            for (int b = 0; b < nb; ++b) {
-                const int key0 = (first_mine + (k0 + b) * S) * kPageSlots;
-                inside = inside && key0 >= edge_lo && key0 + kPageSlots - 1 <= edge_hi;
-            }
+            // the block's keys rise with its pages: the first and the last key
+            // decide whether every row sees all of them
+            const int key_first = (first_mine + k0 * S) * kPageSlots;
+            const int key_last = (first_mine + (k0 + nb - 1) * S) * kPageSlots + kPageSlots - 1;
+            const bool inside = nb == kA2Block && key_first >= edge_lo && key_last <= edge_hi;
             bool landed = mbar_try_wait(full0 + 8 * rb, ph) ||
                           bounded_wait(full0 + 8 * rb, ph, s_flags, p.wait_limit_ns, true);
-            inside = inside && nb == kA2Block;
             const uint32_t kreg = sRing + (uint32_t)rb * (kA2Block * kA2PageBytes);   // the block's K rows
             const uint32_t vreg = kreg + kA2Block * 2048;                            // then its V rows
             // every warp of the group is past the previous block's tcgen05.ld
@@ -519,7 +518,9 @@ __global__ void __launch_bounds__(kA2Threads, 1)
                 const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
                 const float base_a = mn_a == -INFINITY ? 0.f : mn_a;
                 const float base_b = mn_b == -INFINITY ? 0.f : mn_b;
-                const float al_a = a2_ex2(m_a - base_a), al_b = a2_ex2(m_b - base_b);
+                // O and the sums are rescaled only when some row's maximum grew
+                // (otherwise the factor is exactly 1 and the product the same)
+                const bool grew = __any_sync(0xffffffffu, mn_a != m_a || mn_b != m_b);
                 // weights 2^(scale s - base), one FMA and one ex2 each; sums as trees
                 float ts[2 * kA2Block][2];
 #pragma unroll
@@ -537,17 +538,22 @@ __global__ void __launch_bounds__(kA2Threads, 1)
                         ts[nt][0] += ts[nt + w][0];
                         ts[nt][1] += ts[nt + w][1];
                     }
-                l_a = l_a * al_a + ts[0][0];
-                l_b = l_b * al_b + ts[0][1];
+                if (grew) {
+                    const float al_a = a2_ex2(m_a - base_a), al_b = a2_ex2(m_b - base_b);
+                    l_a = l_a * al_a;
+                    l_b = l_b * al_b;
+#pragma unroll
+                    for (int nd = 0; nd < 8; ++nd) {
+                        o[nd][0] *= al_a;
+                        o[nd][1] *= al_a;
+                        o[nd][2] *= al_b;
+                        o[nd][3] *= al_b;
+                    }
+                }
+                l_a = l_a + ts[0][0];
+                l_b = l_b + ts[0][1];
                 m_a = mn_a;
                 m_b = mn_b;
-#pragma unroll
-                for (int nd = 0; nd < 8; ++nd) {
-                    o[nd][0] *= al_a;
-                    o[nd][1] *= al_a;
-                    o[nd][2] *= al_b;
-                    o[nd][3] *= al_b;
-                }
 #pragma unroll
                 for (int b = 0; b < kA2Block; ++b) {
                     if (b < nb) {
