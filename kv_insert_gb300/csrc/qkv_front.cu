@@ -233,25 +233,24 @@ __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap *m)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }
 
-// 2-D tiled TMA load of one box into shared memory, completing on `bar`.
-// c0 is the innermost (k) coordinate in elements: always a multiple of 64
-// here, so the 16-byte rule on the inner coordinate holds.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *m, uint32_t bar,
-                                            int c0, int c1, uint64_t policy)
+// 3-D tiled TMA load (k within a 64-k block, rows, 64-k blocks): one copy
+// brings a ring stage's kb boxes.  c0 is always 0.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *m, uint32_t bar, int c0, int c1,
+                                            int c2, uint64_t policy)
 {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "l"(policy)
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
         : "memory");
 }
 
-// Prefetch one W box into L2 (no shared-memory destination, no barrier).
-__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *m, int c0, int c1)
+// Prefetch one stage of W into L2 (no shared-memory destination, no barrier).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap *m, int c0, int c1, int c2)
 {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
                      reinterpret_cast<uint64_t>(m)),
-                 "r"(c0), "r"(c1)
+                 "r"(c0), "r"(c1), "r"(c2)
                  : "memory");
 }
 
@@ -542,25 +541,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_map(&tmX);
             const int row0 = head * kHeadDim;
             const int npre = steps < stages ? steps : stages;
+            // one copy per stage for W and one for x: the maps are 3-D
+            // (k, rows, 64-k blocks) with a box of the stage's kb blocks
             for (int i = 0; i < npre; ++i) {
                 const int j = (int)rank + i * S;
                 mbar_expect_tx(full0 + 8 * i, kStageTx);
-                for (int b = 0; b < KB; ++b)
-                    tma_load_2d(sW + (uint32_t)(i * KB + b) * kBoxBytesW, &tmW, full0 + 8 * i,
-                                (j * KB + b) * kBoxK, row0, pol_w);
+                tma_load_3d(sW + (uint32_t)(i * KB) * kBoxBytesW, &tmW, full0 + 8 * i, 0, row0, j * KB, pol_w);
             }
             // weights further ahead into L2 while the previous kernel finishes
             const int pf_end = npre + p.l2_prefetch < steps ? npre + p.l2_prefetch : steps;
-            for (int i = npre; i < pf_end; ++i) {
-                const int j = (int)rank + i * S;
-                for (int b = 0; b < KB; ++b) tma_prefetch_l2_2d(&tmW, (j * KB + b) * kBoxK, row0);
-            }
+            for (int i = npre; i < pf_end; ++i) tma_prefetch_l2_3d(&tmW, 0, row0, ((int)rank + i * S) * KB);
             griddep_wait();   // x is written by the kernel before this one
             for (int i = 0; i < npre; ++i) {
                 const int j = (int)rank + i * S;
-                for (int b = 0; b < KB; ++b)
-                    tma_load_2d(sX + (uint32_t)(i * KB + b) * kBoxBytesX, &tmX, full0 + 8 * i,
-                                (j * KB + b) * kBoxK, 0, pol_x);
+                tma_load_3d(sX + (uint32_t)(i * KB) * kBoxBytesX, &tmX, full0 + 8 * i, 0, 0, j * KB, pol_x);
             }
             int issued = npre;
             int s = npre == stages ? 0 : npre;
@@ -571,12 +565,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 const int j = (int)rank + i * S;
                 mbar_expect_tx(full0 + 8 * s, kStageTx);
-                for (int b = 0; b < KB; ++b) {
-                    tma_load_2d(sW + (uint32_t)(s * KB + b) * kBoxBytesW, &tmW, full0 + 8 * s,
-                                (j * KB + b) * kBoxK, row0, pol_w);
-                    tma_load_2d(sX + (uint32_t)(s * KB + b) * kBoxBytesX, &tmX, full0 + 8 * s,
-                                (j * KB + b) * kBoxK, 0, pol_x);
-                }
+                tma_load_3d(sW + (uint32_t)(s * KB) * kBoxBytesW, &tmW, full0 + 8 * s, 0, row0, j * KB, pol_w);
+                tma_load_3d(sX + (uint32_t)(s * KB) * kBoxBytesX, &tmX, full0 + 8 * s, 0, 0, j * KB, pol_x);
                 ++issued;
                 if (++s == stages) {
                     s = 0;
@@ -1336,22 +1326,26 @@ const char *check_args(const uint16_t *x, const uint16_t *W, const int64_t *posi
     return nullptr;
 }
 
-int encode_maps(const uint16_t *x, const uint16_t *W, int M, int N, int mt, CUtensorMap *mw,
+// The ring's maps: W and x viewed as 3-D (64 k within a block, rows, the
+// 128 blocks of 64 k, 128 bytes apart), so that one box of kb blocks is a
+// whole ring stage; each block lands as 64 (W) or mt (x) rows of 128
+// swizzled bytes, block after block.
+int encode_maps(const uint16_t *x, const uint16_t *W, int M, int N, int mt, int kb, CUtensorMap *mw,
                 CUtensorMap *mx)
 {
-    const cuuint64_t wdim[2] = {(cuuint64_t)kHidden, (cuuint64_t)N};
-    const cuuint64_t wstride[1] = {(cuuint64_t)kHidden * 2};
-    const cuuint32_t wbox[2] = {(cuuint32_t)kBoxK, (cuuint32_t)kHeadDim};
-    const cuuint32_t estride[2] = {1, 1};
-    if (g_encode(mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (void *)W, wdim, wstride, wbox, estride,
+    const cuuint64_t stride[2] = {(cuuint64_t)kHidden * 2, 128};
+    const cuuint32_t estride[3] = {1, 1, 1};
+    const cuuint64_t wdim[3] = {(cuuint64_t)kBoxK, (cuuint64_t)N, (cuuint64_t)(kHidden / kBoxK)};
+    const cuuint32_t wbox[3] = {(cuuint32_t)kBoxK, (cuuint32_t)kHeadDim, (cuuint32_t)kb};
+    if (g_encode(mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, (void *)W, wdim, stride, wbox, estride,
                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return QKVF_ERR_CUDA;
     // x rows past M read as zeros (out-of-bounds fill), so a tile of 8 or 16
     // tokens covers any M
-    const cuuint64_t xdim[2] = {(cuuint64_t)kHidden, (cuuint64_t)M};
-    const cuuint32_t xbox[2] = {(cuuint32_t)kBoxK, (cuuint32_t)mt};
-    if (g_encode(mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (void *)x, xdim, wstride, xbox, estride,
+    const cuuint64_t xdim[3] = {(cuuint64_t)kBoxK, (cuuint64_t)M, (cuuint64_t)(kHidden / kBoxK)};
+    const cuuint32_t xbox[3] = {(cuuint32_t)kBoxK, (cuuint32_t)mt, (cuuint32_t)kb};
+    if (g_encode(mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, (void *)x, xdim, stride, xbox, estride,
                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return QKVF_ERR_CUDA;
@@ -1390,7 +1384,7 @@ int launch_front(const uint16_t *x, const uint16_t *W, const int64_t *positions,
 {
     CUtensorMap mw, mx;
     int rc = v.resident ? encode_resident_maps(x, W, M, N, v.mt, &mw, &mx)
-                        : encode_maps(x, W, M, N, v.mt, &mw, &mx);
+                        : encode_maps(x, W, M, N, v.mt, v.kb, &mw, &mx);
     if (rc != QKVF_OK) return rc;
     FrontParams prm;
     prm.W = W;
