@@ -564,6 +564,7 @@ def per_config_records(qf, dev, stream, sampler, seconds: float, graph_calls: in
             "us_per_call_p90": float(q[2]), "bytes_per_call": w.roofline_bytes(), "gbs": gbs,
             "frac": gbs / peak, "frac_of_measured_peak": gbs / peak, "peak_kind": peak_kind,
             "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS,
+            "traffic": recorded_traffic("qkv_front", name),
             "calls": reps * f["per_graph"], "graph_calls": f["per_graph"],
             "l2": f"W rotated over {f['copies']} copies of {f['w_bytes'] / 1e6:.1f} MB",
             "clocks": None, "window": (t0, t1)})
