@@ -16,13 +16,14 @@
 //
 // Design: a CTA per (request r, KV head g, split z).  A producer warp streams
 // the CTA's pages (p0 + z, p0 + z + S, ...) into a ring of blocks of 4 pages
-// (the block's 64 K rows, then its 64 V rows, 128-byte swizzled TMA boxes)
-// sharing one full / empty barrier pair.  Groups of four compute warps
-// (16 of the 64 query rows each — 8 tokens x 8 heads, row 8 i + j) take
-// blocks of 4 pages in turn: one thread of the group issues Q K^T for the
-// block's 64 keys as four tcgen05.mma (M = 64 rows, N = 64 keys, K = 16)
-// into the group's 64 tensor-memory columns, the warps read the scores back
-// with tcgen05.ld in the mma.sync accumulator layout, run the online softmax
+// (one 4-KB TMA box per page: its 16 K rows, then its 16 V rows, 128-byte
+// swizzled) sharing one full / empty barrier pair.  Groups of four compute
+// warps (16 of the 64 query rows each — 8 tokens x 8 heads, row 8 i + j) take
+// blocks of 4 pages in turn: one thread of the group issues Q K^T over the
+// block's 128 rows (K and V alternating by page) as four tcgen05.mma (M = 64
+// rows, N = 128, K = 16) into the group's 128 tensor-memory columns, the
+// warps read back the 64 key columns with tcgen05.ld in the mma.sync
+// accumulator layout (the V columns are never read), run the online softmax
 // (base 2; masks only near the causal / window edges) and P V with mma.sync,
 // P going from the score registers straight into the A fragments.  Each
 // group keeps its own (max, sum, O), folded into one per CTA in group order.
@@ -38,15 +39,15 @@ constexpr int kA2Groups = 3;                              // groups of 4 compute
 constexpr int kA2ComputeWarps = 4 * kA2Groups;
 constexpr int kA2Threads = 32 * (kA2ComputeWarps + 1);   // the last warp produces
 constexpr int kA2Block = 4;                               // pages per softmax step (16 per page)
-constexpr int kA2TmemCols = 256;                          // one 64-column S tile per group
+constexpr int kA2TmemCols = 512;                          // one 128-column S tile per group
 constexpr int kA2RingBlocks = 12;
 constexpr int kA2Stages = kA2RingBlocks * kA2Block;       // pages in flight per CTA
 // ring slot k % stages always serves group (k / block) % groups: each group
 // waits on its own slots in order, so a full barrier's parity never aliases
 static_assert(kA2RingBlocks % kA2Groups == 0, "ring blocks must be a multiple of the groups");
 static_assert(32 % kA2Block == 0, "a block's table entries lie in one 32-entry chunk");
-static_assert(kA2Block == 4 && kA2Groups * 64 <= kA2TmemCols, "tcgen05 Q K^T: 64-key blocks");
-constexpr uint32_t kA2PageBytes = 4096;                   // K box + V box
+static_assert(kA2Block == 4 && kA2Groups * 128 <= kA2TmemCols, "tcgen05 Q K^T: 4-page blocks, N = 128");
+constexpr uint32_t kA2PageBytes = 4096;                   // one box: 16 K rows, then 16 V rows
 constexpr int kA2OStride = 68;                            // floats per row of the O partial
 constexpr int kA2MaxSplits = 16;
 constexpr int kA2AutoSplits = 8;   // the largest split chosen by default
@@ -161,21 +162,15 @@ __device__ __forceinline__ void a2_tmem_dealloc(uint32_t taddr)
                  : "memory");
 }
 
-// 16 lanes x 64 consecutive 32-bit columns of tensor memory in the layout of
+// 16 lanes x 16 consecutive 32-bit columns of tensor memory in the layout of
 // mma.sync accumulators: register 4 i + e of thread (gq = lane / 4, t = lane % 4)
 // holds lane taddr.lane + gq (+ 8 for e >= 2), column taddr.col + 8 i + 2 t + (e & 1).
-__device__ __forceinline__ void a2_tmem_ld_16x256b_x8(uint32_t taddr, uint32_t (&r)[32])
+__device__ __forceinline__ void a2_tmem_ld_16x256b_x2(uint32_t taddr, uint32_t *r)
 {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
-        "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
-        "%30, %31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
-          "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
-          "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
+    asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                   "=r"(r[7])
+                 : "r"(taddr));
 }
 
 // 2^x for x <= 0 (softmax weights): the hardware approximation, subnormal
@@ -311,13 +306,34 @@ __global__ void __launch_bounds__(kA2Threads, 1)
     griddep_wait();   // q, the cache, the table and the lengths come from earlier kernels
 
     // ---- the request: length and visible pages ----------------------------
+    // Issued together, before anything waits on one of them: the length, the
+    // producer's first 32 table entries (without a window they do not depend
+    // on the length), and the compute warps' Q and gate tiles.
+    const int32_t *bt = p.block_table + (size_t)r * p.max_blocks;
+    int first_entry = 0;
+    if (warp == kA2ComputeWarps && p.window == 0 && (int)z + lane * S < p.max_blocks) first_entry = bt[z + lane * S];
     const int L = p.context_lens[r];
+    if (warp < kA2ComputeWarps) {
+        // Q tile [64 rows][64 dims], row 8 i + j = token i, head 8 g + j;
+        // 128-byte rows with the chunk XORed by row % 8 (as TMA would); the
+        // same rows' gate heads for the finish (no global load at the tail)
+        const int gate_col = kQPerKv * p.nkv * kHeadDim + 2 * p.nkv * kHeadDim;
+        for (int c = threadIdx.x; c < 512; c += 32 * kA2ComputeWarps) {
+            const int row = c >> 3, cc = c & 7;
+            const uint16_t *src = p.qkv + ((size_t)r * 8 + (row >> 3)) * p.N + (size_t)(8 * g + (row & 7)) * kHeadDim + 8 * cc;
+            const uint4 qv = *reinterpret_cast<const uint4 *>(src);
+            const uint4 gv = *reinterpret_cast<const uint4 *>(src + gate_col);
+            *reinterpret_cast<uint4 *>(smem + LY.q + row * 128 + ((cc ^ (row & 7)) << 4)) = qv;
+            *reinterpret_cast<uint4 *>(smem + LY.gate + row * 128 + 16 * cc) = gv;
+        }
+        // the tensor cores read Q through the async proxy
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
     const int nblk = (L + kPageSlots - 1) / kPageSlots;
     const bool len_ok = L >= 8 && nblk <= p.max_blocks;
     if (!len_ok && threadIdx.x == 0 && z == 0 && g == 0) atomicOr(&g_status, QKVF_STATUS_BAD_REQUEST);
     const int p_first = (p.window > 0 && L - 8 - p.window + 1 > 0) ? (L - 8 - p.window + 1) / kPageSlots : 0;
     const int p_last = len_ok ? (L - 1) / kPageSlots : -1;
-    const int32_t *bt = p.block_table + (size_t)r * p.max_blocks;
     const bool req_ok = len_ok;
     const int first_mine = p_first + (int)z;
     const int npages = (len_ok && first_mine <= p_last) ? (p_last - first_mine) / S + 1 : 0;
@@ -328,7 +344,8 @@ __global__ void __launch_bounds__(kA2Threads, 1)
         // chunk c), one chunk ahead of the copies, so no copy waits on a
         // table read.  Per block of 4 pages: lane 0 waits for the ring block
         // and arms its full barrier with the block's bytes, then the lanes
-        // holding the block's pages issue their copies side by side.  An
+        // holding the block's pages issue their copies side by side, one
+        // 4-KB box per page.  An
         // entry outside the cache is flagged (the request's rows are then
         // skipped by every rank) and page 0 copied instead, so the ring's
         // accounting does not change.
@@ -337,7 +354,8 @@ __global__ void __launch_bounds__(kA2Threads, 1)
         int issued = 0;   // blocks
         unsigned bad = 0u;
         bool stop = false;
-        int next = lane < npages ? bt[first_mine + lane * S] : 0;
+        // (with a window the first entries wait for the length)
+        int next = lane < npages ? (p.window == 0 ? first_entry : bt[first_mine + lane * S]) : 0;
         for (int c = 0; c < npages && !stop; c += 32) {
             int page = next;
             if (c + 32 + lane < npages) next = bt[first_mine + (c + 32 + lane) * S];
@@ -361,12 +379,9 @@ __global__ void __launch_bounds__(kA2Threads, 1)
                 }
                 const int b = c + lane - k0;   // this lane's page within the block
                 if (b >= 0 && b < nb) {
-                    // the block's K rows together, then its V rows: 64 keys of
-                    // 128 bytes each, one operand for Q K^T
+                    // page b of the block: its 16 K rows, then its 16 V rows
                     const uint32_t blk = sRing + (uint32_t)rb * (kA2Block * kA2PageBytes);
-                    tma_load_4d(blk + (uint32_t)b * 2048, &tmKV, full0 + 8 * rb, 0, 0, 0, page * p.nkv + g,
-                                pol_kv);
-                    tma_load_4d(blk + (uint32_t)(kA2Block + b) * 2048, &tmKV, full0 + 8 * rb, 0, 0, 1,
+                    tma_load_4d(blk + (uint32_t)b * kA2PageBytes, &tmKV, full0 + 8 * rb, 0, 0, 0,
                                 page * p.nkv + g, pol_kv);
                 }
                 ++issued;
@@ -391,31 +406,13 @@ __global__ void __launch_bounds__(kA2Threads, 1)
         // ---- compute: group grp = warp / 4 takes blocks grp, grp + G, ... ----
         const int tid = threadIdx.x;
         const int grp = warp >> 2, wig = warp & 3;   // group, warp in group (rows 16 wig ..)
-        if (req_ok) {
-            // Q tile [64 rows][64 dims], row 8 i + j = token i, head 8 g + j;
-            // 128-byte rows with the chunk XORed by row % 8 (as TMA would)
-            for (int c = tid; c < 512; c += 32 * kA2ComputeWarps) {
-                const int row = c >> 3, cc = c & 7;
-                const uint4 v = *reinterpret_cast<const uint4 *>(
-                    p.qkv + ((size_t)r * 8 + (row >> 3)) * p.N + (size_t)(8 * g + (row & 7)) * kHeadDim + 8 * cc);
-                *reinterpret_cast<uint4 *>(smem + LY.q + row * 128 + ((cc ^ (row & 7)) << 4)) = v;
-            }
-            // the same rows' gate heads, for the finish (no global load at the tail)
-            const int gate_col = kQPerKv * p.nkv * kHeadDim + 2 * p.nkv * kHeadDim;
-            for (int c = tid; c < 512; c += 32 * kA2ComputeWarps) {
-                const int row = c >> 3, cc = c & 7;
-                *reinterpret_cast<uint4 *>(smem + LY.gate + row * 128 + 16 * cc) = *reinterpret_cast<const uint4 *>(
-                    p.qkv + ((size_t)r * 8 + (row >> 3)) * p.N + gate_col + (size_t)(8 * g + (row & 7)) * kHeadDim + 8 * cc);
-            }
-            // the tensor cores read Q through the async proxy
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        }
-        a2_compute_bar_sync();
+        a2_compute_bar_sync();   // the Q tile is in shared memory
         const int gq = lane >> 2, t = lane & 3;
-        // tcgen05 Q K^T: the group's S tile [64 rows x 64 keys] in tensor memory
-        // columns 64 grp.., rows 16 w .. 16 w + 15 in lanes 32 w .. 32 w + 15
+        // tcgen05 Q K^T: the group's S tile [64 rows x 128] in tensor memory
+        // columns 128 grp.., rows 16 w .. 16 w + 15 in lanes 32 w .. 32 w + 15;
+        // column 32 b + s is key s of the block's page b (32 b + 16 + s: Q . V, unused)
         const uint32_t sbar = smem_u32(smem + LY.sbar) + 8 * grp;
-        const uint32_t tS = *reinterpret_cast<volatile uint32_t *>(smem + LY.tslot) + 64u * grp;
+        const uint32_t tS = *reinterpret_cast<volatile uint32_t *>(smem + LY.tslot) + 128u * grp;
         const bool issuer = wig == 0 && lane == 0;
         uint32_t sph = 0;            // phase of sbar this block waits for
         int committed = 0, observed = 0;   // the issuer's commits, and those it saw complete
@@ -450,8 +447,8 @@ __global__ void __launch_bounds__(kA2Threads, 1)
             const bool inside = nb == kA2Block && key_first >= edge_lo && key_last <= edge_hi;
             bool landed = mbar_try_wait(full0 + 8 * rb, ph) ||
                           bounded_wait(full0 + 8 * rb, ph, s_flags, p.wait_limit_ns, true);
-            const uint32_t kreg = sRing + (uint32_t)rb * (kA2Block * kA2PageBytes);   // the block's K rows
-            const uint32_t vreg = kreg + kA2Block * 2048;                            // then its V rows
+            // the block's 4 pages, each 16 K rows then 16 V rows of 128 bytes
+            const uint32_t kreg = sRing + (uint32_t)rb * (kA2Block * kA2PageBytes);
             // every warp of the group is past the previous block's tcgen05.ld
             tc_fence_before();
             a2_group_bar_sync(grp);
@@ -460,7 +457,7 @@ __global__ void __launch_bounds__(kA2Threads, 1)
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)   // K = 16 dims per instruction: 32 bytes along the rows
                     umma_bf16(tS, umma_desc_sw128(sQ + 32u * kk), umma_desc_sw128(kreg + 32u * kk),
-                              umma_idesc_bf16(64, 64), kk != 0 ? 1u : 0u);
+                              umma_idesc_bf16(64, 128), kk != 0 ? 1u : 0u);
                 umma_commit(sbar);
                 ++committed;
             }
@@ -472,7 +469,9 @@ __global__ void __launch_bounds__(kA2Threads, 1)
                 float sc[2 * kA2Block][4];
                 tc_fence_after();
                 uint32_t rr[32];
-                a2_tmem_ld_16x256b_x8(tS + ((uint32_t)(32 * wig) << 16), rr);
+#pragma unroll
+                for (int b = 0; b < kA2Block; ++b)   // page b's 16 key columns
+                    a2_tmem_ld_16x256b_x2(tS + ((uint32_t)(32 * wig) << 16) + 32u * b, rr + 8 * b);
                 tmem_ld_wait();
 #pragma unroll
                 for (int nt = 0; nt < 2 * kA2Block; ++nt)
@@ -557,7 +556,7 @@ __global__ void __launch_bounds__(kA2Threads, 1)
 #pragma unroll
                 for (int b = 0; b < kA2Block; ++b) {
                     if (b < nb) {
-                        const uint32_t vbox = vreg + (uint32_t)b * 2048;
+                        const uint32_t vbox = kreg + (uint32_t)b * kA2PageBytes + 2048;   // page b's V rows
                         // P (rows a / b x the page's 16 keys) as the A fragment of PV
                         const uint32_t pa0 = pack_f2bf(sc[2 * b][0], sc[2 * b][1]);
                         const uint32_t pa1 = pack_f2bf(sc[2 * b][2], sc[2 * b][3]);
@@ -589,71 +588,115 @@ __global__ void __launch_bounds__(kA2Threads, 1)
             l_a += __shfl_xor_sync(0xffffffffu, l_a, off);
             l_b += __shfl_xor_sync(0xffffffffu, l_b, off);
         }
-        // this group's partial: rows of the CTA, the group's own slice
-        float *og = o_part + grp * (64 * kA2OStride);
+        // Fold the groups' partials into group 0's registers, in group order:
+        // groups 1.. leave theirs in shared memory (over the drained ring)
         const int ra = wig * 16 + gq, rb = ra + 8;
+        if (grp > 0) {
+            float *og = o_part + grp * (64 * kA2OStride);
 #pragma unroll
-        for (int nd = 0; nd < 8; ++nd) {
-            og[ra * kA2OStride + 8 * nd + 2 * t] = o[nd][0];
-            og[ra * kA2OStride + 8 * nd + 2 * t + 1] = o[nd][1];
-            og[rb * kA2OStride + 8 * nd + 2 * t] = o[nd][2];
-            og[rb * kA2OStride + 8 * nd + 2 * t + 1] = o[nd][3];
+            for (int nd = 0; nd < 8; ++nd) {
+                *reinterpret_cast<float2 *>(og + ra * kA2OStride + 8 * nd + 2 * t) = make_float2(o[nd][0], o[nd][1]);
+                *reinterpret_cast<float2 *>(og + rb * kA2OStride + 8 * nd + 2 * t) = make_float2(o[nd][2], o[nd][3]);
+            }
+            if (t == 0) {
+                m_part[grp * 64 + ra] = m_a;
+                m_part[grp * 64 + rb] = m_b;
+                l_part[grp * 64 + ra] = l_a;
+                l_part[grp * 64 + rb] = l_b;
+            }
         }
-        if (t == 0) {
-            m_part[grp * 64 + ra] = m_a;
-            m_part[grp * 64 + rb] = m_b;
-            l_part[grp * 64 + ra] = l_a;
-            l_part[grp * 64 + rb] = l_b;
-        }
-        if (kA2Groups > 1) {
-            // fold the groups' partials into group 0's, in group order
-            a2_compute_bar_sync();
-            for (int it = tid; it < 64 * 32; it += 32 * kA2ComputeWarps) {
-                const int row = it >> 5, d = 2 * (it & 31);
-                float M = -INFINITY;
+        a2_compute_bar_sync();
+        if (grp == 0) {
+            float w_a[kA2Groups], w_b[kA2Groups];
+            {
+                float mg_a[kA2Groups], mg_b[kA2Groups];
+                mg_a[0] = m_a;
+                mg_b[0] = m_b;
 #pragma unroll
-                for (int gg = 0; gg < kA2Groups; ++gg) M = fmaxf(M, m_part[gg * 64 + row]);
-                const float base = M == -INFINITY ? 0.f : M;
-                float o0 = 0.f, o1 = 0.f;
+                for (int gg = 1; gg < kA2Groups; ++gg) {
+                    mg_a[gg] = m_part[gg * 64 + ra];
+                    mg_b[gg] = m_part[gg * 64 + rb];
+                }
+                float M_a = -INFINITY, M_b = -INFINITY;
 #pragma unroll
                 for (int gg = 0; gg < kA2Groups; ++gg) {
-                    const float w = exp2f(m_part[gg * 64 + row] - base);
-                    const float2 v = *reinterpret_cast<const float2 *>(o_part + gg * 64 * kA2OStride + row * kA2OStride + d);
-                    o0 = o0 + v.x * w;
-                    o1 = o1 + v.y * w;
+                    M_a = fmaxf(M_a, mg_a[gg]);
+                    M_b = fmaxf(M_b, mg_b[gg]);
                 }
-                *reinterpret_cast<float2 *>(o_part + row * kA2OStride + d) = make_float2(o0, o1);
+                const float base_a = M_a == -INFINITY ? 0.f : M_a, base_b = M_b == -INFINITY ? 0.f : M_b;
+#pragma unroll
+                for (int gg = 0; gg < kA2Groups; ++gg) {
+                    w_a[gg] = exp2f(mg_a[gg] - base_a);
+                    w_b[gg] = exp2f(mg_b[gg] - base_b);
+                }
+                m_a = M_a;
+                m_b = M_b;
             }
-            a2_compute_bar_sync();   // every O item used the groups' maxima
-            if (tid < 64) {
-                float M = -INFINITY;
+            float lt_a = 0.f, lt_b = 0.f;
+            lt_a = lt_a + l_a * w_a[0];
+            lt_b = lt_b + l_b * w_b[0];
 #pragma unroll
-                for (int gg = 0; gg < kA2Groups; ++gg) M = fmaxf(M, m_part[gg * 64 + tid]);
-                const float base = M == -INFINITY ? 0.f : M;
-                float lt = 0.f;
+            for (int gg = 1; gg < kA2Groups; ++gg) {
+                lt_a = lt_a + l_part[gg * 64 + ra] * w_a[gg];
+                lt_b = lt_b + l_part[gg * 64 + rb] * w_b[gg];
+            }
+            l_a = lt_a;
+            l_b = lt_b;
 #pragma unroll
-                for (int gg = 0; gg < kA2Groups; ++gg) lt = lt + l_part[gg * 64 + tid] * exp2f(m_part[gg * 64 + tid] - base);
-                m_part[tid] = M;
-                l_part[tid] = lt;
+            for (int nd = 0; nd < 8; ++nd) {
+                float f0 = 0.f, f1 = 0.f, f2 = 0.f, f3 = 0.f;
+                f0 = f0 + o[nd][0] * w_a[0];
+                f1 = f1 + o[nd][1] * w_a[0];
+                f2 = f2 + o[nd][2] * w_b[0];
+                f3 = f3 + o[nd][3] * w_b[0];
+#pragma unroll
+                for (int gg = 1; gg < kA2Groups; ++gg) {
+                    const float *og = o_part + gg * (64 * kA2OStride);
+                    const float2 va = *reinterpret_cast<const float2 *>(og + ra * kA2OStride + 8 * nd + 2 * t);
+                    const float2 vb = *reinterpret_cast<const float2 *>(og + rb * kA2OStride + 8 * nd + 2 * t);
+                    f0 = f0 + va.x * w_a[gg];
+                    f1 = f1 + va.y * w_a[gg];
+                    f2 = f2 + vb.x * w_b[gg];
+                    f3 = f3 + vb.y * w_b[gg];
+                }
+                o[nd][0] = f0;
+                o[nd][1] = f1;
+                o[nd][2] = f2;
+                o[nd][3] = f3;
+            }
+            if constexpr (kWorkspace) {
+                // ---- publish this CTA's partial: O [64][64], m, l, the bad-entry flag ----
+                float *slot = p.ws + (((size_t)r * p.nkv + g) * S + z) * kA2WsSlotFloats;
+#pragma unroll
+                for (int nd = 0; nd < 8; ++nd) {
+                    __stcg(reinterpret_cast<float2 *>(slot + ra * 64 + 8 * nd + 2 * t), make_float2(o[nd][0], o[nd][1]));
+                    __stcg(reinterpret_cast<float2 *>(slot + rb * 64 + 8 * nd + 2 * t), make_float2(o[nd][2], o[nd][3]));
+                }
+                if (t == 0) {
+                    __stcg(slot + 4096 + ra, m_a);
+                    __stcg(slot + 4096 + rb, m_b);
+                    __stcg(slot + 4160 + ra, l_a);
+                    __stcg(slot + 4160 + rb, l_b);
+                }
+                if (tid == 0) __stcg(reinterpret_cast<int *>(slot + 4224), s_flags[1]);
+            } else {
+                // the CTA's partial for the ranks' merge or the finish: slice 0
+#pragma unroll
+                for (int nd = 0; nd < 8; ++nd) {
+                    *reinterpret_cast<float2 *>(o_part + ra * kA2OStride + 8 * nd + 2 * t) = make_float2(o[nd][0], o[nd][1]);
+                    *reinterpret_cast<float2 *>(o_part + rb * kA2OStride + 8 * nd + 2 * t) = make_float2(o[nd][2], o[nd][3]);
+                }
+                if (t == 0) {
+                    m_part[ra] = m_a;
+                    m_part[rb] = m_b;
+                    l_part[ra] = l_a;
+                    l_part[rb] = l_b;
+                }
             }
         }
     }
     __syncthreads();
-    if constexpr (kWorkspace) {
-        // ---- publish this CTA's partial: O [64][64], m, l, the bad-entry flag ----
-        const int tid = threadIdx.x;
-        float *slot = p.ws + (((size_t)r * p.nkv + g) * S + z) * kA2WsSlotFloats;
-        for (int it = tid; it < 64 * 16; it += kA2Threads) {
-            const int row = it >> 4, c4 = it & 15;
-            __stcg(reinterpret_cast<float4 *>(slot + row * 64 + 4 * c4),
-                   *reinterpret_cast<const float4 *>(o_part + row * kA2OStride + 4 * c4));
-        }
-        if (tid < 64) {
-            __stcg(slot + 4096 + tid, m_part[tid]);
-            __stcg(slot + 4160 + tid, l_part[tid]);
-        }
-        if (tid == 0) __stcg(reinterpret_cast<int *>(slot + 4224), s_flags[1]);
-    } else {
+    if constexpr (!kWorkspace) {
         if (S > 1) cluster_sync_all();
 
         // a request with an entry outside the cache on any rank is skipped by all
@@ -718,12 +761,16 @@ __global__ void __launch_bounds__(kA2Threads, 1)
 
 // Merge of the split-KV engine, the grid after attn2_kernel<true> on the
 // stream: one warp per output row of (request, KV head).  Lane l holds the
-// maxima and sums of splits l, l + 32, ...; the row's maximum and sum are warp
-// reductions in a fixed order; O is summed over the splits in split order,
-// 32 splits' loads in flight per batch; then o-norm, gate, store.
-constexpr int kA2MergeWarps = 8;
+// maximum and sum of split l (of l, l + 32, ... past 32 splits); the row's
+// maximum and sum are warp reductions in a fixed order; O is summed over the
+// splits in split order, 32 splits' loads in flight per batch; then o-norm,
+// gate, store.  Every load of the first batch is issued before any is used
+// (one round trip), and the grid's CTAs are small enough (128 threads, at most
+// 96 registers) to sit beside an attn2_kernel CTA (416 x 128 registers), so
+// they are resident and waiting when the partials land.
+constexpr int kA2MergeWarps = 4;
 
-__global__ void __launch_bounds__(32 * kA2MergeWarps) attn2_merge_kernel(const Attn2Params p)
+__global__ void __maxnreg__(96) attn2_merge_kernel(const Attn2Params p)
 {
     __shared__ float w_sh[kA2MergeWarps][kA2WsMaxSplits];
     if (threadIdx.x == 0) griddep_launch_dependents();
@@ -732,47 +779,38 @@ __global__ void __launch_bounds__(32 * kA2MergeWarps) attn2_merge_kernel(const A
     const int row = blockIdx.x * kA2MergeWarps + warp, g = blockIdx.y, r = blockIdx.z;
     const int S = p.splits;
     const float *slots = p.ws + ((size_t)r * p.nkv + g) * S * kA2WsSlotFloats;
-    // every load of the row first: the length, the gate, the splits' maxima,
-    // sums and flags, and the first 32 splits' O
     const int L = p.context_lens[r];
     const __nv_bfloat162 gt = a2_gate(p, r, g, row, lane);
-    constexpr int kPer = kA2WsMaxSplits / 32;
-    float ml[kPer], ll[kPer];
+    float m0 = -INFINITY, l0 = 0.f;
     unsigned bad = 0u;
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-        const int src = lane + 32 * j;
-        ml[j] = -INFINITY;
-        ll[j] = 0.f;
-        if (src < S) {
-            const float *sl = slots + (size_t)src * kA2WsSlotFloats;
-            ml[j] = __ldcg(sl + 4096 + row);
-            ll[j] = __ldcg(sl + 4160 + row);
-            bad |= (unsigned)__ldcg(reinterpret_cast<const int *>(sl + 4224));
-        }
+    if (lane < S) {
+        const float *sl = slots + (size_t)lane * kA2WsSlotFloats;
+        m0 = __ldcg(sl + 4096 + row);
+        l0 = __ldcg(sl + 4160 + row);
+        bad = (unsigned)__ldcg(reinterpret_cast<const int *>(sl + 4224));
     }
     float2 v[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j)
         if (j < S)
             v[j] = __ldcg(reinterpret_cast<const float2 *>(slots + (size_t)j * kA2WsSlotFloats + row * 64 + 2 * lane));
-    if (L < 8 || (L + kPageSlots - 1) / kPageSlots > p.max_blocks) return;   // a bad request: rows skipped
-    if (__any_sync(0xffffffffu, bad != 0u)) return;                          // a page outside the cache
-    float M = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) M = fmaxf(M, ml[j]);
+    float M = m0;
+    for (int src = lane + 32; src < S; src += 32) M = fmaxf(M, __ldcg(slots + (size_t)src * kA2WsSlotFloats + 4096 + row));
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     const float base = M == -INFINITY ? 0.f : M;
     float lt = 0.f;
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-        const int src = lane + 32 * j;
-        if (src < S) {
-            const float w = exp2f(ml[j] - base);
-            w_sh[warp][src] = w;
-            lt = lt + ll[j] * w;
-        }
+    if (lane < S) {
+        const float w = exp2f(m0 - base);
+        w_sh[warp][lane] = w;
+        lt = lt + l0 * w;
+    }
+    for (int src = lane + 32; src < S; src += 32) {
+        const float *sl = slots + (size_t)src * kA2WsSlotFloats;
+        const float w = exp2f(__ldcg(sl + 4096 + row) - base);
+        w_sh[warp][src] = w;
+        lt = lt + __ldcg(sl + 4160 + row) * w;
+        bad |= (unsigned)__ldcg(reinterpret_cast<const int *>(sl + 4224));
     }
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) lt += __shfl_xor_sync(0xffffffffu, lt, off);
@@ -795,7 +833,9 @@ __global__ void __launch_bounds__(32 * kA2MergeWarps) attn2_merge_kernel(const A
             }
         }
     }
-    a2_finish_row(p, r, g, row, o0, o1, lt, lane, gt);
+    // a bad request, or a page outside the cache on any split: rows skipped
+    const bool req_ok = L >= 8 && (L + kPageSlots - 1) / kPageSlots <= p.max_blocks;
+    if (req_ok && !__any_sync(0xffffffffu, bad != 0u)) a2_finish_row(p, r, g, row, o0, o1, lt, lane, gt);
 }
 
 int encode_kv_map(const uint16_t *kv_cache, int64_t num_pages, int nkv, CUtensorMap *m)
@@ -803,11 +843,11 @@ int encode_kv_map(const uint16_t *kv_cache, int64_t num_pages, int nkv, CUtensor
     // the cache [pages * nkv][16 slots][2 halves][64] seen with the half
     // dimension outside the slot dimension: dim 0 = 64 elements of a half,
     // dim 1 = slot (256 B apart), dim 2 = K / V half (128 B apart), dim 3 =
-    // (page, KV head).  A {64, 16, 1, 1} box is the 16 K (or V) rows of a
-    // page of one KV head, 128 bytes each, swizzled
+    // (page, KV head).  A {64, 16, 2, 1} box is one page of one KV head in
+    // shared memory as its 16 K rows, then its 16 V rows, 128 bytes each, swizzled
     const cuuint64_t dims[4] = {64, (cuuint64_t)kPageSlots, 2, (cuuint64_t)num_pages * nkv};
     const cuuint64_t strides[3] = {256, 128, (cuuint64_t)kPageSlots * kSlotWidth * 2};
-    const cuuint32_t box[4] = {64, (cuuint32_t)kPageSlots, 1, 1};
+    const cuuint32_t box[4] = {64, (cuuint32_t)kPageSlots, 2, 1};
     const cuuint32_t es[4] = {1, 1, 1, 1};
     return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, (void *)kv_cache, dims, strides, box, es,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
