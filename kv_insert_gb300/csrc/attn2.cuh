@@ -53,7 +53,25 @@ constexpr int kA2MaxSplits = 16;
 constexpr int kA2AutoSplits = 8;   // the largest split chosen by default
 constexpr int kA2MaxRequests = 65535;   // grid z
 constexpr int kA2WsMaxSplits = 256;     // workspace engine: CTAs per (request, KV head)
-constexpr int kA2WsSlotFloats = 64 * 64 + 64 + 64 + 64;   // O [64][64], m, l, flags: 17152 bytes
+constexpr int kA2WsSlotFloats = 64 * 64 + 64 + 64 + 64;   // per split: O [64][64], m, l, flag: 17152 bytes
+
+// The split-KV partials of one (request, KV head), S * kA2WsSlotFloats floats:
+// the S O partials [64 rows][64] (split order), then the row maxima [64][S]
+// and the row sums [64][S] (a row's S values side by side, so one load of a
+// warp reads them all), then the S bad-entry flags, then padding.
+struct A2WsRegion {
+    float *o, *m, *l;
+    int *bad;
+};
+__device__ __forceinline__ A2WsRegion a2_ws_region(float *ws, int r, int nkv, int g, int S)
+{
+    A2WsRegion w;
+    w.o = ws + ((size_t)r * nkv + g) * S * kA2WsSlotFloats;
+    w.m = w.o + (size_t)S * 4096;
+    w.l = w.m + (size_t)S * 64;
+    w.bad = reinterpret_cast<int *>(w.l + (size_t)S * 64);
+    return w;
+}
 
 struct A2Layout {
     uint32_t q, gate, ring, full, empty, sbar, tslot, o, m, l, flags, total;
@@ -666,19 +684,20 @@ __global__ void __launch_bounds__(kA2Threads, 1)
             }
             if constexpr (kWorkspace) {
                 // ---- publish this CTA's partial: O [64][64], m, l, the bad-entry flag ----
-                float *slot = p.ws + (((size_t)r * p.nkv + g) * S + z) * kA2WsSlotFloats;
+                const A2WsRegion wr = a2_ws_region(p.ws, r, p.nkv, g, S);
+                float *slot = wr.o + (size_t)z * 4096;
 #pragma unroll
                 for (int nd = 0; nd < 8; ++nd) {
                     __stcg(reinterpret_cast<float2 *>(slot + ra * 64 + 8 * nd + 2 * t), make_float2(o[nd][0], o[nd][1]));
                     __stcg(reinterpret_cast<float2 *>(slot + rb * 64 + 8 * nd + 2 * t), make_float2(o[nd][2], o[nd][3]));
                 }
                 if (t == 0) {
-                    __stcg(slot + 4096 + ra, m_a);
-                    __stcg(slot + 4096 + rb, m_b);
-                    __stcg(slot + 4160 + ra, l_a);
-                    __stcg(slot + 4160 + rb, l_b);
+                    __stcg(wr.m + ra * S + z, m_a);
+                    __stcg(wr.m + rb * S + z, m_b);
+                    __stcg(wr.l + ra * S + z, l_a);
+                    __stcg(wr.l + rb * S + z, l_b);
                 }
-                if (tid == 0) __stcg(reinterpret_cast<int *>(slot + 4224), s_flags[1]);
+                if (tid == 0) __stcg(wr.bad + z, s_flags[1]);
             } else {
                 // the CTA's partial for the ranks' merge or the finish: slice 0
 #pragma unroll
@@ -765,12 +784,11 @@ __global__ void __launch_bounds__(kA2Threads, 1)
 // maximum and sum are warp reductions in a fixed order; O is summed over the
 // splits in split order, 32 splits' loads in flight per batch; then o-norm,
 // gate, store.  Every load of the first batch is issued before any is used
-// (one round trip), and the grid's CTAs are small enough (128 threads, at most
-// 96 registers) to sit beside an attn2_kernel CTA (416 x 128 registers), so
-// they are resident and waiting when the partials land.
+// (one round trip); a row's maxima, sums and flags are one coalesced load
+// each (scattered per-split loads doubled the round trip at 19 splits).
 constexpr int kA2MergeWarps = 4;
 
-__global__ void __maxnreg__(96) attn2_merge_kernel(const Attn2Params p)
+__global__ void __launch_bounds__(32 * kA2MergeWarps) attn2_merge_kernel(const Attn2Params p)
 {
     __shared__ float w_sh[kA2MergeWarps][kA2WsMaxSplits];
     if (threadIdx.x == 0) griddep_launch_dependents();
@@ -778,24 +796,23 @@ __global__ void __maxnreg__(96) attn2_merge_kernel(const Attn2Params p)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int row = blockIdx.x * kA2MergeWarps + warp, g = blockIdx.y, r = blockIdx.z;
     const int S = p.splits;
-    const float *slots = p.ws + ((size_t)r * p.nkv + g) * S * kA2WsSlotFloats;
+    const A2WsRegion wr = a2_ws_region(p.ws, r, p.nkv, g, S);
+    const float *mrow = wr.m + row * S, *lrow = wr.l + row * S;
     const int L = p.context_lens[r];
     const __nv_bfloat162 gt = a2_gate(p, r, g, row, lane);
     float m0 = -INFINITY, l0 = 0.f;
     unsigned bad = 0u;
     if (lane < S) {
-        const float *sl = slots + (size_t)lane * kA2WsSlotFloats;
-        m0 = __ldcg(sl + 4096 + row);
-        l0 = __ldcg(sl + 4160 + row);
-        bad = (unsigned)__ldcg(reinterpret_cast<const int *>(sl + 4224));
+        m0 = __ldcg(mrow + lane);
+        l0 = __ldcg(lrow + lane);
+        bad = (unsigned)__ldcg(wr.bad + lane);
     }
     float2 v[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j)
-        if (j < S)
-            v[j] = __ldcg(reinterpret_cast<const float2 *>(slots + (size_t)j * kA2WsSlotFloats + row * 64 + 2 * lane));
+        if (j < S) v[j] = __ldcg(reinterpret_cast<const float2 *>(wr.o + (size_t)j * 4096 + row * 64 + 2 * lane));
     float M = m0;
-    for (int src = lane + 32; src < S; src += 32) M = fmaxf(M, __ldcg(slots + (size_t)src * kA2WsSlotFloats + 4096 + row));
+    for (int src = lane + 32; src < S; src += 32) M = fmaxf(M, __ldcg(mrow + src));
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     const float base = M == -INFINITY ? 0.f : M;
@@ -806,11 +823,10 @@ __global__ void __maxnreg__(96) attn2_merge_kernel(const Attn2Params p)
         lt = lt + l0 * w;
     }
     for (int src = lane + 32; src < S; src += 32) {
-        const float *sl = slots + (size_t)src * kA2WsSlotFloats;
-        const float w = exp2f(__ldcg(sl + 4096 + row) - base);
+        const float w = exp2f(__ldcg(mrow + src) - base);
         w_sh[warp][src] = w;
-        lt = lt + __ldcg(sl + 4160 + row) * w;
-        bad |= (unsigned)__ldcg(reinterpret_cast<const int *>(sl + 4224));
+        lt = lt + __ldcg(lrow + src) * w;
+        bad |= (unsigned)__ldcg(wr.bad + src);
     }
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) lt += __shfl_xor_sync(0xffffffffu, lt, off);
@@ -821,8 +837,7 @@ __global__ void __maxnreg__(96) attn2_merge_kernel(const Attn2Params p)
 #pragma unroll
             for (int j = 0; j < 32; ++j)
                 if (s0 + j < S)
-                    v[j] = __ldcg(reinterpret_cast<const float2 *>(slots + (size_t)(s0 + j) * kA2WsSlotFloats +
-                                                                   row * 64 + 2 * lane));
+                    v[j] = __ldcg(reinterpret_cast<const float2 *>(wr.o + (size_t)(s0 + j) * 4096 + row * 64 + 2 * lane));
         }
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
@@ -927,8 +942,9 @@ int attn2_split_kv_splits_for(int num_reqs, int nkv, int max_blocks, int window,
     return s < 1 ? 1 : (int)s;
 }
 
-// Workspace of the split-KV engine: R * nkv * S partial slots of 17152 bytes
-// (O [64][64], the 64 row maxima and sums, the bad-entry flag; FP32).
+// Workspace of the split-KV engine: R * nkv * S partials of 17152 bytes
+// (O [64][64], the 64 row maxima and sums, the bad-entry flag; FP32), laid
+// out per (request, KV head) as a2_ws_region describes.
 size_t a2_workspace_bytes(int num_reqs, int nkv, int splits)
 {
     return (size_t)num_reqs * nkv * splits * kA2WsSlotFloats * 4;
