@@ -16,14 +16,15 @@
 //
 // Design: a CTA per (request r, KV head g, split z).  A producer warp streams
 // the CTA's pages (p0 + z, p0 + z + S, ...) into a ring of blocks of 4 pages
-// (one 4-KB TMA box per page: its 16 K rows, then its 16 V rows, 128-byte
-// swizzled) sharing one full / empty barrier pair.  Groups of four compute
-// warps (16 of the 64 query rows each — 8 tokens x 8 heads, row 8 i + j) take
-// blocks of 4 pages in turn: one thread of the group issues Q K^T over the
-// block's 128 rows (K and V alternating by page) as four tcgen05.mma (M = 64
-// rows, N = 128, K = 16) into the group's 128 tensor-memory columns, the
-// warps read back the 64 key columns with tcgen05.ld in the mma.sync
-// accumulator layout (the V columns are never read), run the online softmax
+// (one 4-KB TMA box per page, 128-byte swizzled: K rows of slots 0-7, V rows
+// of slots 0-7, K rows of slots 8-15, V rows of slots 8-15, 1 KB each)
+// sharing one full / empty barrier pair.  Groups of four compute warps (16 of
+// the 64 query rows each — 8 tokens x 8 heads, row 8 i + j) take blocks of 4
+// pages in turn: one thread of the group issues Q K^T for the block's 64 keys
+// as four tcgen05.mma (M = 64 rows, N = 64 keys, K = 16; the keys' 8-row
+// groups 2 KB apart) into the group's 64 tensor-memory columns, the warps
+// read the scores back with tcgen05.ld in the mma.sync accumulator layout,
+// run the online softmax
 // (base 2; masks only near the causal / window edges) and P V with mma.sync,
 // P going from the score registers straight into the A fragments.  Each
 // group keeps its own (max, sum, O), folded into one per CTA in group order.
@@ -39,15 +40,15 @@ constexpr int kA2Groups = 3;                              // groups of 4 compute
 constexpr int kA2ComputeWarps = 4 * kA2Groups;
 constexpr int kA2Threads = 32 * (kA2ComputeWarps + 1);   // the last warp produces
 constexpr int kA2Block = 4;                               // pages per softmax step (16 per page)
-constexpr int kA2TmemCols = 512;                          // one 128-column S tile per group
+constexpr int kA2TmemCols = 256;                          // one 64-column S tile per group
 constexpr int kA2RingBlocks = 12;
 constexpr int kA2Stages = kA2RingBlocks * kA2Block;       // pages in flight per CTA
 // ring slot k % stages always serves group (k / block) % groups: each group
 // waits on its own slots in order, so a full barrier's parity never aliases
 static_assert(kA2RingBlocks % kA2Groups == 0, "ring blocks must be a multiple of the groups");
 static_assert(32 % kA2Block == 0, "a block's table entries lie in one 32-entry chunk");
-static_assert(kA2Block == 4 && kA2Groups * 128 <= kA2TmemCols, "tcgen05 Q K^T: 4-page blocks, N = 128");
-constexpr uint32_t kA2PageBytes = 4096;                   // one box: 16 K rows, then 16 V rows
+static_assert(kA2Block == 4 && kA2Groups * 64 <= kA2TmemCols, "tcgen05 Q K^T: 4-page blocks of 64 keys");
+constexpr uint32_t kA2PageBytes = 4096;                   // one box: K 0-7, V 0-7, K 8-15, V 8-15
 constexpr int kA2OStride = 68;                            // floats per row of the O partial
 constexpr int kA2MaxSplits = 16;
 constexpr int kA2AutoSplits = 8;   // the largest split chosen by default
@@ -127,16 +128,17 @@ struct Attn2Params {
     float eps;
 };
 
-// `policy`: an L2 cache policy (createpolicy); the cache is streamed once, so
-// its lines go first and the rest of the working set (q, the partials, the
-// code) stays in L2
-__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *m, uint32_t bar, int c0,
-                                            int c1, int c2, int c3, uint64_t policy)
+// One page box of the 5-D cache map (coordinates 0, 0, 0, 0, c4).  `policy`:
+// an L2 cache policy (createpolicy); the cache is streamed once, so its lines
+// go first and the rest of the working set (q, the partials, the code) stays
+// in L2
+__device__ __forceinline__ void tma_load_page(uint32_t dst, const CUtensorMap *m, uint32_t bar, int c4,
+                                              uint64_t policy)
 {
     asm volatile(
-        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "l"(policy)
+        "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %3, %3, %3, %4}], [%2], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(0), "r"(c4), "l"(policy)
         : "memory");
 }
 
@@ -180,15 +182,34 @@ __device__ __forceinline__ void a2_tmem_dealloc(uint32_t taddr)
                  : "memory");
 }
 
-// 16 lanes x 16 consecutive 32-bit columns of tensor memory in the layout of
+// 16 lanes x 64 consecutive 32-bit columns of tensor memory in the layout of
 // mma.sync accumulators: register 4 i + e of thread (gq = lane / 4, t = lane % 4)
 // holds lane taddr.lane + gq (+ 8 for e >= 2), column taddr.col + 8 i + 2 t + (e & 1).
-__device__ __forceinline__ void a2_tmem_ld_16x256b_x2(uint32_t taddr, uint32_t *r)
+__device__ __forceinline__ void a2_tmem_ld_16x256b_x8(uint32_t taddr, uint32_t (&r)[32])
 {
-    asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-                   "=r"(r[7])
-                 : "r"(taddr));
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+        "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+        "%30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+          "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+          "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
+// Shared-memory descriptor of a 128-byte-swizzled K-major operand whose
+// 8-row groups lie `sbo` bytes apart (a page's K rows of slots 0-7 and 8-15,
+// and the next page's, are 2 KB apart in the ring)
+__device__ __forceinline__ uint64_t a2_desc_sw128(uint32_t saddr, uint32_t sbo)
+{
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);   // start address / 16
+    d |= (uint64_t)1 << 16;                             // leading offset (unused when swizzled)
+    d |= (uint64_t)(sbo >> 4) << 32;                    // stride offset: one 8-row group
+    d |= (uint64_t)1 << 46;                             // descriptor version
+    d |= (uint64_t)2 << 61;                             // 128-byte swizzle
+    return d;
 }
 
 // 2^x for x <= 0 (softmax weights): the hardware approximation, subnormal
@@ -396,11 +417,9 @@ __global__ void __launch_bounds__(kA2Threads, 1)
                     break;
                 }
                 const int b = c + lane - k0;   // this lane's page within the block
-                if (b >= 0 && b < nb) {
-                    // page b of the block: its 16 K rows, then its 16 V rows
+                if (b >= 0 && b < nb) {   // page b of the block
                     const uint32_t blk = sRing + (uint32_t)rb * (kA2Block * kA2PageBytes);
-                    tma_load_4d(blk + (uint32_t)b * kA2PageBytes, &tmKV, full0 + 8 * rb, 0, 0, 0,
-                                page * p.nkv + g, pol_kv);
+                    tma_load_page(blk + (uint32_t)b * kA2PageBytes, &tmKV, full0 + 8 * rb, page * p.nkv + g, pol_kv);
                 }
                 ++issued;
             }
@@ -426,11 +445,11 @@ __global__ void __launch_bounds__(kA2Threads, 1)
         const int grp = warp >> 2, wig = warp & 3;   // group, warp in group (rows 16 wig ..)
         a2_compute_bar_sync();   // the Q tile is in shared memory
         const int gq = lane >> 2, t = lane & 3;
-        // tcgen05 Q K^T: the group's S tile [64 rows x 128] in tensor memory
-        // columns 128 grp.., rows 16 w .. 16 w + 15 in lanes 32 w .. 32 w + 15;
-        // column 32 b + s is key s of the block's page b (32 b + 16 + s: Q . V, unused)
+        // tcgen05 Q K^T: the group's S tile [64 rows x 64 keys] in tensor memory
+        // columns 64 grp.., rows 16 w .. 16 w + 15 in lanes 32 w .. 32 w + 15;
+        // column 16 b + s is slot s of the block's page b
         const uint32_t sbar = smem_u32(smem + LY.sbar) + 8 * grp;
-        const uint32_t tS = *reinterpret_cast<volatile uint32_t *>(smem + LY.tslot) + 128u * grp;
+        const uint32_t tS = *reinterpret_cast<volatile uint32_t *>(smem + LY.tslot) + 64u * grp;
         const bool issuer = wig == 0 && lane == 0;
         uint32_t sph = 0;            // phase of sbar this block waits for
         int committed = 0, observed = 0;   // the issuer's commits, and those it saw complete
@@ -448,7 +467,8 @@ __global__ void __launch_bounds__(kA2Threads, 1)
             for (int e = 0; e < 4; ++e) o[nd][e] = 0.f;
         float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
 
-        const uint32_t v_key = (uint32_t)((lane & 7) + ((lane >> 3) & 1) * 8); // V: ldmatrix.trans row
+        // V: this lane's ldmatrix.trans row, slot (lane & 7) + 8 ((lane >> 3) & 1) of a page
+        const uint32_t v_row = (uint32_t)((lane & 7) * 128 + ((lane >> 3) & 1) * 2048);
         const uint32_t v_hi = (uint32_t)(lane >> 4);
         const uint32_t sw = (uint32_t)(lane & 7);
 
@@ -465,7 +485,7 @@ __global__ void __launch_bounds__(kA2Threads, 1)
             const bool inside = nb == kA2Block && key_first >= edge_lo && key_last <= edge_hi;
             bool landed = mbar_try_wait(full0 + 8 * rb, ph) ||
                           bounded_wait(full0 + 8 * rb, ph, s_flags, p.wait_limit_ns, true);
-            // the block's 4 pages, each 16 K rows then 16 V rows of 128 bytes
+            // the block's 4 pages; the 8-row groups of K (and of V) 2 KB apart
             const uint32_t kreg = sRing + (uint32_t)rb * (kA2Block * kA2PageBytes);
             // every warp of the group is past the previous block's tcgen05.ld
             tc_fence_before();
@@ -474,8 +494,8 @@ __global__ void __launch_bounds__(kA2Threads, 1)
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)   // K = 16 dims per instruction: 32 bytes along the rows
-                    umma_bf16(tS, umma_desc_sw128(sQ + 32u * kk), umma_desc_sw128(kreg + 32u * kk),
-                              umma_idesc_bf16(64, 128), kk != 0 ? 1u : 0u);
+                    umma_bf16(tS, umma_desc_sw128(sQ + 32u * kk), a2_desc_sw128(kreg + 32u * kk, 2048),
+                              umma_idesc_bf16(64, 64), kk != 0 ? 1u : 0u);
                 umma_commit(sbar);
                 ++committed;
             }
@@ -487,9 +507,7 @@ __global__ void __launch_bounds__(kA2Threads, 1)
                 float sc[2 * kA2Block][4];
                 tc_fence_after();
                 uint32_t rr[32];
-#pragma unroll
-                for (int b = 0; b < kA2Block; ++b)   // page b's 16 key columns
-                    a2_tmem_ld_16x256b_x2(tS + ((uint32_t)(32 * wig) << 16) + 32u * b, rr + 8 * b);
+                a2_tmem_ld_16x256b_x8(tS + ((uint32_t)(32 * wig) << 16), rr);
                 tmem_ld_wait();
 #pragma unroll
                 for (int nt = 0; nt < 2 * kA2Block; ++nt)
@@ -574,7 +592,7 @@ __global__ void __launch_bounds__(kA2Threads, 1)
 #pragma unroll
                 for (int b = 0; b < kA2Block; ++b) {
                     if (b < nb) {
-                        const uint32_t vbox = kreg + (uint32_t)b * kA2PageBytes + 2048;   // page b's V rows
+                        const uint32_t vbox = kreg + (uint32_t)b * kA2PageBytes + 1024;   // page b's V rows 0-7
                         // P (rows a / b x the page's 16 keys) as the A fragment of PV
                         const uint32_t pa0 = pack_f2bf(sc[2 * b][0], sc[2 * b][1]);
                         const uint32_t pa1 = pack_f2bf(sc[2 * b][2], sc[2 * b][3]);
@@ -583,7 +601,7 @@ __global__ void __launch_bounds__(kA2Threads, 1)
 #pragma unroll
                         for (int q2 = 0; q2 < 4; ++q2) {   // dims 16 q2 .. 16 q2 + 15
                             uint32_t b0, b1, b2, b3;
-                            ldsm_x4_trans(vbox + v_key * 128u + ((((uint32_t)(2 * q2) + v_hi) ^ sw) << 4), b0, b1, b2, b3);
+                            ldsm_x4_trans(vbox + v_row + ((((uint32_t)(2 * q2) + v_hi) ^ sw) << 4), b0, b1, b2, b3);
                             mma_bf16_16816(o[2 * q2], pa0, pa1, pa2, pa3, b0, b1);
                             mma_bf16_16816(o[2 * q2 + 1], pa0, pa1, pa2, pa3, b2, b3);
                         }
@@ -855,16 +873,17 @@ __global__ void __launch_bounds__(32 * kA2MergeWarps) attn2_merge_kernel(const A
 
 int encode_kv_map(const uint16_t *kv_cache, int64_t num_pages, int nkv, CUtensorMap *m)
 {
-    // the cache [pages * nkv][16 slots][2 halves][64] seen with the half
-    // dimension outside the slot dimension: dim 0 = 64 elements of a half,
-    // dim 1 = slot (256 B apart), dim 2 = K / V half (128 B apart), dim 3 =
-    // (page, KV head).  A {64, 16, 2, 1} box is one page of one KV head in
-    // shared memory as its 16 K rows, then its 16 V rows, 128 bytes each, swizzled
-    const cuuint64_t dims[4] = {64, (cuuint64_t)kPageSlots, 2, (cuuint64_t)num_pages * nkv};
-    const cuuint64_t strides[3] = {256, 128, (cuuint64_t)kPageSlots * kSlotWidth * 2};
-    const cuuint32_t box[4] = {64, (cuuint32_t)kPageSlots, 2, 1};
-    const cuuint32_t es[4] = {1, 1, 1, 1};
-    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, (void *)kv_cache, dims, strides, box, es,
+    // the cache [pages * nkv][2][8 slots][2 halves][64] seen as dim 0 = 64
+    // elements of a half, dim 1 = slot % 8 (256 B apart), dim 2 = K / V half
+    // (128 B apart), dim 3 = slot / 8 (2 KB apart), dim 4 = (page, KV head).
+    // A {64, 8, 2, 2, 1} box is one page of one KV head in shared memory as
+    // K of slots 0-7, V of slots 0-7, K of slots 8-15, V of slots 8-15, 128
+    // bytes a row, swizzled
+    const cuuint64_t dims[5] = {64, 8, 2, 2, (cuuint64_t)num_pages * nkv};
+    const cuuint64_t strides[4] = {256, 128, 2048, (cuuint64_t)kPageSlots * kSlotWidth * 2};
+    const cuuint32_t box[5] = {64, 8, 2, 2, 1};
+    const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, (void *)kv_cache, dims, strides, box, es,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
                ? QKVF_OK
