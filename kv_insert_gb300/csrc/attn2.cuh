@@ -36,19 +36,30 @@
 
 namespace qkvf {
 
-constexpr int kA2Groups = 3;                              // groups of 4 compute warps
-constexpr int kA2ComputeWarps = 4 * kA2Groups;
-constexpr int kA2Threads = 32 * (kA2ComputeWarps + 1);   // the last warp produces
 constexpr int kA2Block = 4;                               // pages per softmax step (16 per page)
-constexpr int kA2TmemCols = 256;                          // one 64-column S tile per group
-constexpr int kA2RingBlocks = 12;
-constexpr int kA2Stages = kA2RingBlocks * kA2Block;       // pages in flight per CTA
-// ring slot k % stages always serves group (k / block) % groups: each group
-// waits on its own slots in order, so a full barrier's parity never aliases
-static_assert(kA2RingBlocks % kA2Groups == 0, "ring blocks must be a multiple of the groups");
-static_assert(32 % kA2Block == 0, "a block's table entries lie in one 32-entry chunk");
-static_assert(kA2Block == 4 && kA2Groups * 64 <= kA2TmemCols, "tcgen05 Q K^T: 4-page blocks of 64 keys");
 constexpr uint32_t kA2PageBytes = 4096;                   // one box: K 0-7, V 0-7, K 8-15, V 8-15
+static_assert(32 % kA2Block == 0, "a block's table entries lie in one 32-entry chunk");
+
+// The kernel's two shapes, by its groups of 4 compute warps (plus one
+// producer warp): 3 groups, a 12-block ring (192 KB) and one CTA per SM, the
+// default; 2 groups, a 4-block ring (64 KB) and two CTAs per SM, for a direct
+// launch whose (request, KV head) pairs outnumber the SMs (all of its CTAs in
+// one wave, 4 block chains per SM).
+template <int kG>
+struct A2Shape {
+    static constexpr int groups = kG;
+    static constexpr int compute_warps = 4 * kG;
+    static constexpr int threads = 32 * (compute_warps + 1);   // the last warp produces
+    static constexpr int ring_blocks = kG == 3 ? 12 : 4;
+    static constexpr int ctas_per_sm = kG == 3 ? 1 : 2;
+    static constexpr int tmem_cols = kG == 3 ? 256 : 128;      // one 64-column S tile per group
+    // ring slot k % stages always serves group (k / block) % groups: each group
+    // waits on its own slots in order, so a full barrier's parity never aliases
+    static_assert(ring_blocks % groups == 0, "ring blocks must be a multiple of the groups");
+    static_assert(kA2Block == 4 && groups * 64 <= tmem_cols, "tcgen05 Q K^T: 4-page blocks of 64 keys");
+};
+constexpr int kA2Groups = A2Shape<3>::groups;   // the default shape
+constexpr int kA2Threads = A2Shape<3>::threads;
 constexpr int kA2OStride = 68;                            // floats per row of the O partial
 constexpr int kA2MaxSplits = 16;
 constexpr int kA2AutoSplits = 8;   // the largest split chosen by default
@@ -78,12 +89,16 @@ struct A2Layout {
     uint32_t q, gate, ring, full, empty, sbar, tslot, o, m, l, flags, total;
 };
 
-// the groups' O partials overlay the ring: written only once every page has
-// been consumed and every copy has landed
-static_assert(kA2Groups * 64 * kA2OStride * 4 <= kA2Stages * kA2PageBytes, "O partials must fit the ring");
+// groups 1.. leave their O partials over the ring: written only once every
+// page has been consumed and every copy has landed
+static_assert((A2Shape<3>::groups - 1) * 64 * kA2OStride * 4 <= A2Shape<3>::ring_blocks * kA2Block * kA2PageBytes &&
+                  (A2Shape<2>::groups - 1) * 64 * kA2OStride * 4 <= A2Shape<2>::ring_blocks * kA2Block * kA2PageBytes,
+              "O partials must fit the ring");
 
+template <int kG>
 __host__ __device__ inline A2Layout a2_layout()
 {
+    using Sh = A2Shape<kG>;
     A2Layout L;
     uint32_t off = 0;
     L.q = off;
@@ -92,19 +107,19 @@ __host__ __device__ inline A2Layout a2_layout()
     off += 64 * 128;
     L.ring = off;
     L.o = off;
-    off += kA2Stages * kA2PageBytes;
+    off += Sh::ring_blocks * kA2Block * kA2PageBytes;
     L.full = off;
-    off += kA2RingBlocks * 8;
+    off += Sh::ring_blocks * 8;
     L.empty = off;
-    off += kA2RingBlocks * 8;
+    off += Sh::ring_blocks * 8;
     L.sbar = off;   // per group: its Q K^T (tcgen05) is done
-    off += kA2Groups * 8;
+    off += Sh::groups * 8;
     L.tslot = off;  // tensor-memory base address
     off += 8;
     L.m = off;
-    off += kA2Groups * 64 * 4;
+    off += Sh::groups * 64 * 4;
     L.l = off;
-    off += kA2Groups * 64 * 4;
+    off += Sh::groups * 64 * 4;
     L.flags = off;
     off += 16;
     L.total = off + 1024;   // alignment slack
@@ -151,15 +166,17 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t &r0, uint3
 }
 
 // named barrier 2 over the compute warps only
+template <int kG>
 __device__ __forceinline__ void a2_compute_bar_sync()
 {
-    asm volatile("bar.sync 2, %0;" ::"n"(32 * kA2ComputeWarps) : "memory");
+    asm volatile("bar.sync 2, %0;" ::"n"(32 * A2Shape<kG>::compute_warps) : "memory");
 }
 
 // named barrier 3 over every warp: the ring is drained and free
+template <int kG>
 __device__ __forceinline__ void a2_ring_done_sync()
 {
-    asm volatile("bar.sync 3, %0;" ::"n"(kA2Threads) : "memory");
+    asm volatile("bar.sync 3, %0;" ::"n"(A2Shape<kG>::threads) : "memory");
 }
 
 // named barrier 4 + grp over the 4 warps of compute group grp
@@ -168,17 +185,19 @@ __device__ __forceinline__ void a2_group_bar_sync(int grp)
     asm volatile("bar.sync %0, 128;" ::"r"(4 + grp) : "memory");
 }
 
+template <int kCols>
 __device__ __forceinline__ void a2_tmem_alloc(uint32_t slot_saddr)
 {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_saddr),
-                 "n"(kA2TmemCols)
+                 "n"(kCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
 }
 
+template <int kCols>
 __device__ __forceinline__ void a2_tmem_dealloc(uint32_t taddr)
 {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "n"(kA2TmemCols)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "n"(kCols)
                  : "memory");
 }
 
@@ -308,13 +327,15 @@ __device__ __forceinline__ void a2_finish_row8(const Attn2Params &p, int r, int 
 // over distributed shared memory.  true: no cluster; each CTA writes its
 // partial to its slot of the caller's workspace and attn2_merge_kernel, the
 // next grid on the stream, merges the S slots.
-template <bool kWorkspace>
-__global__ void __launch_bounds__(kA2Threads, 1)
+template <bool kWorkspace, int kG>
+__global__ void __launch_bounds__(A2Shape<kG>::threads, A2Shape<kG>::ctas_per_sm)
     attn2_kernel(const __grid_constant__ CUtensorMap tmKV, const Attn2Params p)
 {
+    using Sh = A2Shape<kG>;
+    constexpr int kGroupsN = Sh::groups, kComputeWarps = Sh::compute_warps, kRing = Sh::ring_blocks;
     extern __shared__ uint8_t a2_smem_dyn[];
     uint8_t *smem = a2_smem_dyn + ((1024u - (smem_u32(a2_smem_dyn) & 1023u)) & 1023u);
-    const A2Layout LY = a2_layout();
+    const A2Layout LY = a2_layout<kG>();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int S = p.splits;
     const uint32_t z = kWorkspace ? blockIdx.x : (S > 1 ? cluster_rank() : 0u);
@@ -328,17 +349,17 @@ __global__ void __launch_bounds__(kA2Threads, 1)
     volatile int *s_flags = reinterpret_cast<volatile int *>(smem + LY.flags);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kA2RingBlocks; ++s) {   // one full / empty pair per block of pages
+        for (int s = 0; s < kRing; ++s) {   // one full / empty pair per block of pages
             mbar_init(full0 + 8 * s, 1);
             mbar_init(empty0 + 8 * s, 4);   // the 4 warps of the group that owns the block
         }
-        for (int q = 0; q < kA2Groups; ++q) mbar_init(smem_u32(smem + LY.sbar) + 8 * q, 1);
+        for (int q = 0; q < kGroupsN; ++q) mbar_init(smem_u32(smem + LY.sbar) + 8 * q, 1);
         s_flags[0] = 0;
         s_flags[1] = 0;
         fence_barrier_init();
         griddep_launch_dependents();
     }
-    if (warp == 0) a2_tmem_alloc(smem_u32(smem + LY.tslot));
+    if (warp == 0) a2_tmem_alloc<Sh::tmem_cols>(smem_u32(smem + LY.tslot));
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -350,14 +371,14 @@ __global__ void __launch_bounds__(kA2Threads, 1)
     // on the length), and the compute warps' Q and gate tiles.
     const int32_t *bt = p.block_table + (size_t)r * p.max_blocks;
     int first_entry = 0;
-    if (warp == kA2ComputeWarps && p.window == 0 && (int)z + lane * S < p.max_blocks) first_entry = bt[z + lane * S];
+    if (warp == kComputeWarps && p.window == 0 && (int)z + lane * S < p.max_blocks) first_entry = bt[z + lane * S];
     const int L = p.context_lens[r];
-    if (warp < kA2ComputeWarps) {
+    if (warp < kComputeWarps) {
         // Q tile [64 rows][64 dims], row 8 i + j = token i, head 8 g + j;
         // 128-byte rows with the chunk XORed by row % 8 (as TMA would); the
         // same rows' gate heads for the finish (no global load at the tail)
         const int gate_col = kQPerKv * p.nkv * kHeadDim + 2 * p.nkv * kHeadDim;
-        for (int c = threadIdx.x; c < 512; c += 32 * kA2ComputeWarps) {
+        for (int c = threadIdx.x; c < 512; c += 32 * kComputeWarps) {
             const int row = c >> 3, cc = c & 7;
             const uint16_t *src = p.qkv + ((size_t)r * 8 + (row >> 3)) * p.N + (size_t)(8 * g + (row & 7)) * kHeadDim + 8 * cc;
             const uint4 qv = *reinterpret_cast<const uint4 *>(src);
@@ -377,7 +398,7 @@ __global__ void __launch_bounds__(kA2Threads, 1)
     const int first_mine = p_first + (int)z;
     const int npages = (len_ok && first_mine <= p_last) ? (p_last - first_mine) / S + 1 : 0;
 
-    if (warp == kA2ComputeWarps) {
+    if (warp == kComputeWarps) {
         // ---- produce: K and V boxes of this CTA's pages -------------------
         // The table entries come in 32 at a time (lane l holds page c + l of
         // chunk c), one chunk ahead of the copies, so no copy waits on a
@@ -404,7 +425,7 @@ __global__ void __launch_bounds__(kA2Threads, 1)
             }
             const int c_end = npages - c < 32 ? npages : c + 32;
             for (int k0 = c; k0 < c_end; k0 += kA2Block) {
-                const int jb = k0 / kA2Block, rb = jb % kA2RingBlocks, use = jb / kA2RingBlocks;
+                const int jb = k0 / kA2Block, rb = jb % kRing, use = jb / kRing;
                 const int nb = npages - k0 < kA2Block ? npages - k0 : kA2Block;
                 int ok = 1;
                 if (lane == 0) {
@@ -431,19 +452,19 @@ __global__ void __launch_bounds__(kA2Threads, 1)
                 atomicOr(&g_status, QKVF_STATUS_BAD_REQUEST);
             }
             if (s_flags[0]) {   // drain our copies before the ring is reused or we leave
-                const int first = issued > kA2RingBlocks ? issued - kA2RingBlocks : 0;
+                const int first = issued > kRing ? issued - kRing : 0;
                 for (int j = first; j < issued; ++j)
-                    bounded_wait(full0 + 8 * (j % kA2RingBlocks), (uint32_t)((j / kA2RingBlocks) & 1),
+                    bounded_wait(full0 + 8 * (j % kRing), (uint32_t)((j / kRing) & 1),
                                  s_flags, p.wait_limit_ns, false);
             }
         }
         __syncwarp();
-        a2_ring_done_sync();
+        a2_ring_done_sync<kG>();
     } else {
         // ---- compute: group grp = warp / 4 takes blocks grp, grp + G, ... ----
         const int tid = threadIdx.x;
         const int grp = warp >> 2, wig = warp & 3;   // group, warp in group (rows 16 wig ..)
-        a2_compute_bar_sync();   // the Q tile is in shared memory
+        a2_compute_bar_sync<kG>();   // the Q tile is in shared memory
         const int gq = lane >> 2, t = lane & 3;
         // tcgen05 Q K^T: the group's S tile [64 rows x 64 keys] in tensor memory
         // columns 64 grp.., rows 16 w .. 16 w + 15 in lanes 32 w .. 32 w + 15;
@@ -474,10 +495,10 @@ __global__ void __launch_bounds__(kA2Threads, 1)
 
         // blocks of up to kA2Block pages (16 kA2Block keys): one softmax
         // reduction and one rescale of O per block, independent mma chains
-        for (int k0 = grp * kA2Block; k0 < npages; k0 += kA2Groups * kA2Block) {
+        for (int k0 = grp * kA2Block; k0 < npages; k0 += kGroupsN * kA2Block) {
             const int nb = npages - k0 < kA2Block ? npages - k0 : kA2Block;   // same for every lane
-            const int jb = k0 / kA2Block, rb = jb % kA2RingBlocks;
-            const uint32_t ph = (uint32_t)((jb / kA2RingBlocks) & 1);
+            const int jb = k0 / kA2Block, rb = jb % kRing;
+            const uint32_t ph = (uint32_t)((jb / kRing) & 1);
             // the block's keys rise with its pages: the first and the last key
             // decide whether every row sees all of them
             const int key_first = (first_mine + k0 * S) * kPageSlots;
@@ -615,9 +636,9 @@ __global__ void __launch_bounds__(kA2Threads, 1)
         if (issuer && committed != observed)   // an abandoned wait: let the MMAs finish first
             bounded_wait(sbar, (uint32_t)((committed - 1) & 1), s_flags, p.wait_limit_ns, false);
         tc_fence_before();
-        a2_ring_done_sync();   // every group is past the ring; the producer has drained
+        a2_ring_done_sync<kG>();   // every group is past the ring; the producer has drained
         tc_fence_after();
-        if (warp == 0) a2_tmem_dealloc(*reinterpret_cast<volatile uint32_t *>(smem + LY.tslot));
+        if (warp == 0) a2_tmem_dealloc<Sh::tmem_cols>(*reinterpret_cast<volatile uint32_t *>(smem + LY.tslot));
         // whole-row sums across the four threads of a row
 #pragma unroll
         for (int off = 1; off <= 2; off <<= 1) {
@@ -641,27 +662,27 @@ __global__ void __launch_bounds__(kA2Threads, 1)
                 l_part[grp * 64 + rb] = l_b;
             }
         }
-        a2_compute_bar_sync();
+        a2_compute_bar_sync<kG>();
         if (grp == 0) {
-            float w_a[kA2Groups], w_b[kA2Groups];
+            float w_a[kGroupsN], w_b[kGroupsN];
             {
-                float mg_a[kA2Groups], mg_b[kA2Groups];
+                float mg_a[kGroupsN], mg_b[kGroupsN];
                 mg_a[0] = m_a;
                 mg_b[0] = m_b;
 #pragma unroll
-                for (int gg = 1; gg < kA2Groups; ++gg) {
+                for (int gg = 1; gg < kGroupsN; ++gg) {
                     mg_a[gg] = m_part[gg * 64 + ra];
                     mg_b[gg] = m_part[gg * 64 + rb];
                 }
                 float M_a = -INFINITY, M_b = -INFINITY;
 #pragma unroll
-                for (int gg = 0; gg < kA2Groups; ++gg) {
+                for (int gg = 0; gg < kGroupsN; ++gg) {
                     M_a = fmaxf(M_a, mg_a[gg]);
                     M_b = fmaxf(M_b, mg_b[gg]);
                 }
                 const float base_a = M_a == -INFINITY ? 0.f : M_a, base_b = M_b == -INFINITY ? 0.f : M_b;
 #pragma unroll
-                for (int gg = 0; gg < kA2Groups; ++gg) {
+                for (int gg = 0; gg < kGroupsN; ++gg) {
                     w_a[gg] = exp2f(mg_a[gg] - base_a);
                     w_b[gg] = exp2f(mg_b[gg] - base_b);
                 }
@@ -672,7 +693,7 @@ __global__ void __launch_bounds__(kA2Threads, 1)
             lt_a = lt_a + l_a * w_a[0];
             lt_b = lt_b + l_b * w_b[0];
 #pragma unroll
-            for (int gg = 1; gg < kA2Groups; ++gg) {
+            for (int gg = 1; gg < kGroupsN; ++gg) {
                 lt_a = lt_a + l_part[gg * 64 + ra] * w_a[gg];
                 lt_b = lt_b + l_part[gg * 64 + rb] * w_b[gg];
             }
@@ -686,7 +707,7 @@ __global__ void __launch_bounds__(kA2Threads, 1)
                 f2 = f2 + o[nd][2] * w_b[0];
                 f3 = f3 + o[nd][3] * w_b[0];
 #pragma unroll
-                for (int gg = 1; gg < kA2Groups; ++gg) {
+                for (int gg = 1; gg < kGroupsN; ++gg) {
                     const float *og = o_part + gg * (64 * kA2OStride);
                     const float2 va = *reinterpret_cast<const float2 *>(og + ra * kA2OStride + 8 * nd + 2 * t);
                     const float2 vb = *reinterpret_cast<const float2 *>(og + rb * kA2OStride + 8 * nd + 2 * t);
@@ -752,7 +773,7 @@ __global__ void __launch_bounds__(kA2Threads, 1)
         if (req_ok && table_ok && S == 1) {
             // one CTA holds the whole partial: 8 lanes per row, 4 rows per warp at a time
             const int sub = lane >> 3, j = lane & 7;
-            for (int base = 4 * warp; base < 64; base += 4 * (kA2ComputeWarps + 1)) {
+            for (int base = 4 * warp; base < 64; base += 4 * (kComputeWarps + 1)) {
                 const int row = base + sub;
                 const int rr = row < 64 ? row : 63;
                 const float4 oa = *reinterpret_cast<const float4 *>(o_part + rr * kA2OStride + 8 * j);
@@ -763,7 +784,7 @@ __global__ void __launch_bounds__(kA2Threads, 1)
         } else if (req_ok && table_ok) {
             const int rows = 64 / S;
             const uint32_t o_addr = smem_u32(o_part), m_addr = smem_u32(m_part), l_addr = smem_u32(l_part);
-            for (int i = warp; i < rows; i += kA2ComputeWarps + 1) {
+            for (int i = warp; i < rows; i += kComputeWarps + 1) {
                 const int row = (int)z * rows + i;
                 const __nv_bfloat162 gt = *reinterpret_cast<const __nv_bfloat162 *>(smem + LY.gate + row * 128 + 4 * lane);
                 // the ranks' partials in rank order (short loops: a fully unrolled
@@ -971,21 +992,25 @@ size_t a2_workspace_bytes(int num_reqs, int nkv, int splits)
 
 bool prepare_attn2_kernel()
 {
-    const int smem = (int)a2_layout().total;
-    return cudaFuncSetAttribute((const void *)attn2_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const int smem = (int)a2_layout<3>().total;
+    return cudaFuncSetAttribute((const void *)attn2_kernel<false, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 smem) == cudaSuccess &&
-           cudaFuncSetAttribute((const void *)attn2_kernel<false>,
+           cudaFuncSetAttribute((const void *)attn2_kernel<false, 3>,
                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
-           cudaFuncSetAttribute((const void *)attn2_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                smem) == cudaSuccess;
+           cudaFuncSetAttribute((const void *)attn2_kernel<true, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                smem) == cudaSuccess &&
+           cudaFuncSetAttribute((const void *)attn2_kernel<false, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)a2_layout<2>().total) == cudaSuccess;
 }
 
 // workspace == null: the cluster engine (splits 1..16, a power of two);
-// otherwise the split-KV engine over that workspace (splits 1..256)
+// otherwise the split-KV engine over that workspace (splits 1..256).  A
+// direct launch (one split, no workspace) with more (request, KV head) pairs
+// than SMs takes the two-CTA-per-SM shape, so all of its CTAs run in one wave.
 int launch_attn2(const uint16_t *qkv, const uint16_t *kv_cache, int64_t num_pages,
                  const int32_t *block_table, int max_blocks, const int32_t *context_lens, int num_reqs,
                  int N, int num_kv_heads, int window, float scale, float eps, uint16_t *out, int splits,
-                 void *workspace, void *stream)
+                 void *workspace, int sms, void *stream)
 {
     CUtensorMap m;
     int rc = encode_kv_map(kv_cache, num_pages, num_kv_heads, &m);
@@ -1008,8 +1033,9 @@ int launch_attn2(const uint16_t *qkv, const uint16_t *kv_cache, int64_t num_page
     prm.eps = eps;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)splits, (unsigned)num_kv_heads, (unsigned)num_reqs);
-    cfg.blockDim = dim3(kA2Threads, 1, 1);
-    cfg.dynamicSmemBytes = a2_layout().total;
+    const bool two_per_sm = !ws && splits == 1 && (int64_t)num_reqs * num_kv_heads > sms;
+    cfg.blockDim = dim3(two_per_sm ? A2Shape<2>::threads : A2Shape<3>::threads, 1, 1);
+    cfg.dynamicSmemBytes = two_per_sm ? a2_layout<2>().total : a2_layout<3>().total;
     cfg.stream = (cudaStream_t)stream;
     cudaLaunchAttribute attrs[2];
     int na = 0;
@@ -1025,8 +1051,9 @@ int launch_attn2(const uint16_t *qkv, const uint16_t *kv_cache, int64_t num_page
     ++na;
     cfg.attrs = attrs;
     cfg.numAttrs = (unsigned)na;
-    cudaError_t e = ws ? cudaLaunchKernelEx(&cfg, attn2_kernel<true>, m, prm)
-                       : cudaLaunchKernelEx(&cfg, attn2_kernel<false>, m, prm);
+    cudaError_t e = ws ? cudaLaunchKernelEx(&cfg, attn2_kernel<true, 3>, m, prm)
+                       : two_per_sm ? cudaLaunchKernelEx(&cfg, attn2_kernel<false, 2>, m, prm)
+                                    : cudaLaunchKernelEx(&cfg, attn2_kernel<false, 3>, m, prm);
     if (e == cudaSuccess && ws) {   // the merge, PDL-linked behind the partials
         cudaLaunchConfig_t mc = {};
         mc.gridDim = dim3(64 / kA2MergeWarps, (unsigned)num_kv_heads, (unsigned)num_reqs);
@@ -1064,7 +1091,7 @@ int attn2(const uint16_t *qkv, const uint16_t *kv_cache, int64_t num_pages,
     if (rc != QKVF_OK) return rc;
     const int splits = qkvf::attn2_splits_for(num_reqs, num_kv_heads, max_blocks, window, d->sms);
     return qkvf::launch_attn2(qkv, kv_cache, num_pages, block_table, max_blocks, context_lens,
-                              num_reqs, N, num_kv_heads, window, scale, eps, out, splits, nullptr, stream);
+                              num_reqs, N, num_kv_heads, window, scale, eps, out, splits, nullptr, d->sms, stream);
 }
 
 const char *attn2_unsupported(const uint16_t *qkv, const uint16_t *kv_cache, int64_t num_pages,
@@ -1097,7 +1124,7 @@ int attn2_launch_splits(const uint16_t *qkv, const uint16_t *kv_cache, int64_t n
     const int rc = qkvf::probe_device(&d);
     if (rc != QKVF_OK) return rc;
     return qkvf::launch_attn2(qkv, kv_cache, num_pages, block_table, max_blocks, context_lens,
-                              num_reqs, N, num_kv_heads, window, scale, eps, out, splits, nullptr, stream);
+                              num_reqs, N, num_kv_heads, window, scale, eps, out, splits, nullptr, d->sms, stream);
 }
 
 int attn2_splits(int num_reqs, int num_kv_heads, int max_blocks, int window)
@@ -1159,9 +1186,9 @@ int attn2_split_kv(const uint16_t *qkv, const uint16_t *kv_cache, int64_t num_pa
     }
     if (splits == 1)   // one CTA per (request, KV head) finishes its own rows: no partials to merge
         return qkvf::launch_attn2(qkv, kv_cache, num_pages, block_table, max_blocks, context_lens, num_reqs,
-                                  N, num_kv_heads, window, scale, eps, out, 1, nullptr, stream);
+                                  N, num_kv_heads, window, scale, eps, out, 1, nullptr, d->sms, stream);
     return qkvf::launch_attn2(qkv, kv_cache, num_pages, block_table, max_blocks, context_lens,
-                              num_reqs, N, num_kv_heads, window, scale, eps, out, splits, workspace, stream);
+                              num_reqs, N, num_kv_heads, window, scale, eps, out, splits, workspace, d->sms, stream);
 }
 
 }  // extern "C"

@@ -1800,7 +1800,8 @@ int attn2_split_kv_noalloc(const uint16_t *qkv, const uint16_t *kv_cache, int64_
         splits = qkvf::attn2_split_kv_splits_for(num_reqs, num_kv_heads, max_blocks, window, d->sms);
     if (splits == 1)   // the direct path: each CTA finishes its own rows, no scratch
         return qkvf::launch_attn2(qkv, kv_cache, num_pages, block_table, max_blocks, context_lens,
-                                  num_reqs, N, num_kv_heads, window, scale, eps, out, 1, nullptr, stream);
+                                  num_reqs, N, num_kv_heads, window, scale, eps, out, 1, nullptr, d->sms,
+                                  stream);
     if ((int64_t)num_reqs * num_kv_heads * splits > qkvf::kNoAllocSlots) return QKVF_ERR_SIZES;
     void *scratch = nullptr;
     rc = qkvf::noalloc_scratch(&scratch);

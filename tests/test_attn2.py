@@ -236,3 +236,41 @@ def test_attn2_split_kv_short_workspace_refused():
     with pytest.raises(qf.QkvFrontError):
         qf.attn2_split_kv(g["qkv"], g["kv_cache"], g["block_table"], g["context_lens"], ws[:-16],
                           splits=4)
+
+
+def test_attn2_two_ctas_per_sm_shape():
+    """A direct launch with more (request, KV head) pairs than SMs runs the
+    two-CTA-per-SM shape (2 compute groups, a 4-block ring): 160 requests of
+    mixed lengths with a window, one request too short and one with a table
+    entry outside the cache, through both entry points, against the oracle
+    and bitwise on a repeat."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    R = sms + 8
+    rng = np.random.default_rng(6600)
+    ctx = tuple(int(x) for x in rng.integers(8, 200, size=R))
+    w = wl.AttnWorkload("two_per_sm", R=R, num_kv_heads=1, context=ctx,
+                        num_pages=sum((c + 15) // 16 for c in ctx) + 8, seed=6601, window=40)
+    inp = wl.make_attn_inputs(w)
+    inp["context_lens"][3] = 5
+    inp["block_table"][7, (int(inp["context_lens"][7]) - 1) // 16] = w.num_pages + 3   # its last page: visible
+    g = _dev(inp)
+    fill = torch.full((8 * R, 512), 7.0, dtype=torch.bfloat16, device="cuda:0")
+    outs = []
+    for _ in range(2):
+        outs.append(qf.attn2(g["qkv"], g["kv_cache"], g["block_table"], g["context_lens"], out=fill.clone(),
+                             window=w.window, splits=1))
+    ws = torch.zeros(qf.attn2_split_kv_workspace_bytes(R, 1, 1), dtype=torch.uint8, device="cuda:0")
+    outs.append(qf.attn2_split_kv(g["qkv"], g["kv_cache"], g["block_table"], g["context_lens"], ws,
+                                  out=fill.clone(), window=w.window, splits=1))
+    torch.cuda.synchronize()
+    assert qf.status() == qf.STATUS_BAD_REQUEST
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    assert torch.equal(outs[0].view(torch.int16), outs[2].view(torch.int16))
+    got = wl.bits(outs[0].cpu())
+    seven = wl.bits(torch.tensor([7.0]).to(torch.bfloat16))[0]
+    assert np.all(got[24:32] == seven) and np.all(got[56:64] == seven)   # requests 3 and 7 skipped
+    ref, _ = _oracle(inp, w)
+    keep = np.ones(8 * R, dtype=bool)
+    keep[24:32] = False
+    keep[56:64] = False
+    assert_values(got[keep], ref[keep], what="attn2, two CTAs per SM")
