@@ -24,10 +24,12 @@
 // as four tcgen05.mma (M = 64 rows, N = 64 keys, K = 16; the keys' 8-row
 // groups 2 KB apart) into the group's 64 tensor-memory columns, the warps
 // read the scores back with tcgen05.ld in the mma.sync accumulator layout,
-// run the online softmax
-// (base 2; masks only near the causal / window edges) and P V with mma.sync,
-// P going from the score registers straight into the A fragments.  Each
-// group keeps its own (max, sum, O), folded into one per CTA in group order.
+// run the online softmax (base 2; masks only near the causal / window edges)
+// and P V with mma.sync, P going from the score registers straight into the
+// A fragments.  Each group keeps its own (max, sum, O), folded into one per
+// CTA in group order.  Two shapes of the kernel (A2Shape): 3 groups and a
+// 12-block ring, one CTA per SM; 2 groups and a 4-block ring, two CTAs per
+// SM, for a direct launch with more (request, KV head) pairs than SMs.
 // Cluster engine: the S CTAs of a (request, KV head) form a cluster and merge
 // their partials through distributed shared memory in rank order — no global
 // workspace, deterministic for a launch shape — then each rank finishes 64 / S
@@ -58,8 +60,6 @@ struct A2Shape {
     static_assert(ring_blocks % groups == 0, "ring blocks must be a multiple of the groups");
     static_assert(kA2Block == 4 && groups * 64 <= tmem_cols, "tcgen05 Q K^T: 4-page blocks of 64 keys");
 };
-constexpr int kA2Groups = A2Shape<3>::groups;   // the default shape
-constexpr int kA2Threads = A2Shape<3>::threads;
 constexpr int kA2OStride = 68;                            // floats per row of the O partial
 constexpr int kA2MaxSplits = 16;
 constexpr int kA2AutoSplits = 8;   // the largest split chosen by default
