@@ -15,10 +15,14 @@
 //
 // HBM-bound elementwise work: per token it reads the 9 nkv q/k heads and the
 // nkv v heads (contiguous in the row: 1280 nkv bytes) and its cos|sin row,
-// and writes the q/k heads back and 2 nkv slot halves.  A producer warp
-// copies each token's region and table row into a shared-memory ring with
-// 16-byte cp.async from its 32 lanes (up to ~100 KB in flight per CTA, two
-// CTAs per SM); consumer warps work from shared memory, 16 bytes per lane.
+// and writes the q/k heads back and 2 nkv slot halves.  With 16 KV heads or
+// more a token is two work items (halves of its head groups), dealt round
+// robin over the CTAs, so the busiest CTA holds at most half a token more
+// than the average.  A
+// producer warp copies each item's heads and table row into a shared-memory
+// ring with 16-byte cp.async from its 32 lanes (up to ~100 KB in flight per
+// CTA, two CTAs per SM); consumer warps work from shared memory, 16 bytes
+// per lane.
 // (A bulk copy per token costs the SM's TMA unit ~0.2 us whatever its size,
 // which set the pace at two copies per token; 32 lanes of cp.async do not.)
 
@@ -43,14 +47,45 @@ constexpr int kEpiThreads = 32 * (kEpiConsumerWarps + 1);   // warp 0 produces
 constexpr int kEpiMaxTokens = 1 << 24;
 constexpr int kEpiCtasPerSm = 2;
 constexpr int kEpiRingBudget = 100 * 1024;   // per CTA: two rings fit one SM
-constexpr int kEpiMaxSlots = 16;
+constexpr int kEpiMaxSlots = 24;
 
-// bytes of one token's ring slot: its q | k | v heads, its cos|sin row, and a
+__host__ __device__ inline int epi_groups(int nkv) { return ((kQPerKv + 2) * nkv + 7) >> 3; }
+
+// Work items per token: with 16 or more 8-head groups (16 KV heads and up) a
+// token is two items (its first ceil(groups / 2) groups, then the rest), so
+// the busiest CTA holds at most half a token more than the average one;
+// below that one item per token (halving then costs more in per-item
+// barriers and index round trips than it saves: 8 KV heads at 4096 tokens
+// 16.2 -> 20.9 us, at 16 KV heads and 8192 tokens 62.6 -> 59.5 us).
+__host__ __device__ inline int epi_parts(int nkv) { return epi_groups(nkv) >= 16 ? 2 : 1; }
+
+// the 8-head groups [lo, hi) of part `part` of a token
+__host__ __device__ inline void epi_part_groups(int nkv, int part, int *lo, int *hi)
+{
+    const int g = epi_groups(nkv);
+    if (epi_parts(nkv) == 1) {
+        *lo = 0;
+        *hi = g;
+        return;
+    }
+    const int half = (g + 1) >> 1;
+    *lo = part == 0 ? 0 : half;
+    *hi = part == 0 ? half : g;
+}
+
+// bytes of one item's ring slot: its heads (all of the token's q | k | v
+// region, or ceil(groups / 2) x 8 heads of it), its cos|sin row, and a
 // 32-byte header (position, slot, flags), rounded to 128 bytes
+__host__ __device__ inline uint32_t epi_part_bytes(int nkv)
+{
+    const int g = epi_groups(nkv);
+    const int heads = (kQPerKv + 2) * nkv;
+    return epi_parts(nkv) == 1 ? (uint32_t)heads * kHeadDim * 2 : (uint32_t)((g + 1) >> 1) * 8 * kHeadDim * 2;
+}
+
 __host__ __device__ inline uint32_t epi_slot_bytes(int nkv)
 {
-    const uint32_t region = (uint32_t)(kQPerKv + 2) * nkv * kHeadDim * 2;
-    return (region + kHeadDim * 4 + 32 + 127u) & ~127u;
+    return (epi_part_bytes(nkv) + kHeadDim * 4 + 32 + 127u) & ~127u;
 }
 
 __host__ __device__ inline int epi_slots(int nkv)
@@ -163,13 +198,13 @@ __device__ __forceinline__ uint4 rope4_pairs(const uint64_t (&ev)[2], const uint
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// CTA b takes tokens b, b + G, b + 2G, ... (G = gridDim.x).  Warp 0 copies
-// each token's q | k | v region (contiguous in its row) and its cos|sin row
-// into a ring slot with 16-byte cp.async; warps 1..8 take the token's heads in
-// groups of 8 (lane l: head 8 g + l / 4, columns 8c..8c+7 and 32+8c..32+8c+7
-// with c = l % 4), norm and
-// rotate q / k heads in place in global memory and write k / v heads into the
-// cache slot.
+// Work item u is part u % P of token u / P (P = epi_parts: the whole token,
+// or its first ceil(groups / 2) 8-head groups and the rest); CTA b takes
+// items b, b + G, b + 2G, ... (G = gridDim.x).  Warp 0 copies each item's heads (contiguous in the token's
+// row) and its cos|sin row into a ring slot with 16-byte cp.async; warps
+// 1..8 take the item's heads in groups of 8 (lane l: head 8 g + l / 4,
+// columns 8c..8c+7 and 32+8c..32+8c+7 with c = l % 4), norm and rotate q / k
+// heads in place in global memory and write k / v heads into the cache slot.
 __global__ void __launch_bounds__(kEpiThreads, kEpiCtasPerSm) qknorm_rope_kv_insert_kernel(const EpiParams p)
 {
     extern __shared__ uint8_t epi_smem_dyn[];
@@ -177,7 +212,9 @@ __global__ void __launch_bounds__(kEpiThreads, kEpiCtasPerSm) qknorm_rope_kv_ins
     const int nkv = p.nkv;
     const uint32_t slot_bytes = epi_slot_bytes(nkv);
     const int nslots = epi_slots(nkv);
-    const uint32_t region = (uint32_t)(kQPerKv + 2) * nkv * kHeadDim * 2;
+    const uint32_t region = epi_part_bytes(nkv);   // the cos|sin row follows an item's heads
+    const int parts = epi_parts(nkv);
+    const int64_t U = (int64_t)p.T * parts;        // work items
     const uint32_t full0 = smem_u32(smem + nslots * slot_bytes);
     const uint32_t empty0 = full0 + 8 * kEpiMaxSlots;
     volatile int *s_abort = reinterpret_cast<volatile int *>(smem + nslots * slot_bytes + 16 * kEpiMaxSlots);
@@ -190,7 +227,7 @@ __global__ void __launch_bounds__(kEpiThreads, kEpiCtasPerSm) qknorm_rope_kv_ins
         for (int s = 0; s < nslots; ++s) {
             // the 32 lanes' copies land (32) and lane 0's header (1)
             mbar_init(full0 + 8 * s, 33);
-            mbar_init(empty0 + 8 * s, (heads + 7) >> 3);   // one arrival per 8-head group
+            mbar_init(empty0 + 8 * s, kEpiConsumerWarps);   // one arrival per consumer warp
         }
         *s_abort = 0;
         fence_barrier_init();
@@ -200,23 +237,27 @@ __global__ void __launch_bounds__(kEpiThreads, kEpiCtasPerSm) qknorm_rope_kv_ins
     griddep_wait();   // qkv, indices and table are written by the kernels before this one
 
     if (warp == 0) {
-        // ---- produce: 32 tokens' indices per warp load, then each token's copies ----
-        // A token's q | k | v region needs no index, so its copy is issued
-        // before the index loads are first used: the data and the indices
-        // come in side by side.
+        // ---- produce: 32 items' indices per warp load, then each item's copies ----
+        // An item's heads need no index, so their copy is issued before the
+        // index loads are first used: the data and the indices come in side
+        // by side.
         unsigned bad = 0u;
         int i = 0;
         bool stop = false;
-        for (int64_t tb = blockIdx.x; tb < p.T && !stop; tb += 32 * G) {
-            const int64_t tl = tb + lane * G;
+        for (int64_t ub = blockIdx.x; ub < U && !stop; ub += 32 * G) {
+            const int64_t ul = ub + lane * G, tl = ul / parts;
             int64_t pos_l = -1, slot_l = -1;
-            if (tl < p.T) {
+            if (ul < U) {
                 pos_l = p.positions[tl];
                 slot_l = p.slots[tl];
             }
             for (int j = 0; j < 32; ++j, ++i) {
-                const int64_t t = tb + j * G;
-                if (t >= p.T) break;   // the same for every lane
+                const int64_t u = ub + j * G, t = u / parts;
+                if (u >= U) break;   // the same for every lane
+                int g_lo, g_hi;
+                epi_part_groups(nkv, (int)(u % parts), &g_lo, &g_hi);
+                const int h_end = 8 * g_hi < heads ? 8 * g_hi : heads;
+                const uint32_t bytes = (uint32_t)(h_end - 8 * g_lo) * kHeadDim * 2;
                 const int s = i % nslots, use = i / nslots;
                 int ok = 1;
                 if (lane == 0 && use > 0)
@@ -227,8 +268,9 @@ __global__ void __launch_bounds__(kEpiThreads, kEpiCtasPerSm) qknorm_rope_kv_ins
                 }
                 uint8_t *base = smem + (size_t)s * slot_bytes;
                 const uint32_t bar = full0 + 8 * s;
-                const uint8_t *src = reinterpret_cast<const uint8_t *>(p.qkv + (size_t)t * p.N);
-                for (uint32_t c = (uint32_t)lane; c < region / 16; c += 32)
+                const uint8_t *src =
+                    reinterpret_cast<const uint8_t *>(p.qkv + (size_t)t * p.N + (size_t)8 * g_lo * kHeadDim);
+                for (uint32_t c = (uint32_t)lane; c < bytes / 16; c += 32)
                     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(base) + 16 * c),
                                  "l"(src + 16 * c)
                                  : "memory");
@@ -249,7 +291,7 @@ __global__ void __launch_bounds__(kEpiThreads, kEpiCtasPerSm) qknorm_rope_kv_ins
                 asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
                 if (lane == 0) mbar_arrive(bar);   // the header
             }
-            if (tl < p.T)
+            if (ul < U)
                 bad |= (pos_l >= 0 && pos_l < p.cos_rows ? 0u : QKVF_STATUS_BAD_POSITION) |
                        (slot_l >= slot_end ? QKVF_STATUS_BAD_SLOT : 0u);
         }
@@ -258,19 +300,22 @@ __global__ void __launch_bounds__(kEpiThreads, kEpiCtasPerSm) qknorm_rope_kv_ins
         if (lane == 0 && bad != 0u) atomicOr(&g_status, bad);
     } else {
         // ---- consume: groups of 8 heads, 4 lanes x 32 bytes per head ------
-        // The CTA's (token, group) items are dealt round robin over the consumer
-        // warps across token boundaries, so a token with fewer groups than warps
-        // does not leave warps idle.  Every warp still waits on every token in
-        // order (the barrier parity never runs more than one phase ahead) and
-        // arrives on the token's empty barrier once per group it processed.
+        // The CTA's (item, group) pairs are dealt round robin over the consumer
+        // warps across item boundaries, so an item with fewer groups than warps
+        // does not leave warps idle.  Every warp waits on every item in order
+        // (the barrier parity never runs more than one phase ahead) and arrives
+        // once on the item's empty barrier after its groups of the item.
         const int cw = warp - 1, sub = lane >> 2, part = lane & 3;
-        const int groups8 = (heads + 7) >> 3;
         int i = 0;
-        int64_t first = 0;   // item index of this token's first group
-        for (int64_t t = blockIdx.x; t < p.T; t += G, ++i, first += groups8) {
+        int64_t first = 0;   // (item, group) index of this item's first group
+        for (int64_t u = blockIdx.x; u < U; u += G, ++i) {
+            const int64_t t = u / parts;
+            int g_lo, g_hi;
+            epi_part_groups(nkv, (int)(u % parts), &g_lo, &g_hi);
             const int s = i % nslots;
-            const int g0 = (int)(((int64_t)cw - first % kEpiConsumerWarps + kEpiConsumerWarps) %
-                                 kEpiConsumerWarps);
+            const int g0 = g_lo + (int)(((int64_t)cw - first % kEpiConsumerWarps + kEpiConsumerWarps) %
+                                        kEpiConsumerWarps);
+            first += g_hi - g_lo;
             const bool landed = mbar_try_wait(full0 + 8 * s, (uint32_t)((i / nslots) & 1)) ||
                                 bounded_wait(full0 + 8 * s, (uint32_t)((i / nslots) & 1), s_abort,
                                              p.wait_limit_ns, true);
@@ -287,12 +332,12 @@ __global__ void __launch_bounds__(kEpiThreads, kEpiCtasPerSm) qknorm_rope_kv_ins
                     const int64_t page = sl / kPageSlots, offs = sl % kPageSlots;
                     crow = p.kv_cache + ((page * nkv) * kPageSlots + offs) * kSlotWidth + 8 * part;
                 }
-                for (int grp = g0; grp < groups8; grp += kEpiConsumerWarps) {
+                for (int grp = g0; grp < g_hi; grp += kEpiConsumerWarps) {
                     // lane: head 8 grp + l / 4; bytes 16 c and 64 + 16 c of the head (c = l % 4)
                     const int h = grp * 8 + sub;
                     uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
                     if (h < heads) {
-                        const uint8_t *src = base + h * (kHeadDim * 2) + 16 * part;
+                        const uint8_t *src = base + (h - 8 * g_lo) * (kHeadDim * 2) + 16 * part;
                         v0 = *reinterpret_cast<const uint4 *>(src);
                         v1 = *reinterpret_cast<const uint4 *>(src + 64);
                     }
@@ -321,13 +366,10 @@ __global__ void __launch_bounds__(kEpiThreads, kEpiCtasPerSm) qknorm_rope_kv_ins
                         *reinterpret_cast<uint4 *>(dst) = v0;
                         *reinterpret_cast<uint4 *>(dst + 32) = v1;
                     }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(empty0 + 8 * s);
                 }
-            } else {
-                for (int grp = g0; grp < groups8; grp += kEpiConsumerWarps)
-                    if (lane == 0) mbar_arrive(empty0 + 8 * s);
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8 * s);
         }
     }
 }
@@ -370,9 +412,10 @@ const char *check_epi_args(uint16_t *qkv, const int64_t *positions, const int64_
 
 bool prepare_epi_kernel()
 {
+    uint32_t most = 0;   // the largest ring over every KV head count
+    for (int nkv = 1; nkv <= 64; ++nkv) most = epi_smem_bytes(nkv) > most ? epi_smem_bytes(nkv) : most;
     return cudaFuncSetAttribute((const void *)qknorm_rope_kv_insert_kernel,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)epi_smem_bytes(64)) == cudaSuccess;   // the largest ring (64 KV heads)
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most) == cudaSuccess;
 }
 
 int launch_epi(uint16_t *qkv, const int64_t *positions, const int64_t *slots, const float *cos_sin,
@@ -391,8 +434,8 @@ int launch_epi(uint16_t *qkv, const int64_t *positions, const int64_t *slots, co
     prm.N = N;
     prm.nkv = num_kv_heads;
     prm.wait_limit_ns = g_wait_limit_ns;
-    int64_t blocks = (int64_t)sms * kEpiCtasPerSm;   // CTAs per SM, each walking its tokens
-    if (blocks > T) blocks = T;
+    int64_t blocks = (int64_t)sms * kEpiCtasPerSm;   // CTAs per SM, each walking its items
+    if (blocks > (int64_t)T * epi_parts(num_kv_heads)) blocks = (int64_t)T * epi_parts(num_kv_heads);
     if (blocks < 1) blocks = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)blocks, 1, 1);
