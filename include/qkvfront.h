@@ -300,10 +300,11 @@ int attn2_splits(int num_reqs, int num_kv_heads, int max_blocks, int window);
  * attn2, split-KV engine: the same result as attn2 (same arguments, readings
  * and bad-request rule) with the pages a row sees split over `splits` CTAs
  * per (request, KV head) without clusters, so that few requests can still
- * cover every SM.  Two grids, PDL-linked on the stream: the first writes each
- * CTA's partial (row maxima, sums and unnormalised O, FP32) to its slot of
- * the caller's workspace; the second merges a row's slots in split order (a
- * fixed `splits` gives the same bits every time) and finishes the rows.
+ * cover every SM.  Two grids on the stream (the second PDL-linked when the
+ * first leaves SMs idle): the first writes each CTA's partial (row maxima,
+ * sums and unnormalised O, FP32) to its slot of the caller's workspace; the
+ * second merges a row's slots in split order (a fixed `splits` gives the
+ * same bits every time) and finishes the rows.
  *   splits          1 .. 256, or 0 for attn2_split_kv_splits' choice;
  *                   otherwise QKVF_ERR_VARIANT.
  *   workspace       device memory, 256-byte aligned, at least

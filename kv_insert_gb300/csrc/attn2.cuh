@@ -1054,14 +1054,19 @@ int launch_attn2(const uint16_t *qkv, const uint16_t *kv_cache, int64_t num_page
     cudaError_t e = ws ? cudaLaunchKernelEx(&cfg, attn2_kernel<true, 3>, m, prm)
                        : two_per_sm ? cudaLaunchKernelEx(&cfg, attn2_kernel<false, 2>, m, prm)
                                     : cudaLaunchKernelEx(&cfg, attn2_kernel<false, 3>, m, prm);
-    if (e == cudaSuccess && ws) {   // the merge, PDL-linked behind the partials
+    if (e == cudaSuccess && ws) {   // the merge, behind the partials
         cudaLaunchConfig_t mc = {};
         mc.gridDim = dim3(64 / kA2MergeWarps, (unsigned)num_kv_heads, (unsigned)num_reqs);
         mc.blockDim = dim3(32 * kA2MergeWarps, 1, 1);
         mc.stream = (cudaStream_t)stream;
+        // PDL lets the merge's CTAs start on SMs the page grid leaves idle;
+        // when it covers every SM they cannot start before its CTAs exit, and
+        // the plain stream order releases the merge sooner (one 32K request,
+        // 19 splits on 152 SMs: 20.6 -> 20.1 us a call)
+        const bool idle_sms = (int64_t)num_reqs * num_kv_heads * splits < sms;
         cudaLaunchAttribute ma;
         ma.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        ma.val.programmaticStreamSerializationAllowed = g_pdl ? 1 : 0;
+        ma.val.programmaticStreamSerializationAllowed = g_pdl && idle_sms ? 1 : 0;
         mc.attrs = &ma;
         mc.numAttrs = 1;
         e = cudaLaunchKernelEx(&mc, attn2_merge_kernel, prm);
