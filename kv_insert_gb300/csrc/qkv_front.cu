@@ -1749,29 +1749,17 @@ constexpr int kNoAllocSlots = 256;
 constexpr size_t kNoAllocBytes = (size_t)kNoAllocSlots * kA2WsSlotFloats * 4;
 static __device__ __align__(256) float g_a2_noalloc_scratch[(size_t)kNoAllocSlots * kA2WsSlotFloats];
 
-constexpr int kNoAllocMaxDevices = 64;
-std::mutex g_noalloc_mutex;
-void *g_noalloc_ptr[kNoAllocMaxDevices] = {};
-
-// The array's device address on the current device (host code only sees a
-// stand-in under its name), looked up once per device.
+// The array's device address in the current context (host code only sees a
+// stand-in under its name).  Looked up on every call: a cached address
+// would outlive a device reset, after which the module is loaded anew.
 int noalloc_scratch(void **ptr)
 {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_a2_noalloc_scratch) != cudaSuccess || !p) {
         (void)cudaGetLastError();
-        return QKVF_ERR_DEVICE;
+        return QKVF_ERR_CUDA;
     }
-    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (!g_noalloc_ptr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_a2_noalloc_scratch) != cudaSuccess || !p) {
-            (void)cudaGetLastError();
-            return QKVF_ERR_CUDA;
-        }
-        g_noalloc_ptr[dev] = p;
-    }
-    *ptr = g_noalloc_ptr[dev];
+    *ptr = p;
     return QKVF_OK;
 }
 
