@@ -274,3 +274,29 @@ def test_attn2_two_ctas_per_sm_shape():
     keep[24:32] = False
     keep[56:64] = False
     assert_values(got[keep], ref[keep], what="attn2, two CTAs per SM")
+
+
+def test_attn2_most_kv_heads():
+    """64 KV heads (512 q heads, out rows of 32768 columns): the cluster engine
+    at its own split and at two, the direct launch (192 pairs: the
+    two-CTA-per-SM shape) and the split-KV engine, against the oracle."""
+    w = wl.AttnWorkload("r3_nkv64", R=3, num_kv_heads=64, context=(8, 77, 300), num_pages=64,
+                        seed=6700)
+    inp = wl.make_attn_inputs(w)
+    g = _dev(inp)
+    outs = {
+        "attn2": qf.attn2(g["qkv"], g["kv_cache"], g["block_table"], g["context_lens"]),
+        "attn2 splits=2": qf.attn2(g["qkv"], g["kv_cache"], g["block_table"], g["context_lens"], splits=2),
+        "attn2 splits=1": qf.attn2(g["qkv"], g["kv_cache"], g["block_table"], g["context_lens"], splits=1),
+    }
+    S = qf.attn2_split_kv_splits(w.R, w.num_kv_heads, w.max_blocks(), w.window)
+    ws = _workspace(w.R, w.num_kv_heads, S)
+    outs[f"split-KV S={S}"] = qf.attn2_split_kv(g["qkv"], g["kv_cache"], g["block_table"],
+                                                g["context_lens"], ws)
+    torch.cuda.synchronize()
+    assert qf.status() == 0
+    ref, err = _oracle(inp, w)
+    assert err == 0
+    for what, out in outs.items():
+        assert out.shape == (24, 32768)
+        assert_values(wl.bits(out.cpu()), ref, what=what)

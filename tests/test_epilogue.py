@@ -85,6 +85,19 @@ def test_epilogue_token_counts(T):
     check(inp, 2, g, out_ref, cache_ref)
 
 
+@pytest.mark.parametrize("nkv", [4, 12, 16, 24, 64])
+@pytest.mark.parametrize("T", [3, 37])
+def test_epilogue_kv_head_counts(T, nkv):
+    """Head counts on both sides of the two-items-per-token rule (16 KV heads
+    and up) and the most the op accepts, at token counts far below the grid."""
+    w = wl.EpiWorkload(f"t{T}_nkv{nkv}", T=T, num_kv_heads=nkv, max_pos=1024, num_pages=16,
+                       seed=4200 + 100 * T + nkv)
+    inp = wl.make_epi_inputs(w)
+    g, st, out_ref, cache_ref, err, _ = run_both(inp, nkv)
+    assert st == 0 and err == 0
+    check(inp, nkv, g, out_ref, cache_ref)
+
+
 def test_epilogue_index_rules():
     w = wl.EpiWorkload("bad", T=40, num_kv_heads=1, max_pos=256, num_pages=8, seed=4100)
     inp = wl.make_epi_inputs(w)

@@ -130,6 +130,15 @@ def test_other_kv_head_counts(nkv):
     check_workload(w)
 
 
+@pytest.mark.parametrize("nkv,M", [(24, 9), (64, 2)])
+def test_many_kv_heads(nkv, M):
+    """Up to the most KV heads the front accepts (64: N = 73728, 1152 heads,
+    several waves of CTAs), with a ragged second token tile at M = 9."""
+    w = wl.Workload(f"m{M}_nkv{nkv}", M=M, num_kv_heads=nkv, max_pos=4096, num_pages=64,
+                    seed=2150 + nkv)
+    check_workload(w)
+
+
 def test_negative_slot_inserts_nothing():
     w = wl.Workload("pad", M=6, num_kv_heads=2, max_pos=1024, num_pages=16, seed=2201)
     inp = wl.make_inputs(w)
