@@ -68,8 +68,9 @@ PER_CONFIG = (["m1_nkv1_n1152", "m8_nkv8_n9216", "m16_nkv8_n9216_consecutive"]
 SPIN_CYCLES = 100_000   # ~50 us at 2 GHz: the region's graph is queued before it starts
 # rotated input copies span this many L2 sizes (set by --l2-multiple): at 3
 # back-to-back calls still found ~10 % of W in L2 (per-call DRAM reads over a
-# range of calls), at 10 every call reads all of its W from DRAM
-L2_MULTIPLE = 10
+# range of calls), at 10 ~3 % (with 3 stages of L2 prefetch per CTA), at 30
+# every call reads all of its W from DRAM
+L2_MULTIPLE = 30
 
 
 def parse_args(argv=None):
@@ -99,7 +100,7 @@ def parse_args(argv=None):
                     help="attn2 engine: clusters merging over DSMEM (the attn2 entry point, no "
                          "workspace) or split-KV over the whole GPU with partials in a workspace")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--l2-multiple", type=float, default=10.0,
+    ap.add_argument("--l2-multiple", type=float, default=30.0,
                     help="the rotated copies of the streamed input (W, qkv or the cache) span at least "
                          "this many L2 sizes")
     ap.add_argument("--ncu-range", type=int, default=0,

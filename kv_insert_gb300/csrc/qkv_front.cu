@@ -1161,7 +1161,7 @@ KernelFn kernel_for(int mt, bool tc)
     return mt == 8 ? (KernelFn)qkv_front_kernel<8, false> : (KernelFn)qkv_front_kernel<16, false>;
 }
 constexpr int kDefaultKB = 4;          // 64-k boxes per ring stage: 256 k, 32 KB of W
-constexpr int kDefaultL2Prefetch = 8;  // W stages prefetched into L2 before the PDL wait
+constexpr int kDefaultL2Prefetch = 3;  // W stages prefetched into L2 before the PDL wait
 constexpr bool kDefaultTC = false;     // consumer: tcgen05 (true) or mma.sync
 
 bool prepare_epi_kernel();
