@@ -21,8 +21,8 @@
 // than the average.  A
 // producer warp copies each item's heads and table row into a shared-memory
 // ring with 16-byte cp.async from its 32 lanes (up to ~100 KB in flight per
-// CTA, two CTAs per SM); consumer warps work from shared memory, 16 bytes
-// per lane.
+// CTA, two CTAs per SM; 48 KB and four CTAs per SM for 4 KV heads or fewer);
+// consumer warps work from shared memory, 16 bytes per lane.
 // (A bulk copy per token costs the SM's TMA unit ~0.2 us whatever its size,
 // which set the pace at two copies per token; 32 lanes of cp.async do not.)
 
@@ -42,12 +42,25 @@ struct EpiParams {
     int nkv;
 };
 
-constexpr int kEpiConsumerWarps = 8;
-constexpr int kEpiThreads = 32 * (kEpiConsumerWarps + 1);   // warp 0 produces
 constexpr int kEpiMaxTokens = 1 << 24;
-constexpr int kEpiCtasPerSm = 2;
-constexpr int kEpiRingBudget = 100 * 1024;   // per CTA: two rings fit one SM
 constexpr int kEpiMaxSlots = 24;
+
+// The kernel's two shapes, by their consumer warps (warp 0 produces): two
+// CTAs per SM with 8 consumer warps and 100 KB rings, the default; and for 4
+// KV heads or fewer, where a token is 5 KB or less and the per-token steps
+// (index loads, barriers) weigh most, four CTAs per SM with 4 consumer warps
+// and 48 KB rings once there are more tokens than the default's CTAs (4096
+// tokens at 1 / 2 / 4 KV heads: 9.30 -> 6.16, 9.87 -> 7.26, 11.49 -> 9.51
+// us a call; with 8 or 16 KV heads no shape wins everywhere).
+template <int kCW>
+struct EpiShape {
+    static constexpr int consumer_warps = kCW;
+    static constexpr int threads = 32 * (kCW + 1);
+    static constexpr int ctas_per_sm = kCW == 8 ? 2 : 4;
+    static constexpr int ring_budget = kCW == 8 ? 100 * 1024 : 48 * 1024;   // the CTAs' rings fit one SM
+    static_assert(kCW == 8 || kCW == 4, "two shapes");
+};
+constexpr int kEpiSmallNkv = 4;   // KV heads up to this take the four-CTA shape
 
 __host__ __device__ inline int epi_groups(int nkv) { return ((kQPerKv + 2) * nkv + 7) >> 3; }
 
@@ -88,16 +101,16 @@ __host__ __device__ inline uint32_t epi_slot_bytes(int nkv)
     return (epi_part_bytes(nkv) + kHeadDim * 4 + 32 + 127u) & ~127u;
 }
 
-__host__ __device__ inline int epi_slots(int nkv)
+__host__ __device__ inline int epi_slots(int nkv, int ring_budget)
 {
-    int n = kEpiRingBudget / (int)epi_slot_bytes(nkv);
+    int n = ring_budget / (int)epi_slot_bytes(nkv);
     return n < 2 ? 2 : (n > kEpiMaxSlots ? kEpiMaxSlots : n);
 }
 
-__host__ __device__ inline uint32_t epi_smem_bytes(int nkv)
+__host__ __device__ inline uint32_t epi_smem_bytes(int nkv, int ring_budget)
 {
     // slots, then full and empty barriers and the abort flag, plus alignment slack
-    return (uint32_t)epi_slots(nkv) * epi_slot_bytes(nkv) + 2 * kEpiMaxSlots * 8 + 16 + 128;
+    return (uint32_t)epi_slots(nkv, ring_budget) * epi_slot_bytes(nkv) + 2 * kEpiMaxSlots * 8 + 16 + 128;
 }
 
 // Packed FP32 pairs (Blackwell's f32x2 arithmetic): two IEEE round-to-nearest
@@ -202,16 +215,19 @@ __device__ __forceinline__ uint4 rope4_pairs(const uint64_t (&ev)[2], const uint
 // or its first ceil(groups / 2) 8-head groups and the rest); CTA b takes
 // items b, b + G, b + 2G, ... (G = gridDim.x).  Warp 0 copies each item's heads (contiguous in the token's
 // row) and its cos|sin row into a ring slot with 16-byte cp.async; warps
-// 1..8 take the item's heads in groups of 8 (lane l: head 8 g + l / 4,
+// 1..kCW take the item's heads in groups of 8 (lane l: head 8 g + l / 4,
 // columns 8c..8c+7 and 32+8c..32+8c+7 with c = l % 4), norm and rotate q / k
 // heads in place in global memory and write k / v heads into the cache slot.
-__global__ void __launch_bounds__(kEpiThreads, kEpiCtasPerSm) qknorm_rope_kv_insert_kernel(const EpiParams p)
+template <int kCW>
+__global__ void __launch_bounds__(EpiShape<kCW>::threads, EpiShape<kCW>::ctas_per_sm)
+    qknorm_rope_kv_insert_kernel(const EpiParams p)
 {
+    constexpr int kEpiConsumerWarps = kCW;
     extern __shared__ uint8_t epi_smem_dyn[];
     uint8_t *smem = epi_smem_dyn + ((128u - (smem_u32(epi_smem_dyn) & 127u)) & 127u);
     const int nkv = p.nkv;
     const uint32_t slot_bytes = epi_slot_bytes(nkv);
-    const int nslots = epi_slots(nkv);
+    const int nslots = epi_slots(nkv, EpiShape<kCW>::ring_budget);
     const uint32_t region = epi_part_bytes(nkv);   // the cos|sin row follows an item's heads
     const int parts = epi_parts(nkv);
     const int64_t U = (int64_t)p.T * parts;        // work items
@@ -412,10 +428,20 @@ const char *check_epi_args(uint16_t *qkv, const int64_t *positions, const int64_
 
 bool prepare_epi_kernel()
 {
-    uint32_t most = 0;   // the largest ring over every KV head count
-    for (int nkv = 1; nkv <= 64; ++nkv) most = epi_smem_bytes(nkv) > most ? epi_smem_bytes(nkv) : most;
-    return cudaFuncSetAttribute((const void *)qknorm_rope_kv_insert_kernel,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most) == cudaSuccess;
+    // each shape's largest ring over the KV head counts it takes
+    uint32_t most8 = 0, most4 = 0;
+    for (int nkv = kEpiSmallNkv + 1; nkv <= 64; ++nkv) {
+        const uint32_t b = epi_smem_bytes(nkv, EpiShape<8>::ring_budget);
+        most8 = b > most8 ? b : most8;
+    }
+    for (int nkv = 1; nkv <= kEpiSmallNkv; ++nkv) {
+        const uint32_t b = epi_smem_bytes(nkv, EpiShape<4>::ring_budget);
+        most4 = b > most4 ? b : most4;
+    }
+    return cudaFuncSetAttribute((const void *)qknorm_rope_kv_insert_kernel<8>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most8) == cudaSuccess &&
+           cudaFuncSetAttribute((const void *)qknorm_rope_kv_insert_kernel<4>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most4) == cudaSuccess;
 }
 
 int launch_epi(uint16_t *qkv, const int64_t *positions, const int64_t *slots, const float *cos_sin,
@@ -434,20 +460,28 @@ int launch_epi(uint16_t *qkv, const int64_t *positions, const int64_t *slots, co
     prm.N = N;
     prm.nkv = num_kv_heads;
     prm.wait_limit_ns = g_wait_limit_ns;
-    int64_t blocks = (int64_t)sms * kEpiCtasPerSm;   // CTAs per SM, each walking its items
+    // the four-CTA shape once the default's CTAs would hold more than one
+    // item each (below that a token's groups spread over 8 warps finish sooner)
+    const bool small = num_kv_heads <= kEpiSmallNkv &&
+                       (int64_t)T * epi_parts(num_kv_heads) > (int64_t)sms * EpiShape<8>::ctas_per_sm;
+    const int per_sm = small ? EpiShape<4>::ctas_per_sm : EpiShape<8>::ctas_per_sm;
+    int64_t blocks = (int64_t)sms * per_sm;   // CTAs per SM, each walking its items
     if (blocks > (int64_t)T * epi_parts(num_kv_heads)) blocks = (int64_t)T * epi_parts(num_kv_heads);
     if (blocks < 1) blocks = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)blocks, 1, 1);
-    cfg.blockDim = dim3(kEpiThreads, 1, 1);
-    cfg.dynamicSmemBytes = epi_smem_bytes(num_kv_heads);
+    cfg.blockDim = dim3(small ? EpiShape<4>::threads : EpiShape<8>::threads, 1, 1);
+    cfg.dynamicSmemBytes =
+        epi_smem_bytes(num_kv_heads, small ? EpiShape<4>::ring_budget : EpiShape<8>::ring_budget);
     cfg.stream = (cudaStream_t)stream;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr.val.programmaticStreamSerializationAllowed = g_pdl ? 1 : 0;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, qknorm_rope_kv_insert_kernel, prm) != cudaSuccess) {
+    const cudaError_t e = small ? cudaLaunchKernelEx(&cfg, qknorm_rope_kv_insert_kernel<4>, prm)
+                                : cudaLaunchKernelEx(&cfg, qknorm_rope_kv_insert_kernel<8>, prm);
+    if (e != cudaSuccess) {
         (void)cudaGetLastError();
         return QKVF_ERR_CUDA;
     }

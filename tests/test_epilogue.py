@@ -98,6 +98,25 @@ def test_epilogue_kv_head_counts(T, nkv):
     check(inp, nkv, g, out_ref, cache_ref)
 
 
+@pytest.mark.parametrize("nkv", [1, 2, 4])
+@pytest.mark.parametrize("T", [305, 1000, 2051])
+def test_epilogue_four_cta_shape(T, nkv):
+    """With 4 KV heads or fewer and more tokens than two CTAs per SM take,
+    the kernel runs its four-CTA-per-SM shape (4 consumer warps): against
+    the oracle, and bitwise on a repeat."""
+    w = wl.EpiWorkload(f"s{T}_nkv{nkv}", T=T, num_kv_heads=nkv, max_pos=8192,
+                       num_pages=(T + 15) // 16 + 64, seed=4400 + 10 * T + nkv)
+    inp = wl.make_epi_inputs(w)
+    g, st, out_ref, cache_ref, err, _ = run_both(inp, nkv)
+    assert st == 0 and err == 0
+    check(inp, nkv, g, out_ref, cache_ref)
+    g2 = {k: v.to("cuda:0") for k, v in inp.items()}
+    qf.qknorm_rope_kv_insert(g2["qkv"], g2["positions"], g2["slots"], g2["cos_sin"], g2["kv_cache"])
+    torch.cuda.synchronize()
+    assert torch.equal(g["qkv"].view(torch.int16), g2["qkv"].view(torch.int16))
+    assert torch.equal(g["kv_cache"].view(torch.int16), g2["kv_cache"].view(torch.int16))
+
+
 def test_epilogue_index_rules():
     w = wl.EpiWorkload("bad", T=40, num_kv_heads=1, max_pos=256, num_pages=8, seed=4100)
     inp = wl.make_epi_inputs(w)
