@@ -335,7 +335,7 @@ int attn2_split_kv_splits(int num_reqs, int num_kv_heads, int max_blocks, int wi
  * attn2_split_kv for callers that cannot allocate device memory: a plugin
  * whose host process owns every device allocation through its own pool, or
  * a decode step that must not risk cudaMalloc's implicit synchronisation or
- * a failed allocation mid-step.  The paper has no counterpart of this entry
+ * a failed allocation mid-step.  The pages have no counterpart of this entry
  * point.  Same arguments and result as attn2_split_kv without the workspace:
  * the partials go to a file-scope device array of the library, 256 slots of
  * 17152 bytes (4,390,912 bytes), which every GPU that loads the library holds
